@@ -1,0 +1,254 @@
+"""fp64 CPU oracle for the sorted-expert 4-bit gathered MoE layer (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  The CUDA library never imports, links or loads
+this package; only the tests, the smoke check of the entry module and the
+CPU-baseline leg of the benchmark do.  The arithmetic lives in ``oracle.c``
+(plain C, fp64), built with gcc on first use; each C function cites the
+passage of the pages it follows.  This wrapper only marshals numpy arrays.
+
+Parity status: every function here is pinned by the CPU test suite against
+values fixed by the pages and by mathematics (hand-decoded nibble words,
+brute-force ranks, closed forms of the projections, GELU limits and its
+known distance to the erf form, zero-weight and linearity invariants).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_oracle.so")
+_lib = None
+_lock = threading.Lock()
+
+OK, ERR_UNSORTED, ERR_RANGE = 0, 4, 5
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into _oracle.so (gcc -O2, OpenMP, no fast-math)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-ffp-contract=off", "-Wall", "-Wextra", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        i32, i64, f64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+        lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_f64.restype = f64
+        lib.oracle_nibble.argtypes = [ctypes.c_uint32, ctypes.c_int]
+        lib.oracle_nibble.restype = ctypes.c_int
+        lib.oracle_dequant.argtypes = [p, p, p, i64, i64, i64]
+        lib.oracle_dequant.restype = f64
+        lib.oracle_dequant_matrix.argtypes = [p, p, p, i64, i64, p]
+        lib.oracle_gelu_tanh.argtypes = [f64]
+        lib.oracle_gelu_tanh.restype = f64
+        lib.oracle_gelu_tanh_array.argtypes = [p, i64, p]
+        lib.oracle_round_bf16.argtypes = [f64]
+        lib.oracle_round_bf16.restype = f64
+        lib.oracle_round_bf16_array.argtypes = [p, i64, p]
+        lib.oracle_sort_assignments.argtypes = [p, i32, i32, i32, p, p, p]
+        lib.oracle_sort_assignments.restype = ctypes.c_int
+        lib.oracle_build_expert_tiles.argtypes = [p, i32, i32, i32, i32, p, p, p]
+        lib.oracle_build_expert_tiles.restype = ctypes.c_int
+        lib.oracle_expert_geglu.argtypes = [p, i32, i32, i32, p, p, p, p]
+        lib.oracle_geglu_slots.argtypes = [p, i32, i32, i32, p, p, p, p, p, p, i32, p]
+        lib.oracle_expert_down.argtypes = [p, i32, i32, i32, p, p, p, p]
+        lib.oracle_down_unsort.argtypes = [p, p, p, p, i32, i32, i32, i32, p, p, p, p, i32, p]
+        lib.oracle_moe_layer_tokens.argtypes = [p, p, p, i32, i32, i32, p, p, p, p, p, p, p,
+                                                i32, p]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a, a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def nibble(word: int, j: int) -> int:
+    return int(_load().oracle_nibble(ctypes.c_uint32(word), j))
+
+
+def bf16_to_f64(bits: int) -> float:
+    return float(_load().oracle_bf16_to_f64(bits))
+
+
+def dequant_matrix(packed, scales, biases) -> np.ndarray:
+    """Dequantised [N, K] fp64 matrix of one packed [N, K/8] tensor."""
+    packed, pp = _c(packed, np.uint32)
+    scales, ps = _c(scales, np.uint16)
+    biases, pb = _c(biases, np.uint16)
+    N, K = packed.shape[0], packed.shape[1] * 8
+    out = np.empty((N, K), np.float64)
+    _load().oracle_dequant_matrix(pp, ps, pb, N, K, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def gelu_tanh(z) -> np.ndarray:
+    z, pz = _c(np.atleast_1d(z), np.float64)
+    out = np.empty_like(z)
+    _load().oracle_gelu_tanh_array(pz, z.size, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def round_bf16(v) -> np.ndarray:
+    v, pv = _c(v, np.float64)
+    out = np.empty_like(v)
+    _load().oracle_round_bf16_array(pv, v.size, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def sort_assignments(topk_ids, E: int):
+    """-> (status, sorted_ids [A], perm [A], counts [E])."""
+    ids, pid = _c(topk_ids, np.int32)
+    T, k = ids.shape
+    A = T * k
+    sorted_ids = np.zeros(A, np.int32)
+    perm = np.zeros(A, np.int32)
+    counts = np.zeros(E, np.int32)
+    st = _load().oracle_sort_assignments(pid, T, k, E, sorted_ids.ctypes.data_as(ctypes.c_void_p),
+                                         perm.ctypes.data_as(ctypes.c_void_p),
+                                         counts.ctypes.data_as(ctypes.c_void_p))
+    return int(st), sorted_ids, perm, counts
+
+
+def max_tiles(A: int, E: int, BM: int) -> int:
+    """Upper bound on the descriptor count: floor(A/BM) + min(E, A)."""
+    return A // BM + min(E, A)
+
+
+def build_expert_tiles(sorted_ids, E: int, BM: int, max_t: int | None = None):
+    """-> (status, offsets [E+1], tiles [tile_count, 3], tile_count)."""
+    sid, ps = _c(sorted_ids, np.int32)
+    A = sid.size
+    if max_t is None:
+        max_t = max_tiles(A, E, BM)
+    offsets = np.zeros(E + 1, np.int32)
+    tiles = np.zeros((max(max_t, 1), 3), np.int32)
+    tc = np.zeros(1, np.int32)
+    st = _load().oracle_build_expert_tiles(ps, A, E, BM, max_t,
+                                           offsets.ctypes.data_as(ctypes.c_void_p),
+                                           tiles.ctypes.data_as(ctypes.c_void_p),
+                                           tc.ctypes.data_as(ctypes.c_void_p))
+    return int(st), offsets, tiles[: int(tc[0])].copy(), int(tc[0])
+
+
+def _weights(d, names):
+    arrs = []
+    for n in names:
+        dt = np.uint32 if n.startswith("W") else np.uint16
+        arrs.append(_c(d[n], dt))
+    return arrs
+
+
+def expert_geglu(x_row, e: int, d) -> np.ndarray:
+    """h = gelu_tanh(Wg[e] x) * (Wu[e] x) for one bf16-bits activation row."""
+    H, I = d["H"], d["I"]
+    (_, pW), (_, pS), (_, pB) = _weights(d, ["Wgu", "Sgu", "Bgu"])
+    x, px = _c(x_row, np.uint16)
+    h = np.empty(I, np.float64)
+    _load().oracle_expert_geglu(px, e, H, I, pW, pS, pB, h.ctypes.data_as(ctypes.c_void_p))
+    return h
+
+
+def geglu_slots(d, sorted_ids, perm, slots) -> np.ndarray:
+    """h rows [len(slots), I] (fp64) for sorted slots of workload dict ``d``."""
+    H, I, k = d["H"], d["I"], d["k"]
+    (_, pW), (_, pS), (_, pB) = _weights(d, ["Wgu", "Sgu", "Bgu"])
+    x, px = _c(d["x"], np.uint16)
+    sid, psid = _c(sorted_ids, np.int32)
+    pm, ppm = _c(perm, np.int32)
+    sl, psl = _c(slots, np.int32)
+    h = np.empty((sl.size, I), np.float64)
+    _load().oracle_geglu_slots(px, H, I, k, pW, pS, pB, psid, ppm, psl, sl.size,
+                               h.ctypes.data_as(ctypes.c_void_p))
+    return h
+
+
+def expert_down(h_row, e: int, d) -> np.ndarray:
+    H, I = d["H"], d["I"]
+    (_, pW), (_, pS), (_, pB) = _weights(d, ["Wd", "Sd", "Bd"])
+    h, ph = _c(h_row, np.float64)
+    o = np.empty(H, np.float64)
+    _load().oracle_expert_down(ph, e, H, I, pW, pS, pB, o.ctypes.data_as(ctypes.c_void_p))
+    return o
+
+
+def down_unsort(d, h, sorted_ids, perm, tokens, topk_weights=None) -> np.ndarray:
+    """y rows [len(tokens), H] from h [A, I] (sorted-slot order, fp64)."""
+    H, I, k = d["H"], d["I"], d["k"]
+    (_, pW), (_, pS), (_, pB) = _weights(d, ["Wd", "Sd", "Bd"])
+    h, ph = _c(h, np.float64)
+    sid, psid = _c(sorted_ids, np.int32)
+    pm, ppm = _c(perm, np.int32)
+    tw, ptw = _c(d["topk_weights"] if topk_weights is None else topk_weights, np.float32)
+    tk, ptk = _c(tokens, np.int32)
+    y = np.empty((tk.size, H), np.float64)
+    _load().oracle_down_unsort(ph, psid, ppm, ptw, sid.size, k, H, I, pW, pS, pB, ptk, tk.size,
+                               y.ctypes.data_as(ctypes.c_void_p))
+    return y
+
+
+def moe_layer_tokens(d, tokens, topk_weights=None, topk_ids=None) -> np.ndarray:
+    """y rows [len(tokens), H] by the direct per-token definition (no sort)."""
+    H, I, k = d["H"], d["I"], d["k"]
+    (_, pWgu), (_, pSgu), (_, pBgu), (_, pWd), (_, pSd), (_, pBd) = _weights(
+        d, ["Wgu", "Sgu", "Bgu", "Wd", "Sd", "Bd"])
+    x, px = _c(d["x"], np.uint16)
+    ids, pids = _c(d["topk_ids"] if topk_ids is None else topk_ids, np.int32)
+    tw, ptw = _c(d["topk_weights"] if topk_weights is None else topk_weights, np.float32)
+    tk, ptk = _c(tokens, np.int32)
+    y = np.empty((tk.size, H), np.float64)
+    _load().oracle_moe_layer_tokens(px, pids, ptw, k, H, I, pWgu, pSgu, pBgu, pWd, pSd, pBd, ptk,
+                                    tk.size, y.ctypes.data_as(ctypes.c_void_p))
+    return y
+
+
+def layer(d, slots=None, tokens=None):
+    """Sort, tiles-free sorted route for the listed slots/tokens (default: all).
+
+    Returns dict(sorted_ids, perm, counts, h (rows for ``slots``), y (rows for ``tokens``)).
+    y is computed from the fp64 h of every slot that feeds the listed tokens.
+    """
+    st, sorted_ids, perm, counts = sort_assignments(d["topk_ids"], d["E"])
+    if st != OK:
+        raise ValueError(f"oracle sort failed with status {st}")
+    A = sorted_ids.size
+    if slots is None:
+        slots = np.arange(A, dtype=np.int32)
+    if tokens is None:
+        tokens = np.arange(d["T"], dtype=np.int32)
+    tokens = np.asarray(tokens, np.int32)
+    slot_of = np.empty(A, np.int32)
+    slot_of[perm] = np.arange(A, dtype=np.int32)
+    need = np.unique(np.concatenate([np.asarray(slots, np.int32),
+                                     slot_of[(tokens[:, None] * d["k"]
+                                              + np.arange(d["k"])[None, :]).ravel()]]))
+    h_need = geglu_slots(d, sorted_ids, perm, need)
+    h_full = np.zeros((A, d["I"]), np.float64)
+    h_full[need] = h_need
+    y = down_unsort(d, h_full, sorted_ids, perm, tokens)
+    return dict(sorted_ids=sorted_ids, perm=perm, counts=counts,
+                h=h_full[np.asarray(slots, np.int32)], y=y, slots=np.asarray(slots, np.int32),
+                tokens=tokens)

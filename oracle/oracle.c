@@ -1,0 +1,345 @@
+/*
+ * fp64 CPU oracle for the sorted-expert 4-bit gathered MoE layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path may call, link or
+ * load this file: only the test suite, the smoke check of the entry module
+ * and the CPU-baseline leg of the benchmark use it.  It shares no code,
+ * header, table or helper with the CUDA library; both sides read the same
+ * seeded inputs and nothing else.
+ *
+ * It is written to be checked by eye against the method as the pages give
+ * it, not to be fast.  Sources (page title, then the part of the page):
+ *
+ *  [P3-What]   Layr-Labs/mlx PR #4 "opt-in Gemma 4 expert-QMM tile kernel
+ *              with parallel descriptor builder", section "What": contiguous
+ *              sorted indices; BM32 expert tiles; one-threadgroup descriptor
+ *              builder (per-expert binary search of the sorted range,
+ *              exclusive scan of per-expert tile counts, emission of the
+ *              descriptors); affine 4-bit group-64 weights; packed gate/up
+ *              [128, 1408, 352] and down [128, 2816, 88] geometry.
+ *  [P3-F2]     same page, review findings table, row F2, and the final
+ *              review wave: the builder verifies global sortedness by a scan
+ *              of adjacent pairs and reports a violation as zero tiles.
+ *  [P1-Miss]   SharpAI/SwiftLM issue #236 "compiled GeGLU product for
+ *              Gemma4 MoE experts", section "Still missing": the MoE expert
+ *              activation is geluApproximate(x_gate) * x_up.
+ *  [P1-Main]   same page, "Already on main": weightedExpertSum, the
+ *              router-weighted sum of each token's expert outputs.
+ *  [P3-Meas]   Layr-Labs/mlx PR #4, "Measured standing": direct weighted
+ *              un-sort back to token order.
+ *
+ * Readings where the pages are silent (each is also listed in the design
+ * notes of the repository):
+ *  - flat assignment index a = t*k + j; the sort is stable, ties between
+ *    equal expert ids keep ascending a;
+ *  - packed gate/up rows: gate = rows [0, I), up = rows [I, 2I);
+ *  - nibble j of a uint32 word is bits 4j..4j+3 (lowest nibble first),
+ *    w = scale * q + bias with the group g = k / 64;
+ *  - geluApproximate is the tanh form 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3)))
+ *    (Hendrycks & Gimpel, "Gaussian Error Linear Units", 2016);
+ *  - tile descriptors are {expert, row_begin, rows} with experts ascending,
+ *    remainder rows forming one short tile;
+ *  - self-check outcome: tile_count = 0 and a status code, out-of-range ids
+ *    (5) reported in preference to order violations (4).
+ *
+ * Everything is fp64: no intermediate (not even h) is rounded.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { ORACLE_OK = 0, ORACLE_ERR_UNSORTED = 4, ORACLE_ERR_RANGE = 5 };
+
+/* bf16 bit pattern -> exact double */
+double oracle_bf16_to_f64(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Nibble j (0..7) of a packed word, lowest nibble first [P3-What; reading]. */
+int oracle_nibble(uint32_t word, int j) { return (int)((word >> (4 * j)) & 0xFu); }
+
+/*
+ * Dequantised weight W[n][kk] of one matrix whose rows are `K` wide:
+ * w = scale[n][kk/64] * q + bias[n][kk/64]  [P3-What: affine, 4-bit, gs=64].
+ */
+double oracle_dequant(const uint32_t *packed, const uint16_t *scales, const uint16_t *biases,
+                      int64_t K, int64_t n, int64_t kk) {
+  uint32_t word = packed[n * (K / 8) + kk / 8];
+  int q = oracle_nibble(word, (int)(kk % 8));
+  double s = oracle_bf16_to_f64(scales[n * (K / 64) + kk / 64]);
+  double b = oracle_bf16_to_f64(biases[n * (K / 64) + kk / 64]);
+  return s * (double)q + b;
+}
+
+/* The whole dequantised [N, K] matrix, element by element (test helper). */
+void oracle_dequant_matrix(const uint32_t *packed, const uint16_t *scales,
+                           const uint16_t *biases, int64_t N, int64_t K, double *out) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t kk = 0; kk < K; ++kk) out[n * K + kk] = oracle_dequant(packed, scales, biases, K, n, kk);
+}
+
+/* geluApproximate, tanh form [P1-Miss; Hendrycks & Gimpel 2016]. */
+double oracle_gelu_tanh(double z) {
+  const double c = sqrt(2.0 / 3.14159265358979323846);
+  return 0.5 * z * (1.0 + tanh(c * (z + 0.044715 * z * z * z)));
+}
+
+void oracle_gelu_tanh_array(const double *z, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_gelu_tanh(z[i]);
+}
+
+/* Round a double to the nearest bf16 value, ties to even (test-input helper). */
+double oracle_round_bf16(double v) {
+  if (v == 0.0 || !isfinite(v)) return v;
+  int e;
+  double m = frexp(v, &e); /* v = m * 2^e, 0.5 <= |m| < 1 */
+  double r = nearbyint(ldexp(m, 8)); /* 8 significant bits; default mode is to-even */
+  return ldexp(r, e - 8);
+}
+
+/* ---- a1: flatten + stable sort by expert [P3-What: sorted indices] ---- */
+
+typedef struct {
+  int32_t id;
+  int32_t a;
+} oracle_pair;
+
+static int pair_cmp(const void *pa, const void *pb) {
+  const oracle_pair *x = (const oracle_pair *)pa, *y = (const oracle_pair *)pb;
+  if (x->id != y->id) return x->id < y->id ? -1 : 1;
+  return x->a < y->a ? -1 : (x->a > y->a);
+}
+
+/*
+ * sorted_ids[s] = expert of sorted slot s, perm[s] = flat index a = t*k + j
+ * it came from, counts[e] = number of assignments to expert e.  The key is
+ * (expert, a), so the order is total and equals a stable sort by expert.
+ * Returns ORACLE_ERR_RANGE (and writes nothing) if an id is outside [0, E).
+ */
+int oracle_sort_assignments(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
+                            int32_t *sorted_ids, int32_t *perm, int32_t *counts) {
+  int64_t A = (int64_t)T * k;
+  for (int64_t a = 0; a < A; ++a)
+    if (topk_ids[a] < 0 || topk_ids[a] >= E) return ORACLE_ERR_RANGE;
+  oracle_pair *p = (oracle_pair *)malloc(sizeof(oracle_pair) * (size_t)(A > 0 ? A : 1));
+  for (int64_t a = 0; a < A; ++a) {
+    p[a].id = topk_ids[a];
+    p[a].a = (int32_t)a;
+  }
+  qsort(p, (size_t)A, sizeof(oracle_pair), pair_cmp);
+  for (int32_t e = 0; e < E; ++e) counts[e] = 0;
+  for (int64_t s = 0; s < A; ++s) {
+    sorted_ids[s] = p[s].id;
+    perm[s] = p[s].a;
+    counts[p[s].id] += 1;
+  }
+  free(p);
+  return ORACLE_OK;
+}
+
+/* ---- a2: offsets, tile descriptors, self-check [P3-What; P3-F2] ---- */
+
+/* first s with sorted_ids[s] >= e (binary search of the sorted range) */
+static int32_t lower_bound_i32(const int32_t *v, int32_t n, int32_t key) {
+  int32_t lo = 0, hi = n;
+  while (lo < hi) {
+    int32_t mid = lo + (hi - lo) / 2;
+    if (v[mid] < key)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+/*
+ * Self-check then build:
+ *   offsets[e] = lower_bound(sorted_ids, e) for e in [0, E], offsets[E] = A;
+ *   per expert ceil(c_e / BM) tiles, numbered by an exclusive scan in expert
+ *   order; tile i = {e, offsets[e] + r*BM, min(BM, c_e - r*BM)} as three
+ *   int32 at tiles[3i .. 3i+2].
+ * On a violation nothing but tile_count (= 0) is written and the status is
+ * returned: ORACLE_ERR_RANGE if any id is outside [0, E), else
+ * ORACLE_ERR_UNSORTED if some adjacent pair has ids[s] > ids[s+1].
+ * Returns -1 if more than max_tiles descriptors would be needed.
+ */
+int oracle_build_expert_tiles(const int32_t *sorted_ids, int32_t A, int32_t E, int32_t BM,
+                              int32_t max_tiles, int32_t *offsets, int32_t *tiles,
+                              int32_t *tile_count) {
+  int range_bad = 0, order_bad = 0;
+  for (int32_t s = 0; s < A; ++s)
+    if (sorted_ids[s] < 0 || sorted_ids[s] >= E) range_bad = 1;
+  for (int32_t s = 0; s + 1 < A; ++s)
+    if (sorted_ids[s] > sorted_ids[s + 1]) order_bad = 1;
+  if (range_bad || order_bad) {
+    *tile_count = 0;
+    return range_bad ? ORACLE_ERR_RANGE : ORACLE_ERR_UNSORTED;
+  }
+  for (int32_t e = 0; e < E; ++e) offsets[e] = lower_bound_i32(sorted_ids, A, e);
+  offsets[E] = A;
+  int32_t next = 0; /* running exclusive scan of per-expert tile counts */
+  for (int32_t e = 0; e < E; ++e) {
+    int32_t c = offsets[e + 1] - offsets[e];
+    int32_t nt = (c + BM - 1) / BM;
+    if (next + nt > max_tiles) {
+      *tile_count = 0;
+      return -1;
+    }
+    for (int32_t r = 0; r < nt; ++r) {
+      int32_t rows = c - r * BM < BM ? c - r * BM : BM;
+      tiles[3 * (next + r) + 0] = e;
+      tiles[3 * (next + r) + 1] = offsets[e] + r * BM;
+      tiles[3 * (next + r) + 2] = rows;
+    }
+    next += nt;
+  }
+  *tile_count = next;
+  return ORACLE_OK;
+}
+
+/* ---- a3-a6: gathered gate/up projection and GeGLU product ---- */
+
+/*
+ * For one activation row x (length H, bf16 bits) and expert e:
+ *   g[n] = sum_kk Wgu[e][n][kk]     * x[kk],  n in [0, I)   (gate rows)
+ *   u[n] = sum_kk Wgu[e][I + n][kk] * x[kk]                  (up rows)
+ *   h[n] = gelu_tanh(g[n]) * u[n]                  [P1-Miss; P3-What]
+ */
+void oracle_expert_geglu(const uint16_t *x_row, int32_t e, int32_t H, int32_t I,
+                         const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                         double *h) {
+  const int64_t rows = 2 * (int64_t)I;
+  const uint32_t *P = Wgu + (int64_t)e * rows * (H / 8);
+  const uint16_t *S = Sgu + (int64_t)e * rows * (H / 64);
+  const uint16_t *B = Bgu + (int64_t)e * rows * (H / 64);
+  for (int32_t n = 0; n < I; ++n) {
+    double g = 0.0, u = 0.0;
+    for (int32_t kk = 0; kk < H; ++kk) {
+      double xv = oracle_bf16_to_f64(x_row[kk]);
+      g += oracle_dequant(P, S, B, H, n, kk) * xv;
+      u += oracle_dequant(P, S, B, H, (int64_t)I + n, kk) * xv;
+    }
+    h[n] = oracle_gelu_tanh(g) * u;
+  }
+}
+
+/*
+ * h rows for a list of sorted slots: slot s reads activation row
+ * x[perm[s] / k] and expert sorted_ids[s] (the gather of [P3-What]).
+ * h_out is [n_slots, I] in the order of `slots`.
+ */
+void oracle_geglu_slots(const uint16_t *x, int32_t H, int32_t I, int32_t k,
+                        const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                        const int32_t *sorted_ids, const int32_t *perm, const int32_t *slots,
+                        int32_t n_slots, double *h_out) {
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int32_t i = 0; i < n_slots; ++i) {
+    int32_t s = slots[i];
+    int32_t t = perm[s] / k;
+    oracle_expert_geglu(x + (int64_t)t * H, sorted_ids[s], H, I, Wgu, Sgu, Bgu,
+                        h_out + (int64_t)i * I);
+  }
+}
+
+/* ---- a7: down projection of one h row ---- */
+
+/* o[n] = sum_i Wd[e][n][i] * h[i], n in [0, H)  [P3-What: down geometry] */
+void oracle_expert_down(const double *h, int32_t e, int32_t H, int32_t I, const uint32_t *Wd,
+                        const uint16_t *Sd, const uint16_t *Bd, double *o) {
+  const uint32_t *P = Wd + (int64_t)e * H * (I / 8);
+  const uint16_t *S = Sd + (int64_t)e * H * (I / 64);
+  const uint16_t *B = Bd + (int64_t)e * H * (I / 64);
+  for (int32_t n = 0; n < H; ++n) {
+    double acc = 0.0;
+    for (int32_t i = 0; i < I; ++i) acc += oracle_dequant(P, S, B, I, n, i) * h[i];
+    o[n] = acc;
+  }
+}
+
+/* ---- a8: weighted un-sort [P1-Main; P3-Meas] ---- */
+
+/*
+ * y[t] = sum over the slots s whose perm[s] / k == t of
+ *        topk_weights[perm[s]] * Wd[sorted_ids[s]] . h[s]
+ * for the listed tokens; h is [A, I] in sorted-slot order, y_out is
+ * [n_tokens, H].  Each token's k terms are added in ascending j = perm[s] % k.
+ */
+void oracle_down_unsort(const double *h, const int32_t *sorted_ids, const int32_t *perm,
+                        const float *topk_weights, int32_t A, int32_t k, int32_t H, int32_t I,
+                        const uint32_t *Wd, const uint16_t *Sd, const uint16_t *Bd,
+                        const int32_t *tokens, int32_t n_tokens, double *y_out) {
+  int32_t *slot_of = (int32_t *)malloc(sizeof(int32_t) * (size_t)(A > 0 ? A : 1));
+  for (int32_t s = 0; s < A; ++s) slot_of[perm[s]] = s; /* inverse permutation */
+#pragma omp parallel
+  {
+    double *o = (double *)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t i = 0; i < n_tokens; ++i) {
+      int32_t t = tokens[i];
+      double *y = y_out + (int64_t)i * H;
+      for (int32_t n = 0; n < H; ++n) y[n] = 0.0;
+      for (int32_t j = 0; j < k; ++j) {
+        int32_t a = t * k + j;
+        int32_t s = slot_of[a];
+        oracle_expert_down(h + (int64_t)s * I, sorted_ids[s], H, I, Wd, Sd, Bd, o);
+        double w = (double)topk_weights[a];
+        for (int32_t n = 0; n < H; ++n) y[n] += w * o[n];
+      }
+    }
+    free(o);
+  }
+  free(slot_of);
+}
+
+/* ---- the whole layer, by its plain per-token definition (no sort) ---- */
+
+/*
+ * y[t] = sum_j w[t,j] * Wd[e] . ( gelu_tanh(Wg[e] x_t) * (Wu[e] x_t) ),
+ * e = topk_ids[t, j], for the listed tokens (y_out [n_tokens, H]).
+ */
+void oracle_moe_layer_tokens(const uint16_t *x, const int32_t *topk_ids,
+                             const float *topk_weights, int32_t k, int32_t H, int32_t I,
+                             const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                             const uint32_t *Wd, const uint16_t *Sd, const uint16_t *Bd,
+                             const int32_t *tokens, int32_t n_tokens, double *y_out) {
+#pragma omp parallel
+  {
+    double *h = (double *)malloc(sizeof(double) * (size_t)I);
+    double *o = (double *)malloc(sizeof(double) * (size_t)H);
+#pragma omp for schedule(dynamic, 1)
+    for (int32_t i = 0; i < n_tokens; ++i) {
+      int32_t t = tokens[i];
+      double *y = y_out + (int64_t)i * H;
+      for (int32_t n = 0; n < H; ++n) y[n] = 0.0;
+      for (int32_t j = 0; j < k; ++j) {
+        int32_t e = topk_ids[t * k + j];
+        oracle_expert_geglu(x + (int64_t)t * H, e, H, I, Wgu, Sgu, Bgu, h);
+        oracle_expert_down(h, e, H, I, Wd, Sd, Bd, o);
+        double w = (double)topk_weights[t * k + j];
+        for (int32_t n = 0; n < H; ++n) y[n] += w * o[n];
+      }
+    }
+    free(h);
+    free(o);
+  }
+}
+
+void oracle_round_bf16_array(const double *v, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(v[i]);
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

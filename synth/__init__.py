@@ -1,0 +1,212 @@
+"""Seeded synthetic inputs for the sorted-expert 4-bit gathered MoE layer.
+
+This module makes the layer's inputs and nothing else: bf16 activations,
+router choices (top-k expert ids plus softmax weights) and affine 4-bit
+group-64 quantised expert weights in the packed layout of the Gemma-4
+26B-A4B expert tensors (Layr-Labs/mlx PR #4, "What": packed gate/up
+[128, 1408, 352] and down [128, 2816, 88] uint32, 4-bit, group size 64).
+It serves the fp64 oracle and the CUDA library alike and holds none of the
+layer's arithmetic.  The generator itself is plain C (``synth.c``), built
+with gcc on first use, so the same inputs appear on any host.
+
+Workloads (all seed 0, one weight set shared by the four Gemma-shaped ones):
+
+=================  ===  ====  ===  ====  =  ===========================================
+name               E    H     I    T     k  router
+=================  ===  ====  ===  ====  =  ===========================================
+tiny               8    128   64   32    2  logits N(0,1), top-2, softmax
+decode             128  2816  704  4     8  logits N(0,1), top-8, softmax
+prefill_uniform    128  2816  704  512   8  logits N(0,1) (near-uniform load)
+prefill_skewed     128  2816  704  1024  8  logits N(0,1) + per-expert bias N(0,1.5)
+prefill_zipf       128  2816  704  2048  8  Zipf(1.1) over 120 ranked experts (8 never
+                                            chosen) via Gumbel top-8; 20 rows of x x20
+=================  ===  ====  ===  ====  =  ===========================================
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_LIB_PATH = os.path.join(_HERE, "_synth.so")
+_lib = None
+_lock = threading.Lock()
+
+WEIGHT_STD = 0.02
+
+CONFIGS = {
+    "tiny": dict(E=8, H=128, I=64, T=32, k=2, router="normal", weights="tiny"),
+    "decode": dict(E=128, H=2816, I=704, T=4, k=8, router="normal", weights="gemma"),
+    "prefill_uniform": dict(E=128, H=2816, I=704, T=512, k=8, router="normal", weights="gemma"),
+    "prefill_skewed": dict(E=128, H=2816, I=704, T=1024, k=8, router="biased", weights="gemma"),
+    "prefill_zipf": dict(E=128, H=2816, I=704, T=2048, k=8, router="zipf", weights="gemma"),
+}
+CONFIG_ORDER = ["tiny", "decode", "prefill_uniform", "prefill_skewed", "prefill_zipf"]
+
+# stream ids: one per tensor so that no two tensors share random numbers
+_WEIGHT_STREAMS = {"tiny": (101, 102), "gemma": (1001, 1002)}
+_X_STREAM, _LOGIT_STREAM, _BIAS_STREAM = 2000, 3000, 4000
+_ZIPF_PERM_STREAM, _GUMBEL_STREAM, _OUTLIER_STREAM = 5000, 6000, 7000
+
+
+def build(force: bool = False) -> str:
+    """Compile synth.c into _synth.so (gcc, OpenMP) if missing or stale."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-fno-fast-math",
+           "-Wall", "-Wextra", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u64, i64, i32, f64, f32, p = (ctypes.c_uint64, ctypes.c_int64, ctypes.c_int32,
+                                      ctypes.c_double, ctypes.c_float, ctypes.c_void_p)
+        lib.synth_u64.argtypes = [u64, u64, u64]
+        lib.synth_u64.restype = u64
+        lib.synth_uniform.argtypes = [u64, u64, u64]
+        lib.synth_uniform.restype = f64
+        lib.synth_normal.argtypes = [u64, u64, u64]
+        lib.synth_normal.restype = f64
+        lib.synth_normals_f64.argtypes = [u64, u64, i64, f64, p]
+        lib.synth_activations_bf16.argtypes = [u64, u64, i64, i64, p, i32, f32, p]
+        lib.synth_quantized_weights.argtypes = [u64, u64, i64, i64, i64, f64, p, p, p]
+        lib.synth_topk_softmax.argtypes = [p, i64, i32, i32, p, p]
+        lib.synth_zipf_scores.argtypes = [u64, u64, u64, i64, i32, f64, i32, p]
+        lib.synth_choose_rows.argtypes = [u64, u64, i32, i32, p]
+        lib.synth_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().synth_num_threads())
+
+
+def normals(seed: int, stream: int, n: int, std: float = 1.0) -> np.ndarray:
+    out = np.empty(n, np.float64)
+    _load().synth_normals_f64(seed, stream, n, std, _ptr(out))
+    return out
+
+
+def quantized_weights(seed: int, stream: int, E: int, N: int, K: int, std: float = WEIGHT_STD):
+    """(packed uint32 [E,N,K/8], scales bf16-bits uint16 [E,N,K/64], biases likewise)."""
+    if K % 64:
+        raise ValueError("K must be a multiple of 64")
+    packed = np.empty((E, N, K // 8), np.uint32)
+    scales = np.empty((E, N, K // 64), np.uint16)
+    biases = np.empty((E, N, K // 64), np.uint16)
+    _load().synth_quantized_weights(seed, stream, E, N, K, std, _ptr(packed), _ptr(scales),
+                                    _ptr(biases))
+    return packed, scales, biases
+
+
+def activations(seed: int, stream: int, rows: int, cols: int, outlier_rows=None,
+                outlier_scale: float = 1.0) -> np.ndarray:
+    """bf16 bits (uint16) [rows, cols]: N(0,1) in fp32, outlier rows scaled, then bf16."""
+    out = np.empty((rows, cols), np.uint16)
+    orow = np.ascontiguousarray(np.asarray(outlier_rows if outlier_rows is not None else [],
+                                           np.int32))
+    _load().synth_activations_bf16(seed, stream, rows, cols, _ptr(orow) if orow.size else None,
+                                   int(orow.size), float(outlier_scale), _ptr(out))
+    return out
+
+
+def topk_softmax(scores: np.ndarray, k: int):
+    scores = np.ascontiguousarray(scores, np.float64)
+    T, E = scores.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    _load().synth_topk_softmax(_ptr(scores), T, E, k, _ptr(ids), _ptr(w))
+    return ids, w
+
+
+def zipf_scores(seed: int, perm_stream: int, gumbel_stream: int, T: int, E: int, s: float,
+                n_active: int) -> np.ndarray:
+    out = np.empty((T, E), np.float64)
+    _load().synth_zipf_scores(seed, perm_stream, gumbel_stream, T, E, s, n_active, _ptr(out))
+    return out
+
+
+def choose_rows(seed: int, stream: int, n: int, k: int) -> np.ndarray:
+    out = np.empty(k, np.int32)
+    _load().synth_choose_rows(seed, stream, n, k, _ptr(out))
+    return out
+
+
+_weight_cache: dict = {}
+
+
+def weights(kind: str, E: int, H: int, I: int, seed: int = 0) -> dict:
+    """Expert weights: Wgu [E,2I,H/8] (gate rows 0..I-1, up rows I..2I-1), Sgu/Bgu
+    [E,2I,H/64]; Wd [E,H,I/8], Sd/Bd [E,H,I/64].  bf16 arrays hold raw bits (uint16)."""
+    key = (kind, E, H, I, seed)
+    if key in _weight_cache:
+        return _weight_cache[key]
+    s_gu, s_d = _WEIGHT_STREAMS[kind]
+    Wgu, Sgu, Bgu = quantized_weights(seed, s_gu, E, 2 * I, H)
+    Wd, Sd, Bd = quantized_weights(seed, s_d, E, H, I)
+    w = dict(Wgu=Wgu, Sgu=Sgu, Bgu=Bgu, Wd=Wd, Sd=Sd, Bd=Bd)
+    _weight_cache[key] = w
+    return w
+
+
+def router(name: str, T: int, E: int, k: int, seed: int = 0):
+    """(topk_ids int32 [T,k], topk_weights float32 [T,k]) for a workload's router."""
+    cfg = CONFIGS[name]
+    ci = CONFIG_ORDER.index(name)
+    if cfg["router"] == "normal":
+        scores = normals(seed, _LOGIT_STREAM + ci, T * E).reshape(T, E)
+    elif cfg["router"] == "biased":
+        z = normals(seed, _LOGIT_STREAM + ci, T * E).reshape(T, E)
+        b = normals(seed, _BIAS_STREAM + ci, E, std=1.5)
+        scores = z + b[None, :]
+    elif cfg["router"] == "zipf":
+        scores = zipf_scores(seed, _ZIPF_PERM_STREAM + ci, _GUMBEL_STREAM + ci, T, E, 1.1,
+                             E - 8)
+    else:
+        raise ValueError(cfg["router"])
+    return topk_softmax(scores, k)
+
+
+def make(name: str, seed: int = 0, T: int | None = None) -> dict:
+    """All inputs of one workload.  ``T`` overrides the token count (a prefix of the
+    same seeded streams is NOT guaranteed; it is a fresh draw of that size)."""
+    cfg = dict(CONFIGS[name])
+    if T is not None:
+        cfg["T"] = int(T)
+    ci = CONFIG_ORDER.index(name)
+    E, H, I, T, k = cfg["E"], cfg["H"], cfg["I"], cfg["T"], cfg["k"]
+    outliers = None
+    if cfg["router"] == "zipf":
+        n_out = int(round(0.01 * T))
+        outliers = choose_rows(seed, _OUTLIER_STREAM + ci, T, n_out)
+    x = activations(seed, _X_STREAM + ci, T, H, outliers, 20.0)
+    ids, tw = router(name, T, E, k, seed)
+    out = dict(name=name, E=E, H=H, I=I, T=T, k=k, x=x, topk_ids=ids, topk_weights=tw,
+               outlier_rows=outliers if outliers is not None else np.zeros(0, np.int32))
+    out.update(weights(cfg["weights"], E, H, I, seed))
+    return out
+
+
+def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
+    """Exact widening of bf16 bit patterns (uint16) to float64."""
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

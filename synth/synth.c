@@ -1,0 +1,247 @@
+/*
+ * Seeded synthetic inputs for the sorted-expert 4-bit gathered MoE layer.
+ *
+ * This file synthesises the *inputs* of the layer only: activations x,
+ * router choices (top-k expert ids and their softmax weights) and affine
+ * 4-bit group-64 quantised expert weights.  It holds none of the layer's
+ * own arithmetic (no dequantisation, no matmul, no GELU, no weighted sum):
+ * both the fp64 oracle and the CUDA library consume what it writes.
+ *
+ * Random numbers: a counter-based generator built on the splitmix64 output
+ * function (Steele, Lea & Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014).  Value i of stream s under seed S is
+ *     mix(key(S, s) + (i + 1) * 0x9E3779B97F4A7C15)
+ * with key(S, s) = mix(S * 0xD1B54A32D192ED03 + s).  Normals use the
+ * Box-Muller transform on uniforms 2i and 2i+1 (cosine branch only).
+ *
+ * Weight quantisation follows the recipe of the Gemma-4 26B-A4B expert
+ * layout on the Layr-Labs/mlx PR #4 page ("What": affine, 4-bit, group
+ * size 64): per group of 64 consecutive K elements, scale = (max-min)/15
+ * and bias = min, both stored as bf16; q = round((w - bias)/scale) clamped
+ * to [0, 15]; eight nibbles per uint32, the lowest nibble first.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static inline uint64_t sm_mix(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+
+static inline uint64_t sm_key(uint64_t seed, uint64_t stream) {
+  return sm_mix(seed * 0xD1B54A32D192ED03ull + stream);
+}
+
+static inline uint64_t sm_u64(uint64_t key, uint64_t i) {
+  return sm_mix(key + (i + 1ull) * 0x9E3779B97F4A7C15ull);
+}
+
+/* uniform in the open interval (0, 1) */
+static inline double sm_unif(uint64_t key, uint64_t i) {
+  return ((double)(sm_u64(key, i) >> 11) + 0.5) * (1.0 / 9007199254740992.0);
+}
+
+static inline double sm_normal(uint64_t key, uint64_t i) {
+  const double two_pi = 6.283185307179586476925286766559;
+  double u1 = sm_unif(key, 2ull * i);
+  double u2 = sm_unif(key, 2ull * i + 1ull);
+  return sqrt(-2.0 * log(u1)) * cos(two_pi * u2);
+}
+
+/* float -> bf16 bits, round to nearest even (inputs are finite here) */
+static inline uint16_t f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static inline float bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+uint64_t synth_u64(uint64_t seed, uint64_t stream, uint64_t i) {
+  return sm_u64(sm_key(seed, stream), i);
+}
+
+double synth_uniform(uint64_t seed, uint64_t stream, uint64_t i) {
+  return sm_unif(sm_key(seed, stream), i);
+}
+
+double synth_normal(uint64_t seed, uint64_t stream, uint64_t i) {
+  return sm_normal(sm_key(seed, stream), i);
+}
+
+/* n normals N(0, std) written as float64 */
+void synth_normals_f64(uint64_t seed, uint64_t stream, int64_t n, double std, double *out) {
+  uint64_t key = sm_key(seed, stream);
+#pragma omp parallel for schedule(static)
+  for (int64_t i = 0; i < n; ++i) out[i] = std * sm_normal(key, (uint64_t)i);
+}
+
+/*
+ * Activations x[rows, cols] as bf16: N(0,1) rounded to fp32; the rows listed
+ * in outlier_rows are multiplied by outlier_scale in fp32; then rounded to
+ * bf16 (nearest even).
+ */
+void synth_activations_bf16(uint64_t seed, uint64_t stream, int64_t rows, int64_t cols,
+                            const int32_t *outlier_rows, int32_t n_outlier, float outlier_scale,
+                            uint16_t *out) {
+  uint64_t key = sm_key(seed, stream);
+  unsigned char *is_out = (unsigned char *)calloc((size_t)(rows > 0 ? rows : 1), 1);
+  for (int32_t j = 0; j < n_outlier; ++j)
+    if (outlier_rows[j] >= 0 && outlier_rows[j] < rows) is_out[outlier_rows[j]] = 1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t c = 0; c < cols; ++c) {
+      float v = (float)sm_normal(key, (uint64_t)(r * cols + c));
+      if (is_out[r]) v = v * outlier_scale;
+      out[r * cols + c] = f32_to_bf16(v);
+    }
+  }
+  free(is_out);
+}
+
+/*
+ * Affine 4-bit group-64 quantised weights for `E` experts of `N` rows and
+ * `K` columns (K % 64 == 0): w ~ N(0, std) rounded to fp32, element
+ * (e, n, k) drawn at counter (e*N + n)*K + k of the stream.
+ *   packed[e, n, k/8]  nibble (k % 8) holds q(e, n, k)
+ *   scales[e, n, k/64], biases[e, n, k/64]  bf16
+ */
+void synth_quantized_weights(uint64_t seed, uint64_t stream, int64_t E, int64_t N, int64_t K,
+                             double std, uint32_t *packed, uint16_t *scales, uint16_t *biases) {
+  uint64_t key = sm_key(seed, stream);
+  const int64_t G = K / 64;
+  const int64_t rows = E * N;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    float w[64];
+    for (int64_t g = 0; g < G; ++g) {
+      float lo = 0.0f, hi = 0.0f;
+      for (int j = 0; j < 64; ++j) {
+        w[j] = (float)(std * sm_normal(key, (uint64_t)(r * K + g * 64 + j)));
+        if (j == 0 || w[j] < lo) lo = w[j];
+        if (j == 0 || w[j] > hi) hi = w[j];
+      }
+      uint16_t s16 = f32_to_bf16((hi - lo) / 15.0f);
+      uint16_t b16 = f32_to_bf16(lo);
+      float s = bf16_to_f32(s16), b = bf16_to_f32(b16);
+      scales[r * G + g] = s16;
+      biases[r * G + g] = b16;
+      for (int j8 = 0; j8 < 8; ++j8) {
+        uint32_t word = 0;
+        for (int t = 0; t < 8; ++t) {
+          uint32_t q = 0;
+          if (s != 0.0f) {
+            float v = rintf((w[j8 * 8 + t] - b) / s);
+            if (v < 0.0f) v = 0.0f;
+            if (v > 15.0f) v = 15.0f;
+            q = (uint32_t)v;
+          }
+          word |= q << (4 * t);
+        }
+        packed[r * (K / 8) + g * 8 + j8] = word;
+      }
+    }
+  }
+}
+
+/*
+ * Top-k of each row of scores[T, E] (descending, ties to the lower expert
+ * id) and the softmax over the k selected scores (fp64, stored fp32).
+ * Entries equal to -INFINITY are never selected while a finite one is left.
+ */
+void synth_topk_softmax(const double *scores, int64_t T, int32_t E, int32_t k,
+                        int32_t *topk_ids, float *topk_weights) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    const double *row = scores + t * E;
+    unsigned char used[1024];
+    memset(used, 0, sizeof(used));
+    double sel[1024];
+    for (int32_t j = 0; j < k; ++j) {
+      int32_t best = -1;
+      for (int32_t e = 0; e < E; ++e) {
+        if (used[e]) continue;
+        if (best < 0 || row[e] > row[best]) best = e;
+      }
+      used[best] = 1;
+      topk_ids[t * k + j] = best;
+      sel[j] = row[best];
+    }
+    double m = sel[0], z = 0.0;
+    for (int32_t j = 0; j < k; ++j) z += exp(sel[j] - m);
+    for (int32_t j = 0; j < k; ++j) topk_weights[t * k + j] = (float)(exp(sel[j] - m) / z);
+  }
+}
+
+/*
+ * Router scores for Zipf(s)-distributed expert popularity: a seeded
+ * permutation gives expert e the rank rank[e] in 1..E; p_e is proportional
+ * to rank^-s for ranks <= n_active and 0 beyond; per token the score is
+ * log p_e + Gumbel(0,1), so taking the top-k draws k experts without
+ * replacement with probabilities p.
+ */
+void synth_zipf_scores(uint64_t seed, uint64_t perm_stream, uint64_t gumbel_stream, int64_t T,
+                       int32_t E, double s, int32_t n_active, double *scores) {
+  int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)E);
+  double *logp = (double *)malloc(sizeof(double) * (size_t)E);
+  uint64_t pkey = sm_key(seed, perm_stream);
+  for (int32_t e = 0; e < E; ++e) order[e] = e;
+  for (int32_t e = E - 1; e > 0; --e) { /* Fisher-Yates */
+    int32_t j = (int32_t)(sm_u64(pkey, (uint64_t)e) % (uint64_t)(e + 1));
+    int32_t tmp = order[e];
+    order[e] = order[j];
+    order[j] = tmp;
+  }
+  double zsum = 0.0;
+  for (int32_t r = 1; r <= n_active; ++r) zsum += pow((double)r, -s);
+  for (int32_t r = 1; r <= E; ++r) {
+    int32_t e = order[r - 1];
+    logp[e] = (r <= n_active) ? log(pow((double)r, -s) / zsum) : -INFINITY;
+  }
+  uint64_t gkey = sm_key(seed, gumbel_stream);
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    for (int32_t e = 0; e < E; ++e) {
+      double u = sm_unif(gkey, (uint64_t)(t * E + e));
+      scores[t * E + e] = logp[e] - log(-log(u));
+    }
+  }
+  free(order);
+  free(logp);
+}
+
+/* k distinct rows of [0, n) chosen by a seeded partial Fisher-Yates shuffle */
+void synth_choose_rows(uint64_t seed, uint64_t stream, int32_t n, int32_t k, int32_t *out) {
+  int32_t *a = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  uint64_t key = sm_key(seed, stream);
+  for (int32_t i = 0; i < n; ++i) a[i] = i;
+  for (int32_t i = 0; i < k && i < n; ++i) {
+    int32_t j = i + (int32_t)(sm_u64(key, (uint64_t)i) % (uint64_t)(n - i));
+    int32_t tmp = a[i];
+    a[i] = a[j];
+    a[j] = tmp;
+    out[i] = a[i];
+  }
+  free(a);
+}
+
+int synth_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,357 @@
+"""Pins of the fp64 oracle to facts outside itself (CPU only).
+
+Each test checks the oracle against something the pages or mathematics fix:
+hand-decoded nibble words, a hand-worked sort and tile example, brute-force
+ranks, closed forms of the projections on hand-built weights, GELU limits and
+its known distance from the erf form, and the invariants of the weighted sum.
+A slip anywhere in the oracle (a dropped bias term, a transposed operand, a
+wrong nibble or group index, gate and up swapped, a wrong token index in the
+un-sort) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def bf16_bits(v: float) -> int:
+    """bf16 bit pattern of a value that bf16 represents exactly."""
+    u = np.array([v], np.float32).view(np.uint32)[0]
+    assert u & 0xFFFF == 0, v
+    return int(u >> 16)
+
+
+# ---------------------------------------------------------------- dequant
+
+
+def test_bf16_widening():
+    assert oracle.bf16_to_f64(0x3F80) == 1.0
+    assert oracle.bf16_to_f64(0xC000) == -2.0
+    assert oracle.bf16_to_f64(0x3F00) == 0.5
+    assert oracle.bf16_to_f64(0x0000) == 0.0
+
+
+def test_dequant_hand_decoded_words():
+    g = _golden("dequant_nibbles.json")
+    for case in g["cases"]:
+        word = int(case["word"], 16)
+        assert [oracle.nibble(word, j) for j in range(8)] == case["q"]
+        # one 64-wide group: this word in slot 0, zeros elsewhere
+        packed = np.zeros((1, 8), np.uint32)
+        packed[0, 0] = word
+        s = np.array([[int(case["scale_bits"], 16)]], np.uint16)
+        b = np.array([[int(case["bias_bits"], 16)]], np.uint16)
+        assert oracle.bf16_to_f64(int(s[0, 0])) == case["scale"]
+        assert oracle.bf16_to_f64(int(b[0, 0])) == case["bias"]
+        W = oracle.dequant_matrix(packed, s, b)
+        assert W.shape == (1, 64)
+        assert W[0, :8].tolist() == case["w"]
+        assert np.all(W[0, 8:] == case["bias"])
+
+
+def test_dequant_group_index_is_k_div_64():
+    # two groups with different affine pairs; nibble value = k % 16 everywhere
+    K = 128
+    word = 0x76543210
+    word2 = 0xFEDCBA98
+    packed = np.array([[word, word2] * (K // 16)], np.uint32)
+    s = np.array([[bf16_bits(0.5), bf16_bits(2.0)]], np.uint16)
+    b = np.array([[bf16_bits(-1.0), bf16_bits(3.0)]], np.uint16)
+    W = oracle.dequant_matrix(packed, s, b)
+    q = np.arange(K) % 16
+    assert np.array_equal(W[0, :64], 0.5 * q[:64] - 1.0)
+    assert np.array_equal(W[0, 64:], 2.0 * q[64:] + 3.0)
+
+
+# ---------------------------------------------------------------- GELU
+
+
+def test_gelu_special_values():
+    z = np.array([0.0, 10.0, -10.0, 30.0, -30.0])
+    g = oracle.gelu_tanh(z)
+    assert g[0] == 0.0
+    assert abs(g[1] - 10.0) < 1e-12 and abs(g[3] - 30.0) < 1e-12
+    assert abs(g[2]) < 1e-12 and abs(g[4]) < 1e-12
+
+
+def test_gelu_odd_part_identity():
+    # gelu(z) - gelu(-z) = z for z * Phi(z)-shaped activations
+    z = np.linspace(-6, 6, 1201)
+    g = oracle.gelu_tanh(z)
+    gm = oracle.gelu_tanh(-z)
+    assert np.max(np.abs((g - gm) - z)) < 1e-13
+
+
+def test_gelu_is_the_tanh_approximation_of_erf_gelu():
+    # the tanh form stays within 5e-4 of z*Phi(z) and differs from it by more than 4e-4
+    # somewhere: the erf form itself, or the tanh form with a wrong constant, fails
+    z = np.linspace(-8, 8, 32001)
+    exact = np.array([0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0))) for v in z])
+    d = np.abs(oracle.gelu_tanh(z) - exact)
+    assert d.max() < 5e-4
+    assert d.max() > 4e-4
+
+
+def test_round_bf16_ties_to_even():
+    v = np.array([1.0 + 2.0**-8, 1.0 + 3 * 2.0**-8, -(1.0 + 2.0**-8), 1.0 + 2.0**-9, 3.0])
+    r = oracle.round_bf16(v)
+    assert r.tolist() == [1.0, 1.0 + 2.0**-6, -1.0, 1.0, 3.0]
+
+
+# ---------------------------------------------------------------- sort
+
+
+def test_sort_hand_worked_example():
+    g = _golden("tiles_example.json")["sort_example"]
+    st, sid, perm, counts = oracle.sort_assignments(np.array(g["topk_ids"]), g["E"])
+    assert st == oracle.OK
+    assert sid.tolist() == g["sorted_ids"]
+    assert perm.tolist() == g["perm"]
+    assert counts.tolist() == g["counts"]
+
+
+def _brute_rank(ids):
+    A = ids.size
+    key = [(int(ids[a]), a) for a in range(A)]
+    return np.array([sum(1 for b in range(A) if key[b] < key[a]) for a in range(A)])
+
+
+@pytest.mark.parametrize("T,k,E,seed", [(1, 1, 1, 0), (7, 3, 5, 1), (16, 2, 1, 2),
+                                        (20, 4, 16, 3), (33, 8, 128, 4), (9, 2, 256, 5)])
+def test_sort_against_brute_force_ranks(T, k, E, seed):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    if seed == 2:
+        ids[:] = 0  # every assignment on one expert
+    st, sid, perm, counts = oracle.sort_assignments(ids, E)
+    assert st == oracle.OK
+    flat = ids.ravel()
+    rank = _brute_rank(flat)
+    assert sorted(rank.tolist()) == list(range(flat.size))
+    for a in range(flat.size):
+        assert sid[rank[a]] == flat[a]
+        assert perm[rank[a]] == a
+    assert np.array_equal(counts, np.bincount(flat, minlength=E))
+    assert counts.sum() == flat.size
+    assert np.array_equal(np.sort(perm), np.arange(flat.size))  # bijection
+
+
+def test_sort_rejects_out_of_range_ids():
+    ids = np.array([[0, 1], [2, 3]], np.int32)
+    assert oracle.sort_assignments(ids, 3)[0] == oracle.ERR_RANGE
+    ids[0, 0] = -1
+    assert oracle.sort_assignments(ids, 8)[0] == oracle.ERR_RANGE
+
+
+# ---------------------------------------------------------------- tiles
+
+
+def test_tiles_hand_worked_example():
+    g = _golden("tiles_example.json")
+    for bm in (2, 4):
+        st, off, tiles, tc = oracle.build_expert_tiles(np.array(g["sorted_ids"]), g["E"], bm)
+        assert st == oracle.OK
+        assert off.tolist() == g["offsets"]
+        assert tiles.tolist() == g[f"BM{bm}"]["tiles"]
+        assert tc == g[f"BM{bm}"]["tile_count"]
+
+
+@pytest.mark.parametrize("A,E,BM,seed", [(1, 1, 32, 0), (64, 8, 32, 1), (1000, 128, 64, 2),
+                                         (4096, 128, 128, 3), (300, 7, 16, 4), (50, 256, 32, 5)])
+def test_tiles_invariants(A, E, BM, seed):
+    rng = np.random.default_rng(seed)
+    sid = np.sort(rng.integers(0, E, size=A)).astype(np.int32)
+    st, off, tiles, tc = oracle.build_expert_tiles(sid, E, BM)
+    assert st == oracle.OK
+    counts = np.bincount(sid, minlength=E)
+    # offsets by direct counting (not a binary search)
+    assert off.tolist() == [int((sid < e).sum()) for e in range(E)] + [A]
+    assert tc == sum((c + BM - 1) // BM for c in counts)
+    assert tc <= oracle.max_tiles(A, E, BM)
+    assert tiles[:, 2].sum() == A
+    covered = np.zeros(A, np.int32)
+    for e, r0, rows in tiles:
+        assert 1 <= rows <= BM
+        assert off[e] <= r0 and r0 + rows <= off[e + 1]
+        covered[r0:r0 + rows] += 1
+    assert np.all(covered == 1)
+    assert np.all(np.diff(tiles[:, 0]) >= 0)
+
+
+def test_tiles_self_check():
+    sid = np.array([0, 1, 1, 3, 2, 4], np.int32)
+    st, _, _, tc = oracle.build_expert_tiles(sid, 8, 32)
+    assert st == oracle.ERR_UNSORTED and tc == 0
+    st, _, _, tc = oracle.build_expert_tiles(np.array([0, 1, 9], np.int32), 8, 32)
+    assert st == oracle.ERR_RANGE and tc == 0
+    st, _, _, tc = oracle.build_expert_tiles(np.array([0, 5, 1, -1], np.int32), 8, 32)
+    assert st == oracle.ERR_RANGE and tc == 0  # range reported in preference to order
+
+
+# ---------------------------------------------------------------- projections
+
+
+def _const_rows(N, K, row_value):
+    """Packed weights whose row n dequantises to the constant row_value[n] (zero nibbles,
+    scale 1, bias = the value, which must be exact in bf16)."""
+    packed = np.zeros((N, K // 8), np.uint32)
+    s = np.full((N, K // 64), bf16_bits(1.0), np.uint16)
+    b = np.array([[bf16_bits(v)] * (K // 64) for v in row_value], np.uint16)
+    return packed, s, b
+
+
+def _layer_dict(E, H, I, Wgu, Sgu, Bgu, Wd, Sd, Bd, x_bits, ids, w):
+    return dict(E=E, H=H, I=I, T=x_bits.shape[0], k=ids.shape[1], x=x_bits, topk_ids=ids,
+                topk_weights=w, Wgu=Wgu[None], Sgu=Sgu[None], Bgu=Bgu[None], Wd=Wd[None],
+                Sd=Sd[None], Bd=Bd[None])
+
+
+def test_gate_up_one_hot_returns_a_weight_column():
+    # W[n][kk] = (n+1) * (kk % 16) / 16 : a transposed read gives another value
+    H, I = 128, 64
+    N = 2 * I
+    packed = np.tile(np.array([0x76543210, 0xFEDCBA98], np.uint32), (N, H // 16))
+    s = np.array([[bf16_bits((n + 1) / 16.0)] * (H // 64) for n in range(N)], np.uint16)
+    b = np.zeros((N, H // 64), np.uint16)
+    d = dict(H=H, I=I, Wgu=packed[None], Sgu=s[None], Bgu=b[None])
+    for i in (0, 5, 63, 64, 127):
+        x = np.zeros(H, np.uint16)
+        x[i] = bf16_bits(1.0)
+        h = oracle.expert_geglu(x, 0, d)
+        g = np.array([(n + 1) * (i % 16) / 16.0 for n in range(I)])
+        u = np.array([(I + n + 1) * (i % 16) / 16.0 for n in range(I)])
+        assert np.allclose(h, oracle.gelu_tanh(g) * u, rtol=1e-15, atol=0)
+
+
+def test_gate_rows_first_then_up_rows():
+    # gate rows dequantise to 2^-6, up rows to 2^-7; x = ones(128) -> g = 2, u = 1
+    H, I = 128, 64
+    packed, s, b = _const_rows(2 * I, H, [2.0**-6] * I + [2.0**-7] * I)
+    d = dict(H=H, I=I, Wgu=packed[None], Sgu=s[None], Bgu=b[None])
+    h = oracle.expert_geglu(np.full(H, bf16_bits(1.0), np.uint16), 0, d)
+    assert np.allclose(h, oracle.gelu_tanh(np.array([2.0]))[0] * 1.0, rtol=1e-15)
+    assert not np.allclose(h, oracle.gelu_tanh(np.array([1.0]))[0] * 2.0)
+
+
+def test_zero_nibbles_leave_the_bias_sum():
+    # q = 0 everywhere: W x = sum_g b_g * sum_{k in g} x_k
+    H, I = 256, 64
+    rng = np.random.default_rng(7)
+    xb = np.array([bf16_bits(float(v)) for v in rng.integers(-4, 5, size=H)], np.uint16)
+    xv = synth.bf16_bits_to_f64(xb)
+    biases = [0.25, -0.5, 1.0, 2.0]
+    packed = np.zeros((2 * I, H // 8), np.uint32)
+    s = np.full((2 * I, H // 64), bf16_bits(3.0), np.uint16)  # scale must not matter
+    b = np.array([[bf16_bits(v) for v in biases]] * (2 * I), np.uint16)
+    d = dict(H=H, I=I, Wgu=packed[None], Sgu=s[None], Bgu=b[None])
+    gsum = sum(biases[g] * xv[64 * g:64 * (g + 1)].sum() for g in range(4))
+    h = oracle.expert_geglu(xb, 0, d)
+    assert np.allclose(h, oracle.gelu_tanh(np.array([gsum]))[0] * gsum, rtol=1e-14)
+
+
+def test_down_one_hot_and_bias_sum():
+    H, I = 128, 128
+    packed = np.tile(np.array([0x76543210, 0xFEDCBA98], np.uint32), (H, I // 16))
+    s = np.array([[bf16_bits((n + 1) / 8.0)] * (I // 64) for n in range(H)], np.uint16)
+    b = np.array([[bf16_bits(-1.0), bf16_bits(0.5)]] * H, np.uint16)
+    d = dict(H=H, I=I, Wd=packed[None], Sd=s[None], Bd=b[None])
+    for i in (0, 17, 64, 127):
+        h = np.zeros(I)
+        h[i] = 1.0
+        o = oracle.expert_down(h, 0, d)
+        bias = -1.0 if i < 64 else 0.5
+        assert np.array_equal(o, np.array([(n + 1) / 8.0 * (i % 16) + bias for n in range(H)]))
+    d0 = dict(H=H, I=I, Wd=np.zeros_like(packed)[None], Sd=s[None], Bd=b[None])
+    o = oracle.expert_down(np.ones(I), 0, d0)
+    assert np.all(o == 64 * (-1.0) + 64 * 0.5)
+
+
+# ---------------------------------------------------------------- whole layer
+
+
+def test_sorted_route_equals_direct_definition_tiny():
+    d = synth.make("tiny")
+    r = oracle.layer(d)
+    y_direct = oracle.moe_layer_tokens(d, np.arange(d["T"]))
+    assert np.max(np.abs(r["y"] - y_direct)) < 1e-12
+    assert np.max(np.abs(r["y"])) > 1e-3  # not trivially zero
+
+
+def test_duplicate_experts_in_one_token_are_summed():
+    d = dict(synth.make("tiny"))
+    ids = d["topk_ids"].copy()
+    ids[:, 1] = ids[:, 0]
+    d["topk_ids"] = ids
+    r = oracle.layer(d, tokens=[0, 3])
+    y_direct = oracle.moe_layer_tokens(d, [0, 3])
+    assert np.max(np.abs(r["y"] - y_direct)) < 1e-12
+    # both terms use the same expert: y = (w0 + w1) * FFN_e(x)
+    for i, t in enumerate([0, 3]):
+        h = oracle.expert_geglu(d["x"][t], int(ids[t, 0]), d)
+        o = oracle.expert_down(h, int(ids[t, 0]), d)
+        w = float(d["topk_weights"][t, 0]) + float(d["topk_weights"][t, 1])
+        assert np.allclose(r["y"][i], w * o, rtol=1e-12, atol=1e-14)
+
+
+def test_zero_weight_contributes_exactly_zero():
+    d = dict(synth.make("tiny"))
+    w = d["topk_weights"].copy()
+    w[:5, :] = 0.0
+    w[5:10, 1] = 0.0
+    d["topk_weights"] = w
+    r = oracle.layer(d)
+    assert np.all(r["y"][:5] == 0.0)
+    for t in range(5, 10):  # only the j=0 term is left
+        e = int(d["topk_ids"][t, 0])
+        o = oracle.expert_down(oracle.expert_geglu(d["x"][t], e, d), e, d)
+        assert np.allclose(r["y"][t], float(w[t, 0]) * o, rtol=1e-12, atol=1e-15)
+
+
+def test_weighted_sum_is_linear_in_the_router_weights():
+    d = synth.make("tiny")
+    y1 = oracle.layer(d)["y"]
+    y2 = oracle.down_unsort(d, oracle.layer(d)["h"], *oracle.sort_assignments(
+        d["topk_ids"], d["E"])[1:3], np.arange(d["T"]), topk_weights=2 * d["topk_weights"])
+    assert np.allclose(y2, 2 * y1, rtol=1e-13, atol=0)
+
+
+def test_k1_unit_weight_is_one_expert_ffn():
+    d = dict(synth.make("tiny"))
+    d["k"] = 1
+    d["topk_ids"] = d["topk_ids"][:, :1].copy()
+    d["topk_weights"] = np.ones((d["T"], 1), np.float32)
+    r = oracle.layer(d)
+    for t in (0, 7, 31):
+        e = int(d["topk_ids"][t, 0])
+        o = oracle.expert_down(oracle.expert_geglu(d["x"][t], e, d), e, d)
+        assert np.array_equal(r["y"][t], o)
+
+
+def test_gemma_shape_one_hot_through_the_full_layer():
+    # Gemma geometry (H=2816, I=704), one expert, constant rows: every output is a
+    # closed form.  x = e_i, gate rows = 2^-2 * (n % 4 + 1), up rows = 2^-3, down = 2^-4.
+    H, I = 2816, 704
+    Wgu, Sgu, Bgu = _const_rows(2 * I, H, [0.25 * (n % 4 + 1) for n in range(I)] + [0.125] * I)
+    Wd, Sd, Bd = _const_rows(H, I, [0.0625] * H)
+    x = np.zeros((1, H), np.uint16)
+    x[0, 1000] = bf16_bits(1.0)
+    d = _layer_dict(1, H, I, Wgu, Sgu, Bgu, Wd, Sd, Bd, x, np.zeros((1, 1), np.int32),
+                    np.array([[0.5]], np.float32))
+    r = oracle.layer(d)
+    g = np.array([0.25 * (n % 4 + 1) for n in range(I)])
+    h_expected = oracle.gelu_tanh(g) * 0.125
+    assert np.allclose(r["h"][0], h_expected, rtol=1e-15)
+    y_expected = 0.5 * 0.0625 * h_expected.sum()
+    assert np.allclose(r["y"][0], y_expected, rtol=1e-13)
