@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark of one MoE expert layer step (sort -> tiles -> gate/up+GeGLU -> down+un-sort).
+
+Prints ONE JSON line (rank 0).  Default workload: the decode step of the
+Gemma-4 26B-A4B-shaped layer (128 experts, hidden 2816, intermediate 704,
+4-bit group-64 affine weights with bf16 scales/biases, 4 tokens x top-8 =
+32 assignments), seeded synthetic inputs.  ``--config`` picks another
+workload (tiny, decode, prefill_uniform, prefill_skewed, prefill_zipf).
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launch stream, with the 129 MB L2 flushed (a 512 MB write) between
+steps outside the events; barrier + synchronize on both sides of the timed
+region; the max over ranks.  Under torchrun each rank runs its own copy of
+the workload on its own GPU (independent layers, no collective): weak
+scaling, value = all ranks' assignments / the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has here) on the host cores, on a bounded sample of the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def per_expert_bytes(H, I):
+    """Algorithmic weight bytes of one expert: 0.5 B per 4-bit weight plus the bf16 scale
+    and bias of every 64-group, for gate/up (2I x H) and down (H x I)."""
+    gu = 2 * I * H // 2 + 2 * (2 * I * (H // 64)) * 2
+    dn = H * I // 2 + 2 * (H * (I // 64)) * 2
+    return gu, dn
+
+
+def flops_per_assignment(H, I):
+    return 2 * (2 * I * H + H * I)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                p = json.load(f)
+            hbm = p.get("hbm_gbs") or p.get("hbm_GBps")
+            tf = p.get("bf16_tflops")
+            tfs = p.get("bf16_tflops_sustained", tf)
+            if hbm and tf:
+                return float(hbm), float(tf), float(tfs), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_traffic(kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary, or None if the kernel
+    source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(kernel_tag)
+        if not rec:
+            return None
+        src = os.path.join(ROOT, rec["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != rec["source_sha"]:
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The fp64 CPU oracle on the host cores, on a bounded sample of the workload."""
+    if rank != 0:
+        return 0
+    import oracle
+    cfg = synth.CONFIGS[args.config]
+    d = synth.make(args.config)
+    A = d["T"] * d["k"]
+    slot_budget = args.ref_slots or A
+    rng = np.random.default_rng(0)
+    st, sid, perm, counts = oracle.sort_assignments(d["topk_ids"], d["E"])
+    # sample: whole tokens (all k of their slots), enough to reach ~slot_budget slots
+    n_tok = max(1, min(d["T"], slot_budget // d["k"]))
+    toks = np.sort(rng.choice(d["T"], size=n_tok, replace=False)).astype(np.int32)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        r = oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+        del r
+    per_step = sum(times) / len(times)
+    assignments = n_tok * d["k"]
+    value = assignments / per_step
+    cores = oracle.num_threads()
+    sample = (f"{n_tok} of {d['T']} tokens ({assignments} of {A} assignments) of workload "
+              f"{args.config}: oracle sort + fp64 gate/up, GeGLU, down and weighted sum")
+    line = {
+        "impl": "reference", "metric": "MoE layer assignments/s", "value": value,
+        "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3 * A / assignments, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_name(args.config, cfg), "assignments": A},
+        "cpu_baseline": {"value": value, "unit": "assignments/s", "cores": cores,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "assignments/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_name(name, cfg):
+    return (f"{name}: E={cfg['E']} H={cfg['H']} I={cfg['I']} T={cfg['T']} top-{cfg['k']} "
+            f"A={cfg['T'] * cfg['k']}, 4-bit gs64 affine, bf16 scales/biases, router={cfg['router']}")
+
+
+def cpu_baseline(d, seconds):
+    """The oracle, as it stands, timed on the host cores on whole tokens of the workload."""
+    import oracle
+    toks_all = np.arange(d["T"], dtype=np.int32)
+    rng = np.random.default_rng(1)
+    n = 1
+    t0 = time.perf_counter()
+    done_tokens = 0
+    elapsed = 0.0
+    while True:
+        toks = np.sort(rng.choice(toks_all, size=min(n, d["T"]), replace=False)).astype(np.int32)
+        t1 = time.perf_counter()
+        oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks)
+        elapsed += time.perf_counter() - t1
+        done_tokens += toks.size
+        if time.perf_counter() - t0 > seconds or done_tokens >= 64 * d["T"]:
+            break
+        n = min(2 * n, d["T"])
+    assignments = done_tokens * d["k"]
+    return {"value": assignments / elapsed, "unit": "assignments/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done_tokens} tokens ({assignments} assignments) of the same workload "
+                      f"in {elapsed:.1f} s, fp64 oracle (sort + gate/up + GeGLU + down + "
+                      f"weighted sum)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="decode", choices=synth.CONFIG_ORDER)
+    ap.add_argument("--variant", default="auto", choices=["auto", "gemv", "tc"])
+    ap.add_argument("--tile-m", type=int, default=128)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-slots", type=int, default=0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import moe_expert_bit_gb300 as mq
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    variant = {"auto": mq.VARIANT_AUTO, "gemv": mq.VARIANT_GEMV, "tc": mq.VARIANT_TC}[args.variant]
+
+    cfg = synth.CONFIGS[args.config]
+    d = synth.make(args.config)
+    E, H, I, T, k = d["E"], d["H"], d["I"], d["T"], d["k"]
+    A = T * k
+    W = device_weights(d, dev, torch)
+    x_h = pinned_bf16(d["x"], torch)
+    ids_h = torch.from_numpy(d["topk_ids"]).pin_memory()
+    tw_h = torch.from_numpy(d["topk_weights"]).pin_memory()
+    x = x_h.to(dev)
+    ids = ids_h.to(dev)
+    tw = tw_h.to(dev)
+    buf = mq.MoeLayerBuffers(T, k, E, H, I, args.tile_m, device=dev)
+    y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    r = buf.routing
+    r.status.zero_()
+
+    def step(ev=None):
+        # the four library calls; events (if given) bracket the gate/up launch
+        mq.moe_sort_assignments(ids, E, r.sorted_ids, r.perm, r.counts, r.status, stream)
+        mq.moe_build_expert_tiles(r.sorted_ids, E, args.tile_m, r.offsets, r.tiles, r.tile_count,
+                                  r.status, stream)
+        if ev is not None:
+            ev[0].record(stream)
+        mq.moe_gather_qmm_geglu(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.h, variant, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        mq.moe_gather_qmm_down_unsort(buf.h, W["Wd"], W["Sd"], W["Bd"], r, tw, H, I, buf.y_acc,
+                                      buf.y, variant, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        ids.copy_(ids_h, non_blocking=True)
+        tw.copy_(tw_h, non_blocking=True)
+        step()
+        y_h.copy_(buf.y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    if int(r.status.item()) != 0:
+        raise SystemExit(f"device status {int(r.status.item())} after warm-up")
+
+    # ---- timed region: K steps, L2 flushed between them outside the events ----
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    time.sleep(0.3)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step(ev[i][1:])
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    step_ms = [e[0].elapsed_time(e[3]) for e in ev]
+    geglu_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    down_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    route_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = sum(step_ms)
+
+    # ---- end-to-end through the public API with host buffers ----
+    for _ in range(2):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    e2e_total_ms = sum(a.elapsed_time(b) for a, b in e2e_ev)
+    status = int(r.status.item())
+
+    if world > 1:
+        t = torch.tensor([total_ms, e2e_total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_total_ms = float(t[0]), float(t[1])
+
+    counts = np.bincount(d["topk_ids"].ravel(), minlength=E)
+    touched = int((counts > 0).sum())
+    gu_b, dn_b = per_expert_bytes(H, I)
+    w_bytes = touched * (gu_b + dn_b)
+    flops = flops_per_assignment(H, I) * A
+    hbm, tf_burst, tf_sus, peak_src = load_peaks()
+    ms = total_ms / args.steps
+    t_roof_ms = max(w_bytes / (hbm * 1e9), flops / (tf_burst * 1e12)) * 1e3
+    geglu_avg = sum(geglu_ms) / len(geglu_ms)
+    geglu_bytes = touched * gu_b + T * H * 2 + A * I * 2
+    achieved = geglu_bytes / (geglu_avg * 1e-3) / 1e9
+    launches_per_step = 5
+    line = {
+        "metric": "MoE layer assignments/s", "value": world * A / (ms * 1e-3),
+        "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(args.config, cfg), "assignments": A,
+                   "experts_touched": touched, "tile_m": args.tile_m, "variant": args.variant,
+                   "l2": "flushed between steps (512 MB write outside the timed events)",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "weight_GBps": w_bytes / (ms * 1e-3) / 1e9,
+        "TFLOPs": flops / (ms * 1e-3) / 1e12,
+        "layer_roofline": {"t_roof_us": t_roof_ms * 1e3, "frac": t_roof_ms / ms,
+                           "weight_bytes": w_bytes, "flops": flops,
+                           "bound": "hbm" if w_bytes / (hbm * 1e9) >= flops / (tf_burst * 1e12)
+                           else "tensor", "peaks": peak_src},
+        "kernels_us": {"route (sort + tiles)": 1e3 * statistics.median(route_ms),
+                       "gather_qmm_geglu": 1e3 * statistics.median(geglu_ms),
+                       "gather_qmm_down_unsort (+zero, cast)": 1e3 * statistics.median(down_ms)},
+        "roofline": {"kernel": "gather_qmm_geglu", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "peak_source": f"{peak_src} (copy bandwidth)",
+                     "traffic": kernel_traffic("gather_qmm_geglu_" + args.config),
+                     "algorithmic_bytes": geglu_bytes},
+        "e2e": {"value": world * A / (e2e_total_ms / args.steps * 1e-3), "unit": "assignments/s",
+                "h2d_bytes_per_step": int(x_h.numel() * 2 + ids_h.numel() * 4 + tw_h.numel() * 4),
+                "d2h_bytes_per_step": int(y_h.numel() * 2)},
+        "clocks": clk,
+        "gpu_launches": launches_per_step * args.steps,
+        "device_status": status,
+        "wall_s_timed": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds)
+    elif rank == 0:
+        line["cpu_baseline"] = None
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def device_weights(d, dev, torch):
+    out = {}
+    for name in ("Wgu", "Wd"):
+        out[name] = torch.from_numpy(d[name].view(np.int32)).to(dev)
+    for name in ("Sgu", "Bgu", "Sd", "Bd"):
+        out[name] = torch.from_numpy(d[name].view(np.int16)).view(torch.bfloat16).to(dev)
+    return out
+
+
+def pinned_bf16(a, torch):
+    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+
+
+if __name__ == "__main__":
+    sys.exit(main() or 0)

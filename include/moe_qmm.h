@@ -1,0 +1,212 @@
+/*
+ * moe_qmm.h -- C ABI of the sorted-expert 4-bit gathered MoE expert layer
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * One MoE layer of the Gemma-4 26B-A4B expert shape runs as four calls on
+ * one CUDA stream:
+ *
+ *   moe_sort_assignments        top-k expert ids -> sorted ids + permutation
+ *   moe_build_expert_tiles      sorted ids -> per-expert offsets + tile descriptors
+ *   moe_gather_qmm_geglu        h = gelu_tanh(x Wg^T) * (x Wu^T), gathered, 4-bit weights
+ *   moe_gather_qmm_down_unsort  y[t] = sum_j w[t,j] * (h Wd^T)[slot(t,j)], back in token order
+ *
+ * Sources on the pages (title, then section):
+ *   Layr-Labs/mlx PR #4, "opt-in Gemma 4 expert-QMM tile kernel with parallel
+ *     descriptor builder", section "What": sorted gathered QMM over contiguous
+ *     sorted indices, expert tiles, the one-threadgroup descriptor builder,
+ *     affine 4-bit group-64 weights with bf16 activations, packed gate/up
+ *     [128, 1408, 352] and down [128, 2816, 88] uint32; review findings
+ *     table, row F2, and the final review wave: the sortedness self-check.
+ *   SharpAI/SwiftLM issue #236, "compiled GeGLU product for Gemma4 MoE
+ *     experts", sections "What #27 set out to do" and "Still missing": the
+ *     geluApproximate(x_gate) * x_up product fused into one dispatch,
+ *     intermediates kept in the activation dtype; "Already on main":
+ *     weightedExpertSum.
+ *   Layr-Labs/mlx PR #4, "Measured standing": direct weighted un-sort.
+ *
+ * Conventions shared by every call:
+ *   - Every pointer argument except `tiles` (a host struct) and the return
+ *     of moe_last_error_string is a DEVICE pointer to a contiguous row-major
+ *     buffer owned by the caller.  The library allocates, frees and
+ *     synchronises nothing; every call only enqueues kernels on `stream`
+ *     (0 = the legacy default stream) and returns.
+ *   - bf16 tensors are passed as `moe_bf16_t` (the raw 16-bit pattern).
+ *   - Host-side validation runs before any launch and returns a status other
+ *     than MOE_OK without enqueueing anything, so no output is half written.
+ *     moe_last_error_string() (per host thread) then says why.
+ *   - Data-dependent errors (an expert id out of range, sorted ids that are
+ *     not sorted) are found on the device.  They are written to the caller's
+ *     device status word (int32, must start at 0): the first error wins.
+ *     Every kernel reads the status word first and does nothing if it is not
+ *     0, so a later call on the same stream is a no-op; the caller reads the
+ *     word whenever it synchronises.  No kernel traps or asserts.
+ *   - Index type is int32 (values stay below 2^31).
+ *   - Flat assignment index: a = t * top_k + j for token t and choice j.
+ *   - No exception crosses the ABI.
+ */
+#ifndef MOE_QMM_H_
+#define MOE_QMM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16_t; /* bf16 bit pattern */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size */
+  MOE_ERR_UNSUPPORTED = 2, /* a shape or option outside what is implemented */
+  MOE_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
+  MOE_ERR_UNSORTED = 4,    /* device status: sorted ids not non-decreasing */
+  MOE_ERR_RANGE = 5        /* device status: an expert id outside [0, E) */
+} moe_status;
+
+/* Kernel choice for the two projection calls. */
+typedef enum {
+  MOE_VARIANT_AUTO = 0, /* weight-streaming GEMV for decode-sized calls, tensor-core GEMM otherwise */
+  MOE_VARIANT_GEMV = 1, /* CUDA-core weight-streaming kernel (any size) */
+  MOE_VARIANT_TC = 2    /* tcgen05 tensor-core grouped GEMM */
+} moe_variant;
+
+#define MOE_MAX_EXPERTS 256
+
+/*
+ * Routing state produced by the first two calls and read by the last two.
+ * A host struct holding device pointers (all caller-owned):
+ *   sorted_ids [A]           expert of sorted slot s (non-decreasing)
+ *   perm       [A]           flat index a of sorted slot s (x row = perm[s] / top_k)
+ *   offsets    [E+1]         first slot of expert e; offsets[E] = A
+ *   tiles      [max_tiles*3] int32 triplets {expert, row_begin, rows}, experts ascending
+ *   tile_count [1]           number of valid descriptors
+ *   status     [1]           device status word (see conventions)
+ * and the sizes they were built with.
+ */
+typedef struct {
+  const int32_t *sorted_ids;
+  const int32_t *perm;
+  const int32_t *offsets;
+  const int32_t *tiles;
+  const int32_t *tile_count;
+  int32_t *status;
+  int32_t num_tokens;      /* T */
+  int32_t top_k;           /* k */
+  int32_t num_assignments; /* A = T * k */
+  int32_t num_experts;     /* E */
+  int32_t tile_m;          /* BM: rows per tile descriptor */
+  int32_t max_tiles;       /* capacity of `tiles` in descriptors */
+} moe_tiles_t;
+
+/*
+ * Capacity needed for the tile descriptors of A assignments over E experts
+ * with BM-row tiles: floor(A / BM) + min(E, A).  (Per expert ceil(c_e/BM)
+ * <= floor(c_e/BM) + 1, and at most min(E, A) experts are non-empty.)
+ * Returns 0 for invalid arguments.
+ */
+size_t moe_max_tiles(int32_t num_assignments, int32_t num_experts, int32_t tile_m);
+
+/*
+ * Bytes of fp32 workspace that moe_gather_qmm_down_unsort needs for T
+ * tokens of width H (the y accumulator, [T, H] fp32).  0 for invalid sizes.
+ */
+size_t moe_workspace_bytes(int32_t num_tokens, int32_t hidden);
+
+/*
+ * Step a1 -- flatten and stable-sort the assignments by expert
+ * (Layr-Labs/mlx PR #4, "What": the gathered QMM reads contiguous sorted
+ * indices).
+ *   topk_ids   [T, k] int32  expert of choice j of token t
+ *   sorted_ids [A]    int32  out: experts in non-decreasing order
+ *   perm       [A]    int32  out: perm[s] = a = t*k + j of slot s; equal
+ *                            experts keep ascending a (stable)
+ *   counts     [E]    int32  out: assignments per expert
+ *   status     [1]    int32  device status word
+ * Any id outside [0, E) sets MOE_ERR_RANGE in *status and leaves the
+ * outputs unspecified.  One CTA; A up to 2^24.
+ * Host errors: MOE_ERR_INVALID_ARG (null pointer, T < 1, k < 1, k > E),
+ * MOE_ERR_UNSUPPORTED (E outside [1, MOE_MAX_EXPERTS], A > 2^24).
+ */
+moe_status moe_sort_assignments(const int32_t *topk_ids, int32_t num_tokens, int32_t top_k,
+                                int32_t num_experts, int32_t *sorted_ids, int32_t *perm,
+                                int32_t *counts, int32_t *status, cudaStream_t stream);
+
+/*
+ * Step a2 -- per-expert offsets and tile descriptors with a sortedness
+ * self-check (Layr-Labs/mlx PR #4, "What": the builder finds each expert's
+ * sorted range by binary search, numbers the tiles by an exclusive scan of
+ * per-expert tile counts and emits the descriptors; review finding F2 and
+ * the final review wave: an adjacent-pair scan proves global order, and a
+ * violation yields zero tiles).
+ *   sorted_ids [A]             int32 input
+ *   offsets    [E+1]           out: offsets[e] = first s with sorted_ids[s] >= e
+ *   tiles      [max_tiles*3]   out: for each expert (ascending) ceil(c_e/BM)
+ *                              descriptors {e, offsets[e] + r*BM, min(BM, c_e - r*BM)}
+ *   tile_count [1]             out: number of descriptors (0 on any violation)
+ *   status     [1]             MOE_ERR_RANGE if an id is outside [0, E),
+ *                              else MOE_ERR_UNSORTED if some ids[s] > ids[s+1]
+ * tile_m must be 16, 32, 64, 128 or 256; max_tiles must be at least
+ * moe_max_tiles(A, E, tile_m).  One CTA.
+ */
+moe_status moe_build_expert_tiles(const int32_t *sorted_ids, int32_t num_assignments,
+                                  int32_t num_experts, int32_t tile_m, int32_t max_tiles,
+                                  int32_t *offsets, int32_t *tiles, int32_t *tile_count,
+                                  int32_t *status, cudaStream_t stream);
+
+/*
+ * Steps a3-a6 -- gathered 4-bit gate/up projection with the GeGLU product
+ * in its epilogue (Layr-Labs/mlx PR #4, "What"; SharpAI/SwiftLM issue #236,
+ * "Still missing": geluApproximate(x_gate) * x_up in one dispatch).
+ *   x   [T, H]       bf16   activations (token order)
+ *   Wgu [E, 2I, H/8] uint32 packed 4-bit weights; rows [0, I) gate, [I, 2I) up;
+ *                           nibble j of a word is bits 4j..4j+3 (lowest first)
+ *   Sgu, Bgu [E, 2I, H/64] bf16  per-64-group scale and bias: w = s*q + b
+ *   h   [A, I]       bf16   out, sorted-slot order:
+ *        h[s, n] = gelu_tanh(g) * u,  g = sum_k Wg[e][n][k] x[perm[s]/k][k],
+ *        u = sum_k Wu[e][n][k] x[...][k],  e = sorted_ids[s],
+ *        gelu_tanh(z) = 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+ *      fp32 accumulation; the GELU product in fp32; h rounded to bf16.
+ * Requires H % 64 == 0 and I % 64 == 0 (MOE_ERR_UNSUPPORTED otherwise) and
+ * the routing state of this layer in `tiles`.  Does nothing if *status != 0.
+ */
+moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu, const moe_bf16_t *Sgu,
+                                const moe_bf16_t *Bgu, const moe_tiles_t *tiles, int32_t hidden,
+                                int32_t inter, int32_t variant, moe_bf16_t *h,
+                                cudaStream_t stream);
+
+/*
+ * Steps a7-a8 -- gathered 4-bit down projection whose epilogue does the
+ * router-weighted scatter-add back into token order (SharpAI/SwiftLM issue
+ * #236, "Already on main": weightedExpertSum; Layr-Labs/mlx PR #4,
+ * "Measured standing": direct weighted un-sort).
+ *   h   [A, I]       bf16   sorted-slot order (from moe_gather_qmm_geglu)
+ *   Wd  [E, H, I/8]  uint32 packed 4-bit down weights
+ *   Sd, Bd [E, H, I/64] bf16
+ *   topk_weights [T, k] fp32 router weights
+ *   y_acc_ws [T, H]  fp32   caller-owned workspace of moe_workspace_bytes(T, H)
+ *                           bytes; overwritten
+ *   y   [T, H]       bf16   out: y[t] = sum_j topk_weights[t, j] * (Wd[e] . h[s]),
+ *                           s the slot of a = t*k + j, e = sorted_ids[s]
+ * The k terms of a token are added with fp32 atomics, so the order of the
+ * additions (and the last bits of y) may differ from run to run.  Tokens
+ * whose weights are all zero get y = 0 exactly.  Requires H % 64 == 0 and
+ * I % 64 == 0.  Does nothing if *status != 0.
+ */
+moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
+                                      const moe_bf16_t *Sd, const moe_bf16_t *Bd,
+                                      const moe_tiles_t *tiles, const float *topk_weights,
+                                      int32_t hidden, int32_t inter, int32_t variant,
+                                      float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream);
+
+/* Why the last call on this host thread did not return MOE_OK ("" if it did). */
+const char *moe_last_error_string(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_QMM_H_ */

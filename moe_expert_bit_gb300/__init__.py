@@ -1,0 +1,225 @@
+"""Python binding of libmoeqmm.so, the sorted-expert 4-bit gathered MoE layer for GB300.
+
+The binding only marshals arguments: it checks dtype, device and contiguity of
+torch tensors and passes their device pointers and the current CUDA stream
+to the C ABI declared in ``include/moe_qmm.h``.  Every step of the layer runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback, and a
+missing or unbuildable library raises.
+
+Entry points (same names as the C ABI):
+
+* :func:`moe_sort_assignments`        top-k ids -> sorted ids, permutation, counts
+* :func:`moe_build_expert_tiles`      sorted ids -> offsets, tile descriptors, count
+* :func:`moe_gather_qmm_geglu`        gathered 4-bit gate/up + gelu_tanh(gate) * up -> h
+* :func:`moe_gather_qmm_down_unsort`  gathered 4-bit down + weighted un-sort -> y
+
+and :func:`moe_layer`, which runs the four on fresh output buffers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoeqmm.so")
+
+MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
+MOE_ERR_UNSORTED, MOE_ERR_RANGE = 4, 5
+VARIANT_AUTO, VARIANT_GEMV, VARIANT_TC = 0, 1, 2
+MAX_EXPERTS = 256
+
+# every symbol include/moe_qmm.h declares
+ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
+               "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
+               "moe_last_error_string")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[status {status}] {message}")
+        self.status = status
+
+
+class MoeTiles(ctypes.Structure):
+    """Mirror of ``moe_tiles_t``: device pointers plus the sizes they were built with."""
+    _fields_ = [("sorted_ids", ctypes.c_void_p), ("perm", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("tiles", ctypes.c_void_p),
+                ("tile_count", ctypes.c_void_p), ("status", ctypes.c_void_p),
+                ("num_tokens", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("num_assignments", ctypes.c_int32), ("num_experts", ctypes.c_int32),
+                ("tile_m", ctypes.c_int32), ("max_tiles", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(build_if_needed: bool = True):
+    """Load libmoeqmm.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if build_if_needed:
+            from . import build as _build
+            _build.build()
+        if not os.path.exists(LIB_PATH):
+            raise MoeError(MOE_ERR_CUDA, f"CUDA library missing: {LIB_PATH}")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i32 = ctypes.c_void_p, ctypes.c_int32
+        lib.moe_max_tiles.argtypes = [i32, i32, i32]
+        lib.moe_max_tiles.restype = ctypes.c_size_t
+        lib.moe_workspace_bytes.argtypes = [i32, i32]
+        lib.moe_workspace_bytes.restype = ctypes.c_size_t
+        lib.moe_sort_assignments.argtypes = [p, i32, i32, i32, p, p, p, p, p]
+        lib.moe_build_expert_tiles.argtypes = [p, i32, i32, i32, i32, p, p, p, p, p]
+        lib.moe_gather_qmm_geglu.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32, i32,
+                                             p, p]
+        lib.moe_gather_qmm_down_unsort.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), p, i32,
+                                                   i32, i32, p, p, p]
+        for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_gather_qmm_geglu",
+                   "moe_gather_qmm_down_unsort"):
+            getattr(lib, fn).restype = ctypes.c_int
+        lib.moe_last_error_string.argtypes = []
+        lib.moe_last_error_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != MOE_OK:
+        msg = load().moe_last_error_string().decode(errors="replace")
+        raise MoeError(status, msg)
+
+
+def _ptr(t, dtype, name, numel=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: expected a torch.Tensor")
+    if t.dtype != dtype:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_cuda:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: must be contiguous")
+    if numel is not None and t.numel() < numel:
+        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: {t.numel()} elements, need {numel}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def moe_max_tiles(num_assignments: int, num_experts: int, tile_m: int) -> int:
+    return int(load().moe_max_tiles(num_assignments, num_experts, tile_m))
+
+
+def moe_workspace_bytes(num_tokens: int, hidden: int) -> int:
+    return int(load().moe_workspace_bytes(num_tokens, hidden))
+
+
+def moe_sort_assignments(topk_ids, num_experts, sorted_ids, perm, counts, status, stream=None):
+    T, k = topk_ids.shape
+    A = T * k
+    _check(load().moe_sort_assignments(
+        _ptr(topk_ids, torch.int32, "topk_ids"), T, k, num_experts,
+        _ptr(sorted_ids, torch.int32, "sorted_ids", A), _ptr(perm, torch.int32, "perm", A),
+        _ptr(counts, torch.int32, "counts", num_experts), _ptr(status, torch.int32, "status", 1),
+        _stream(stream)))
+
+
+def moe_build_expert_tiles(sorted_ids, num_experts, tile_m, offsets, tiles, tile_count, status,
+                           stream=None):
+    A = sorted_ids.numel()
+    max_tiles = tiles.numel() // 3
+    _check(load().moe_build_expert_tiles(
+        _ptr(sorted_ids, torch.int32, "sorted_ids"), A, num_experts, tile_m, max_tiles,
+        _ptr(offsets, torch.int32, "offsets", num_experts + 1), _ptr(tiles, torch.int32, "tiles"),
+        _ptr(tile_count, torch.int32, "tile_count", 1), _ptr(status, torch.int32, "status", 1),
+        _stream(stream)))
+
+
+class Routing:
+    """Device buffers of the routing state of one layer call (a ``moe_tiles_t`` owner)."""
+
+    def __init__(self, num_tokens, top_k, num_experts, tile_m, device="cuda"):
+        A = num_tokens * top_k
+        self.T, self.k, self.A, self.E, self.tile_m = num_tokens, top_k, A, num_experts, tile_m
+        self.max_tiles = moe_max_tiles(A, num_experts, tile_m)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.sorted_ids = torch.empty(A, **i32)
+        self.perm = torch.empty(A, **i32)
+        self.counts = torch.empty(num_experts, **i32)
+        self.offsets = torch.empty(num_experts + 1, **i32)
+        self.tiles = torch.empty(max(self.max_tiles, 1) * 3, **i32)
+        self.tile_count = torch.zeros(1, **i32)
+        self.status = torch.zeros(1, **i32)
+
+    def struct(self) -> MoeTiles:
+        return MoeTiles(self.sorted_ids.data_ptr(), self.perm.data_ptr(), self.offsets.data_ptr(),
+                        self.tiles.data_ptr(), self.tile_count.data_ptr(), self.status.data_ptr(),
+                        self.T, self.k, self.A, self.E, self.tile_m, self.max_tiles)
+
+
+def _tiles_arg(routing):
+    if isinstance(routing, MoeTiles):
+        return ctypes.byref(routing)
+    return ctypes.byref(routing.struct())
+
+
+def _bf16(t, name, numel=None):
+    return _ptr(t, torch.bfloat16, name, numel)
+
+
+def moe_gather_qmm_geglu(x, Wgu, Sgu, Bgu, routing, hidden, inter, h, variant=VARIANT_AUTO,
+                         stream=None):
+    _check(load().moe_gather_qmm_geglu(
+        _bf16(x, "x"), _ptr(Wgu, torch.int32, "Wgu"), _bf16(Sgu, "Sgu"), _bf16(Bgu, "Bgu"),
+        _tiles_arg(routing), hidden, inter, variant, _bf16(h, "h"), _stream(stream)))
+
+
+def moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y_acc_ws, y,
+                               variant=VARIANT_AUTO, stream=None):
+    _check(load().moe_gather_qmm_down_unsort(
+        _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
+        _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
+        variant, _ptr(y_acc_ws, torch.float32, "y_acc_ws"), _bf16(y, "y"), _stream(stream)))
+
+
+class MoeLayerBuffers:
+    """Every device buffer one layer call writes, allocated once and reused."""
+
+    def __init__(self, T, k, E, H, I, tile_m, device="cuda"):
+        self.routing = Routing(T, k, E, tile_m, device)
+        self.h = torch.empty(T * k, I, dtype=torch.bfloat16, device=device)
+        self.y_acc = torch.empty(moe_workspace_bytes(T, H) // 4, dtype=torch.float32,
+                                 device=device)
+        self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
+        self.H, self.I = H, I
+
+
+def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, variant=VARIANT_AUTO,
+              buffers=None, stream=None):
+    """Run the four calls on one stream.  ``weights``: dict of Wgu, Sgu, Bgu, Wd, Sd, Bd
+    device tensors (uint32 data as int32, bf16 scales/biases).  Returns the buffers."""
+    T, k = topk_ids.shape
+    H = x.shape[1]
+    I = weights["Wd"].shape[2] * 8
+    b = buffers or MoeLayerBuffers(T, k, num_experts, H, I, tile_m, device=x.device)
+    r = b.routing
+    r.status.zero_()
+    moe_sort_assignments(topk_ids, num_experts, r.sorted_ids, r.perm, r.counts, r.status, stream)
+    moe_build_expert_tiles(r.sorted_ids, num_experts, tile_m, r.offsets, r.tiles, r.tile_count,
+                           r.status, stream)
+    moe_gather_qmm_geglu(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I, b.h, variant,
+                         stream)
+    moe_gather_qmm_down_unsort(b.h, weights["Wd"], weights["Sd"], weights["Bd"], r, topk_weights,
+                               H, I, b.y_acc, b.y, variant, stream)
+    return b

@@ -1,0 +1,47 @@
+// Shared device/host helpers of the CUDA library (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe_qmm.h"
+
+namespace moeqmm {
+
+// ---- host-side error reporting (per host thread) ----
+void set_error(const char *fmt, ...);
+void clear_error();
+moe_status check_launch(const char *what);
+
+// ---- device status word ----
+// The first error wins; later kernels see a non-zero word and return.
+__device__ __forceinline__ void raise_status(int32_t *status, int32_t code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ int32_t load_status(const int32_t *status) {
+  return *reinterpret_cast<const volatile int32_t *>(status);
+}
+
+// ---- numerics ----
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ float tanh_approx(float v) {
+  float r;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// geluApproximate: 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
+// (Hendrycks & Gimpel 2016), evaluated in fp32 with the hardware tanh.
+__device__ __forceinline__ float gelu_tanh(float z) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
+  const float k1 = 0.044715f;
+  float inner = k0 * fmaf(k1 * z, z * z, z);
+  return 0.5f * z * (1.0f + tanh_approx(inner));
+}
+
+}  // namespace moeqmm

@@ -1,0 +1,19 @@
+// Internal launchers shared by the C-ABI entry points (not part of the ABI).
+#pragma once
+
+#include <stdint.h>
+
+#include "moe_qmm.h"
+
+namespace moeqmm {
+
+moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
+                             const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
+                             uint16_t *h, cudaStream_t stream);
+moe_status launch_down_gemv(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
+                            const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
+                            int32_t H, int32_t I, float *y_acc, cudaStream_t stream);
+moe_status launch_cast_bf16(const float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
+                            cudaStream_t stream);
+
+}  // namespace moeqmm

@@ -1,0 +1,107 @@
+// C-ABI entry points of the two projections: host validation, then the
+// kernel variant.  Every check runs before the first launch.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moeqmm {
+
+static moe_status validate_tiles(const char *fn, const moe_tiles_t *t) {
+  if (!t) {
+    set_error("%s: tiles is null", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!t->sorted_ids || !t->perm || !t->offsets || !t->tiles || !t->tile_count || !t->status) {
+    set_error("%s: null pointer in tiles", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (t->num_experts < 1 || t->num_experts > MOE_MAX_EXPERTS) {
+    set_error("%s: num_experts %d outside [1, %d]", fn, t->num_experts, MOE_MAX_EXPERTS);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (t->num_tokens < 1 || t->top_k < 1 || t->top_k > t->num_experts ||
+      (int64_t)t->num_tokens * t->top_k != t->num_assignments) {
+    set_error("%s: inconsistent sizes T=%d k=%d A=%d", fn, t->num_tokens, t->top_k,
+              t->num_assignments);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int bm = t->tile_m;
+  if (bm != 16 && bm != 32 && bm != 64 && bm != 128 && bm != 256) {
+    set_error("%s: tile_m %d not in {16, 32, 64, 128, 256}", fn, bm);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (t->max_tiles < 0 ||
+      (size_t)t->max_tiles < moe_max_tiles(t->num_assignments, t->num_experts, bm)) {
+    set_error("%s: max_tiles %d below the bound for A=%d E=%d tile_m=%d", fn, t->max_tiles,
+              t->num_assignments, t->num_experts, bm);
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+static moe_status validate_dims(const char *fn, int32_t H, int32_t I, int32_t variant) {
+  if (H < 64 || I < 64 || H % 64 || I % 64) {
+    set_error("%s: hidden %d and inter %d must be positive multiples of 64", fn, H, I);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (H > 65536 || I > 65536) {
+    set_error("%s: hidden %d / inter %d above 65536", fn, H, I);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (variant != MOE_VARIANT_AUTO && variant != MOE_VARIANT_GEMV && variant != MOE_VARIANT_TC) {
+    set_error("%s: unknown variant %d", fn, variant);
+    return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+}  // namespace moeqmm
+
+using namespace moeqmm;
+
+extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu,
+                                           const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
+                                           const moe_tiles_t *tiles, int32_t H, int32_t I,
+                                           int32_t variant, moe_bf16_t *h, cudaStream_t stream) {
+  const char *fn = "moe_gather_qmm_geglu";
+  clear_error();
+  moe_status st = validate_tiles(fn, tiles);
+  if (st != MOE_OK) return st;
+  if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
+  if (!x || !Wgu || !Sgu || !Bgu || !h) {
+    set_error("%s: null pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (variant == MOE_VARIANT_TC) {
+    set_error("%s: tensor-core variant not built", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
+}
+
+extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
+                                                 const moe_bf16_t *Sd, const moe_bf16_t *Bd,
+                                                 const moe_tiles_t *tiles,
+                                                 const float *topk_weights, int32_t H, int32_t I,
+                                                 int32_t variant, float *y_acc_ws, moe_bf16_t *y,
+                                                 cudaStream_t stream) {
+  const char *fn = "moe_gather_qmm_down_unsort";
+  clear_error();
+  moe_status st = validate_tiles(fn, tiles);
+  if (st != MOE_OK) return st;
+  if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
+  if (!h || !Wd || !Sd || !Bd || !topk_weights || !y_acc_ws || !y) {
+    set_error("%s: null pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (variant == MOE_VARIANT_TC) {
+    set_error("%s: tensor-core variant not built", fn);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t n = (int64_t)tiles->num_tokens * H;
+  if (cudaMemsetAsync(y_acc_ws, 0, (size_t)n * sizeof(float), stream) != cudaSuccess) {
+    return check_launch(fn);
+  }
+  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
+  if (st != MOE_OK) return st;
+  return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
+}

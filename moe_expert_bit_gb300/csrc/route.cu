@@ -1,0 +1,310 @@
+// Routing half of the layer: the stable counting sort of the top-k
+// assignments by expert (step a1) and the tile-descriptor builder with its
+// sortedness self-check (step a2).  Both are single-CTA kernels: the inputs
+// are at most a few tens of KB, and one CTA keeps every step on-chip.
+//
+// Layr-Labs/mlx PR #4, "What": the gathered QMM consumes contiguous sorted
+// indices; its descriptor builder runs on one threadgroup (binary search of
+// each expert's sorted range, exclusive scan of per-expert tile counts,
+// strided emission).  Review finding F2 and the final review wave: an
+// adjacent-pair scan proves global order; a violation yields zero tiles.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace moeqmm {
+
+static thread_local char g_err[512];
+
+void set_error(const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+}
+
+void clear_error() { g_err[0] = 0; }
+
+moe_status check_launch(const char *what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_error("%s: %s", what, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+constexpr int kSortThreads = 1024;
+constexpr int kSortWarps = kSortThreads / 32;
+
+// Stable counting sort, one CTA.
+//  pass 1: histogram of expert ids in shared memory (+ range check);
+//  scan:   exclusive prefix over experts -> first slot of each expert;
+//  pass 2: rounds of 1024 consecutive assignments.  Inside a warp,
+//          __match_any_sync groups equal experts and a popcount of the lower
+//          lanes gives each element's rank; per-warp counts are scanned across
+//          the 32 warps per expert and added to a running cursor, so slots
+//          follow ascending a within every expert.
+__global__ void __launch_bounds__(kSortThreads)
+    sort_assignments_kernel(const int32_t *__restrict__ ids, int32_t A, int32_t E,
+                            int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
+                            int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+  __shared__ int32_t s_hist[MOE_MAX_EXPERTS];
+  __shared__ int32_t s_cursor[MOE_MAX_EXPERTS];
+  __shared__ int32_t s_warp[kSortWarps][MOE_MAX_EXPERTS];
+  __shared__ int32_t s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (load_status(status) != 0) return;
+
+  for (int e = tid; e < E; e += kSortThreads) s_hist[e] = 0;
+  for (int i = tid; i < kSortWarps * MOE_MAX_EXPERTS; i += kSortThreads) (&s_warp[0][0])[i] = 0;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  for (int a = tid; a < A; a += kSortThreads) {
+    int32_t e = ids[a];
+    if (e < 0 || e >= E)
+      s_bad = 1;
+    else
+      atomicAdd(&s_hist[e], 1);
+  }
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) raise_status(status, MOE_ERR_RANGE);
+    return;
+  }
+
+  // exclusive scan over E <= 256 experts by warp 0: 8 consecutive experts per lane
+  if (warp == 0) {
+    int32_t local[8];
+    int32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int e = lane * 8 + i;
+      local[i] = (e < E) ? s_hist[e] : 0;
+      sum += local[i];
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int32_t run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int e = lane * 8 + i;
+      if (e < E) {
+        s_cursor[e] = run;
+        counts[e] = local[i];
+      }
+      run += local[i];
+    }
+  }
+  __syncthreads();
+
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < A; base += kSortThreads) {
+    const int a = base + tid;
+    const bool valid = a < A;
+    const int32_t e = valid ? ids[a] : -1;
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    const int32_t rank = __popc(same & lt_mask);
+    if (valid && rank == 0) s_warp[warp][e] = __popc(same);
+    __syncthreads();
+    for (int ex = tid; ex < E; ex += kSortThreads) {  // per-expert scan over the warps
+      int32_t run = s_cursor[ex];
+#pragma unroll 8
+      for (int w = 0; w < kSortWarps; ++w) {
+        int32_t c = s_warp[w][ex];
+        s_warp[w][ex] = run;
+        run += c;
+      }
+      s_cursor[ex] = run;
+    }
+    __syncthreads();
+    if (valid) {
+      const int32_t slot = s_warp[warp][e] + rank;
+      sorted_ids[slot] = e;
+      perm[slot] = a;
+    }
+    __syncthreads();
+    for (int ex = tid; ex < E; ex += kSortThreads)
+      for (int w = 0; w < kSortWarps; ++w) s_warp[w][ex] = 0;
+    __syncthreads();
+  }
+}
+
+constexpr int kTileThreads = 512;
+
+__device__ __forceinline__ int32_t lower_bound_dev(const int32_t *v, int32_t n, int32_t key) {
+  int32_t lo = 0, hi = n;
+  while (lo < hi) {
+    int32_t mid = (lo + hi) >> 1;
+    if (v[mid] < key)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+// Offsets, tile counts, exclusive scan and strided descriptor emission, one CTA.
+__global__ void __launch_bounds__(kTileThreads)
+    build_expert_tiles_kernel(const int32_t *__restrict__ sorted_ids, int32_t A, int32_t E,
+                              int32_t BM, int32_t *__restrict__ offsets,
+                              int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
+                              int32_t *__restrict__ status) {
+  __shared__ int32_t s_off[MOE_MAX_EXPERTS + 1];
+  __shared__ int32_t s_tstart[MOE_MAX_EXPERTS + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (load_status(status) != 0) {
+    if (tid == 0) *tile_count = 0;
+    return;
+  }
+  // self-check: every id in range and every adjacent pair in order
+  int range_bad = 0, order_bad = 0;
+  for (int s = tid; s < A; s += kTileThreads) {
+    int32_t v = sorted_ids[s];
+    range_bad |= (v < 0 || v >= E);
+    if (s + 1 < A) order_bad |= (v > sorted_ids[s + 1]);
+  }
+  range_bad = __syncthreads_or(range_bad);
+  order_bad = __syncthreads_or(order_bad);
+  if (range_bad || order_bad) {
+    if (tid == 0) {
+      *tile_count = 0;
+      raise_status(status, range_bad ? MOE_ERR_RANGE : MOE_ERR_UNSORTED);
+    }
+    return;
+  }
+  // per-expert sorted range by binary search
+  for (int e = tid; e <= E; e += kTileThreads) s_off[e] = (e == E) ? A : lower_bound_dev(sorted_ids, A, e);
+  __syncthreads();
+  // tiles per expert, exclusive scan by warp 0 (8 experts per lane)
+  if (warp == 0) {
+    int32_t local[8];
+    int32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int e = lane * 8 + i;
+      int32_t c = (e < E) ? (s_off[e + 1] - s_off[e]) : 0;
+      local[i] = (c + BM - 1) / BM;
+      sum += local[i];
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int32_t run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      int e = lane * 8 + i;
+      if (e < E) s_tstart[e] = run;
+      run += local[i];
+    }
+    if (lane == 31) s_tstart[E] = incl;
+  }
+  __syncthreads();
+  for (int e = tid; e <= E; e += kTileThreads) offsets[e] = s_off[e];
+  const int32_t total = s_tstart[E];
+  // strided emission: tile i belongs to the last expert whose first tile is <= i
+  for (int i = tid; i < total; i += kTileThreads) {
+    int32_t lo = 0, hi = E;  // largest e in [0, E) with s_tstart[e] <= i
+    while (hi - lo > 1) {
+      int32_t mid = (lo + hi) >> 1;
+      if (s_tstart[mid] <= i)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int32_t e = lo;
+    const int32_t r = i - s_tstart[e];
+    const int32_t c = s_off[e + 1] - s_off[e];
+    tiles[3 * i + 0] = e;
+    tiles[3 * i + 1] = s_off[e] + r * BM;
+    tiles[3 * i + 2] = min(BM, c - r * BM);
+  }
+  if (tid == 0) *tile_count = total;
+}
+
+}  // namespace moeqmm
+
+using namespace moeqmm;
+
+extern "C" {
+
+const char *moe_last_error_string(void) { return g_err; }
+
+size_t moe_max_tiles(int32_t A, int32_t E, int32_t BM) {
+  if (A < 0 || E < 1 || BM < 1) return 0;
+  return static_cast<size_t>(A / BM) + static_cast<size_t>(A < E ? A : E);
+}
+
+size_t moe_workspace_bytes(int32_t T, int32_t H) {
+  if (T < 1 || H < 1) return 0;
+  return static_cast<size_t>(T) * static_cast<size_t>(H) * sizeof(float);
+}
+
+moe_status moe_sort_assignments(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
+                                int32_t *sorted_ids, int32_t *perm, int32_t *counts,
+                                int32_t *status, cudaStream_t stream) {
+  clear_error();
+  if (!topk_ids || !sorted_ids || !perm || !counts || !status) {
+    set_error("moe_sort_assignments: null pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (E < 1 || E > MOE_MAX_EXPERTS) {
+    set_error("moe_sort_assignments: num_experts %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (T < 1 || k < 1 || k > E) {
+    set_error("moe_sort_assignments: need T >= 1 and 1 <= k <= E (T=%d k=%d E=%d)", T, k, E);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int64_t A = static_cast<int64_t>(T) * k;
+  if (A > (int64_t(1) << 24)) {
+    set_error("moe_sort_assignments: %lld assignments exceed 2^24", (long long)A);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  sort_assignments_kernel<<<1, kSortThreads, 0, stream>>>(topk_ids, static_cast<int32_t>(A), E,
+                                                          sorted_ids, perm, counts, status);
+  return check_launch("moe_sort_assignments");
+}
+
+moe_status moe_build_expert_tiles(const int32_t *sorted_ids, int32_t A, int32_t E, int32_t BM,
+                                  int32_t max_tiles, int32_t *offsets, int32_t *tiles,
+                                  int32_t *tile_count, int32_t *status, cudaStream_t stream) {
+  clear_error();
+  if (!sorted_ids || !offsets || !tiles || !tile_count || !status) {
+    set_error("moe_build_expert_tiles: null pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (E < 1 || E > MOE_MAX_EXPERTS) {
+    set_error("moe_build_expert_tiles: num_experts %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (BM != 16 && BM != 32 && BM != 64 && BM != 128 && BM != 256) {
+    set_error("moe_build_expert_tiles: tile_m %d not in {16, 32, 64, 128, 256}", BM);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (A < 1 || A > (1 << 24)) {
+    set_error("moe_build_expert_tiles: num_assignments %d outside [1, 2^24]", A);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const size_t need = moe_max_tiles(A, E, BM);
+  if (max_tiles < 0 || static_cast<size_t>(max_tiles) < need) {
+    set_error("moe_build_expert_tiles: max_tiles %d < required %zu", max_tiles, need);
+    return MOE_ERR_INVALID_ARG;
+  }
+  build_expert_tiles_kernel<<<1, kTileThreads, 0, stream>>>(sorted_ids, A, E, BM, offsets, tiles,
+                                                            tile_count, status);
+  return check_launch("moe_build_expert_tiles");
+}
+
+}  // extern "C"

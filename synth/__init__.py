@@ -210,3 +210,21 @@ def make(name: str, seed: int = 0, T: int | None = None) -> dict:
 def bf16_bits_to_f64(a: np.ndarray) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16) to float64."""
     return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def make_custom(E: int, H: int, I: int, T: int, k: int, seed: int = 0,
+                router_kind: str = "normal") -> dict:
+    """A workload of any size (edge and ragged cases): N(0,0.02) weights quantised as
+    above, x ~ N(0,1), router logits N(0,1) (``router_kind="one"``: every token on expert 0
+    first)."""
+    base = 9000 + 7 * (E + 3 * H + 5 * I)
+    Wgu, Sgu, Bgu = quantized_weights(seed, base + 1, E, 2 * I, H)
+    Wd, Sd, Bd = quantized_weights(seed, base + 2, E, H, I)
+    x = activations(seed, base + 3, T, H)
+    scores = normals(seed, base + 4, T * E).reshape(T, E)
+    if router_kind == "one":
+        scores[:, 0] = 1e9
+    ids, tw = topk_softmax(scores, k)
+    return dict(name=f"custom_E{E}_H{H}_I{I}_T{T}_k{k}", E=E, H=H, I=I, T=T, k=k, x=x,
+                topk_ids=ids, topk_weights=tw, outlier_rows=np.zeros(0, np.int32),
+                Wgu=Wgu, Sgu=Sgu, Bgu=Bgu, Wd=Wd, Sd=Sd, Bd=Bd)

@@ -1,0 +1,41 @@
+"""Shared test helpers: moving seeded inputs to the device and the parity bound."""
+from __future__ import annotations
+
+import numpy as np
+
+# The activation parity bound: |gpu - oracle| <= REL * max(1, |oracle|), elementwise.
+# Rows of the outlier workload (activation rows scaled x20) are held to the same
+# bound with |oracle| read as the largest magnitude in that row.
+REL = 2e-2
+
+
+def to_device(d: dict, device="cuda") -> dict:
+    import torch
+    out = {}
+    for name in ("Wgu", "Wd"):
+        out[name] = torch.from_numpy(d[name].view(np.int32)).to(device)
+    for name in ("Sgu", "Bgu", "Sd", "Bd"):
+        out[name] = torch.from_numpy(d[name].view(np.int16)).view(torch.bfloat16).to(device)
+    out["x"] = torch.from_numpy(d["x"].view(np.int16)).view(torch.bfloat16).to(device)
+    out["topk_ids"] = torch.from_numpy(d["topk_ids"]).to(device)
+    out["topk_weights"] = torch.from_numpy(d["topk_weights"]).to(device)
+    return out
+
+
+def bf16_to_f64(t) -> np.ndarray:
+    """A bf16 torch tensor (any device) -> exact float64 numpy array."""
+    import torch
+    return t.detach().to("cpu").view(torch.int16).numpy().view(np.uint16).astype(
+        np.uint32).__lshift__(16).view(np.float32).astype(np.float64)
+
+
+def excess(gpu: np.ndarray, ref: np.ndarray, rowwise: np.ndarray | None = None) -> float:
+    """max over elements of |gpu - ref| / (REL * scale) (<= 1 passes).  scale is
+    max(1, |ref|) per element, or max(1, max|ref row|) for rows flagged in ``rowwise``."""
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = np.maximum(1.0, np.abs(ref))
+    if rowwise is not None and np.any(rowwise):
+        rowmax = np.maximum(1.0, np.abs(ref).max(axis=1, keepdims=True))
+        scale = np.where(np.asarray(rowwise)[:, None], rowmax, scale)
+    return float(np.max(np.abs(gpu - ref) / (REL * scale))) if gpu.size else 0.0

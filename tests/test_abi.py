@@ -1,0 +1,108 @@
+"""The C-ABI library builds, loads and exports every symbol its header declares (CPU only).
+
+No compute call is made here: there is no GPU on this host.  Host-side
+validation paths that return before any launch are exercised, because they
+touch no device memory.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import moe_expert_bit_gb300 as mq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for hdr in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(hdr).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == set(mq.ABI_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = mq.load()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_size_helpers():
+    assert mq.moe_max_tiles(4096, 128, 128) == 32 + 128
+    assert mq.moe_max_tiles(32, 128, 64) == 32
+    assert mq.moe_max_tiles(64, 8, 32) == 2 + 8
+    assert mq.moe_max_tiles(10, 0, 32) == 0
+    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4
+    assert mq.moe_workspace_bytes(0, 2816) == 0
+
+
+def _raw():
+    return mq.load()
+
+
+NULL = None
+
+
+@pytest.mark.parametrize("args,code", [
+    ((NULL, 4, 8, 128, 1, 1, 1, 1, NULL), mq.MOE_ERR_INVALID_ARG),   # null topk_ids
+    ((1, 4, 8, 0, 1, 1, 1, 1, NULL), mq.MOE_ERR_UNSUPPORTED),        # E = 0
+    ((1, 4, 8, 257, 1, 1, 1, 1, NULL), mq.MOE_ERR_UNSUPPORTED),      # E > 256
+    ((1, 0, 8, 128, 1, 1, 1, 1, NULL), mq.MOE_ERR_INVALID_ARG),      # T = 0
+    ((1, 4, 9, 8, 1, 1, 1, 1, NULL), mq.MOE_ERR_INVALID_ARG),        # k > E
+    ((1, 1 << 22, 8, 128, 1, 1, 1, 1, NULL), mq.MOE_ERR_UNSUPPORTED),  # A > 2^24
+])
+def test_sort_host_validation(args, code):
+    assert _raw().moe_sort_assignments(*args) == code
+    assert _raw().moe_last_error_string()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((NULL, 64, 8, 32, 10, 1, 1, 1, 1, NULL), mq.MOE_ERR_INVALID_ARG),
+    ((1, 64, 8, 48, 10, 1, 1, 1, 1, NULL), mq.MOE_ERR_UNSUPPORTED),   # tile_m 48
+    ((1, 64, 8, 32, 9, 1, 1, 1, 1, NULL), mq.MOE_ERR_INVALID_ARG),    # max_tiles too small
+    ((1, 0, 8, 32, 10, 1, 1, 1, 1, NULL), mq.MOE_ERR_INVALID_ARG),    # A = 0
+    ((1, 64, 300, 32, 70, 1, 1, 1, 1, NULL), mq.MOE_ERR_UNSUPPORTED),  # E > 256
+])
+def test_build_tiles_host_validation(args, code):
+    assert _raw().moe_build_expert_tiles(*args) == code
+
+
+def _tiles(**kw):
+    base = dict(sorted_ids=1, perm=1, offsets=1, tiles=1, tile_count=1, status=1, num_tokens=32,
+                top_k=2, num_assignments=64, num_experts=8, tile_m=32, max_tiles=10)
+    base.update(kw)
+    return mq.MoeTiles(**base)
+
+
+@pytest.mark.parametrize("tkw,H,I,variant,code", [
+    (dict(), 128, 64, 0, mq.MOE_OK),
+    (dict(perm=None), 128, 64, 0, mq.MOE_ERR_INVALID_ARG),
+    (dict(num_assignments=63), 128, 64, 0, mq.MOE_ERR_INVALID_ARG),
+    (dict(tile_m=24), 128, 64, 0, mq.MOE_ERR_UNSUPPORTED),
+    (dict(max_tiles=9), 128, 64, 0, mq.MOE_ERR_INVALID_ARG),
+    (dict(num_experts=300), 128, 64, 0, mq.MOE_ERR_UNSUPPORTED),
+    (dict(), 96, 64, 0, mq.MOE_ERR_UNSUPPORTED),   # H % 64
+    (dict(), 128, 32, 0, mq.MOE_ERR_UNSUPPORTED),  # I % 64
+    (dict(), 128, 64, 7, mq.MOE_ERR_INVALID_ARG),  # unknown variant
+])
+def test_projection_host_validation(tkw, H, I, variant, code):
+    t = _tiles(**tkw)
+    if code == mq.MOE_OK:
+        pytest.skip("a valid call would launch; covered by the GPU tests")
+    st = _raw().moe_gather_qmm_geglu(1, 1, 1, 1, ctypes.byref(t), H, I, variant, 1, NULL)
+    assert st == code
+    st = _raw().moe_gather_qmm_down_unsort(1, 1, 1, 1, ctypes.byref(t), 1, H, I, variant, 1, 1,
+                                           NULL)
+    assert st == code
+    assert _raw().moe_gather_qmm_geglu(NULL, 1, 1, 1, ctypes.byref(_tiles()), 128, 64, 0, 1,
+                                       NULL) == mq.MOE_ERR_INVALID_ARG

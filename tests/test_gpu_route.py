@@ -1,0 +1,119 @@
+"""GPU parity of the routing half (sort, offsets, tile descriptors): bit-exact vs the oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import moe_expert_bit_gb300 as mq  # noqa: E402
+
+
+def gpu_route(topk_ids: np.ndarray, E: int, tile_m: int):
+    T, k = topk_ids.shape
+    r = mq.Routing(T, k, E, tile_m)
+    ids = torch.from_numpy(np.ascontiguousarray(topk_ids, np.int32)).cuda()
+    mq.moe_sort_assignments(ids, E, r.sorted_ids, r.perm, r.counts, r.status)
+    mq.moe_build_expert_tiles(r.sorted_ids, E, tile_m, r.offsets, r.tiles, r.tile_count, r.status)
+    torch.cuda.synchronize()
+    tc = int(r.tile_count.item())
+    return dict(status=int(r.status.item()), sorted_ids=r.sorted_ids.cpu().numpy(),
+                perm=r.perm.cpu().numpy(), counts=r.counts.cpu().numpy(),
+                offsets=r.offsets.cpu().numpy(), tiles=r.tiles.cpu().numpy()[:3 * tc].reshape(-1, 3),
+                tile_count=tc)
+
+
+def check_against_oracle(topk_ids, E, tile_m):
+    g = gpu_route(topk_ids, E, tile_m)
+    st, sid, perm, counts = oracle.sort_assignments(topk_ids, E)
+    assert st == oracle.OK and g["status"] == 0
+    assert np.array_equal(g["sorted_ids"], sid)
+    assert np.array_equal(g["perm"], perm)
+    assert np.array_equal(g["counts"], counts)
+    st, off, tiles, tc = oracle.build_expert_tiles(sid, E, tile_m)
+    assert st == oracle.OK
+    assert np.array_equal(g["offsets"], off)
+    assert g["tile_count"] == tc
+    assert np.array_equal(g["tiles"], tiles)
+
+
+@pytest.mark.parametrize("name", synth.CONFIG_ORDER)
+@pytest.mark.parametrize("tile_m", [16, 32, 64, 128, 256])
+def test_route_matches_oracle_on_every_workload(name, tile_m):
+    cfg = synth.CONFIGS[name]
+    ids, _ = synth.router(name, cfg["T"], cfg["E"], cfg["k"])
+    check_against_oracle(ids, cfg["E"], tile_m)
+
+
+@pytest.mark.parametrize("T,k,E,seed", [
+    (1, 1, 1, 0),          # A = 1, one expert
+    (1, 8, 128, 1),        # one token
+    (1000, 1, 1, 2),       # every assignment on the only expert
+    (333, 3, 7, 3),        # ragged
+    (4096, 8, 256, 4),     # max experts
+    (65536, 8, 128, 5),    # 524288 assignments: 512 sort rounds
+    (1025, 2, 128, 6),     # one full round + 2 elements
+])
+def test_route_edge_cases(T, k, E, seed):
+    rng = np.random.default_rng(seed)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    for tile_m in (32, 128):
+        check_against_oracle(ids, E, tile_m)
+
+
+def test_route_all_on_one_expert_of_many():
+    ids = np.full((2048, 8), 77, np.int32)
+    check_against_oracle(ids, 128, 128)
+
+
+def test_route_is_deterministic():
+    ids, _ = synth.router("prefill_zipf", 2048, 128, 8)
+    a = gpu_route(ids, 128, 128)
+    b = gpu_route(ids, 128, 128)
+    for key in ("sorted_ids", "perm", "counts", "offsets", "tiles"):
+        assert np.array_equal(a[key], b[key])
+
+
+def test_sort_flags_out_of_range_ids():
+    ids = np.zeros((16, 2), np.int32)
+    ids[5, 1] = 8
+    g = gpu_route(ids, 8, 32)
+    assert g["status"] == mq.MOE_ERR_RANGE
+    assert g["tile_count"] == 0
+    ids[5, 1] = -3
+    assert gpu_route(ids, 8, 32)["status"] == mq.MOE_ERR_RANGE
+
+
+def _build_only(sorted_ids: np.ndarray, E: int, tile_m: int):
+    A = sorted_ids.size
+    r = mq.Routing(A, 1, E, tile_m)
+    r.tile_count.fill_(12345)
+    sid = torch.from_numpy(np.ascontiguousarray(sorted_ids, np.int32)).cuda()
+    mq.moe_build_expert_tiles(sid, E, tile_m, r.offsets, r.tiles, r.tile_count, r.status)
+    torch.cuda.synchronize()
+    return int(r.status.item()), int(r.tile_count.item())
+
+
+@pytest.mark.parametrize("bad,code", [
+    ([0, 1, 1, 3, 2, 4], mq.MOE_ERR_UNSORTED),
+    ([0, 0, 5, 5, 5, 4], mq.MOE_ERR_UNSORTED),   # violation at the last pair
+    ([1, 0], mq.MOE_ERR_UNSORTED),
+    ([0, 1, 9], mq.MOE_ERR_RANGE),
+    ([0, 5, 1, -1], mq.MOE_ERR_RANGE),           # range wins over order
+])
+def test_builder_self_check(bad, code):
+    st, tc = _build_only(np.array(bad, np.int32), 8, 32)
+    assert st == code and tc == 0
+
+
+def test_builder_self_check_long_input():
+    sid = np.sort(np.random.default_rng(0).integers(0, 128, size=100000)).astype(np.int32)
+    assert _build_only(sid, 128, 64) == (0, oracle.build_expert_tiles(sid, 128, 64)[3])
+    sid[77777], sid[77778] = sid[77778] + 1, sid[77777]
+    if sid[77777] > sid[77778]:
+        assert _build_only(sid, 128, 64) == (mq.MOE_ERR_UNSORTED, 0)
