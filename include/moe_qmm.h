@@ -202,6 +202,32 @@ moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
                                       int32_t hidden, int32_t inter, int32_t variant,
                                       float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream);
 
+/*
+ * Variant of moe_gather_qmm_down_unsort that allocates nothing and takes no
+ * workspace, for callers that cannot call cudaMalloc (a runtime plugin whose
+ * execute step must not allocate, a host program without an allocator to
+ * lend a workspace, a loop that must never reach the allocator).  The pages
+ * have no counterpart: it is a packaging of the same computation.
+ *   Same arguments and result as moe_gather_qmm_down_unsort, minus y_acc_ws.
+ *   The fp32 accumulator is a fixed array of MOE_NOALLOC_MAX_Y_ELEMENTS floats
+ *   (16 MiB) of device memory inside the library, which every GPU that loads
+ *   the library holds until the process exits.  T * H above that maximum
+ *   returns MOE_ERR_UNSUPPORTED before any launch.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture.
+ *   Every call on a device shares the one array: it is cleared at the start
+ *   of each call, and calls that overlap on the GPU (two streams, or two host
+ *   threads) race on it -- serialise them.
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304
+moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_t *Wd,
+                                              const moe_bf16_t *Sd, const moe_bf16_t *Bd,
+                                              const moe_tiles_t *tiles, const float *topk_weights,
+                                              int32_t hidden, int32_t inter, int32_t variant,
+                                              moe_bf16_t *y, cudaStream_t stream);
+
 /* Why the last call on this host thread did not return MOE_OK ("" if it did). */
 const char *moe_last_error_string(void);
 

@@ -34,7 +34,8 @@ MAX_EXPERTS = 256
 # every symbol include/moe_qmm.h declares
 ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
-               "moe_last_error_string")
+               "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc")
+NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
 class MoeError(RuntimeError):
@@ -80,8 +81,10 @@ def load(build_if_needed: bool = True):
                                              p, p]
         lib.moe_gather_qmm_down_unsort.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), p, i32,
                                                    i32, i32, p, p, p]
+        lib.moe_gather_qmm_down_unsort_noalloc.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles),
+                                                           p, i32, i32, i32, p, p]
         for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_gather_qmm_geglu",
-                   "moe_gather_qmm_down_unsort"):
+                   "moe_gather_qmm_down_unsort", "moe_gather_qmm_down_unsort_noalloc"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.moe_last_error_string.argtypes = []
         lib.moe_last_error_string.restype = ctypes.c_char_p
@@ -191,6 +194,17 @@ def moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, routing, topk_weights, hidden, int
         _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
         _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
         variant, _ptr(y_acc_ws, torch.float32, "y_acc_ws"), _bf16(y, "y"), _stream(stream)))
+
+
+def moe_gather_qmm_down_unsort_noalloc(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y,
+                                       variant=VARIANT_AUTO, stream=None):
+    """moe_gather_qmm_down_unsort without a workspace argument: for callers that cannot
+    allocate device memory.  The accumulator is the library's built-in fixed array
+    (T * hidden <= NOALLOC_MAX_Y_ELEMENTS); calls that overlap on the GPU race on it."""
+    _check(load().moe_gather_qmm_down_unsort_noalloc(
+        _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
+        _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
+        variant, _bf16(y, "y"), _stream(stream)))
 
 
 class MoeLayerBuffers:
