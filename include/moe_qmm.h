@@ -64,7 +64,8 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2, /* a shape or option outside what is implemented */
   MOE_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
   MOE_ERR_UNSORTED = 4,    /* device status: sorted ids not non-decreasing */
-  MOE_ERR_RANGE = 5        /* device status: an expert id outside [0, E) */
+  MOE_ERR_RANGE = 5,       /* device status: an expert id outside [0, E) */
+  MOE_ERR_TIMEOUT = 6      /* device status: a pipeline wait inside a kernel gave up */
 } moe_status;
 
 /* Kernel choice for the two projection calls. */

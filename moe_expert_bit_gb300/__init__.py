@@ -27,7 +27,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoeqmm.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
-MOE_ERR_UNSORTED, MOE_ERR_RANGE = 4, 5
+MOE_ERR_UNSORTED, MOE_ERR_RANGE, MOE_ERR_TIMEOUT = 4, 5, 6
 VARIANT_AUTO, VARIANT_GEMV, VARIANT_TC = 0, 1, 2
 MAX_EXPERTS = 256
 

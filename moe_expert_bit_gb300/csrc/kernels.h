@@ -13,6 +13,13 @@ moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint1
 moe_status launch_down_gemv(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                             int32_t H, int32_t I, float *y_acc, cudaStream_t stream);
+moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m);
+moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
+                           const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
+                           uint16_t *h, cudaStream_t stream);
+moe_status launch_down_tc(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
+                          const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
+                          int32_t H, int32_t I, float *y_acc, cudaStream_t stream);
 moe_status launch_cast_bf16(const float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
                             cudaStream_t stream);
 

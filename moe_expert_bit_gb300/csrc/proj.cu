@@ -54,6 +54,19 @@ static moe_status validate_dims(const char *fn, int32_t H, int32_t I, int32_t va
   return MOE_OK;
 }
 
+// MOE_VARIANT_AUTO: the tensor-core GEMM wherever it supports the shape.
+static moe_status resolve_variant(const char *fn, const moe_tiles_t *t, int32_t H, int32_t I,
+                                  int32_t *variant) {
+  const bool tc_ok = tc_supported(H, I, t->tile_m) == MOE_OK;
+  if (*variant == MOE_VARIANT_TC && !tc_ok) {
+    set_error("%s: tensor-core variant supports tile_m <= 128 and H, I <= 4096 "
+              "(got tile_m=%d H=%d I=%d)", fn, t->tile_m, H, I);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (*variant == MOE_VARIANT_AUTO) *variant = tc_ok ? MOE_VARIANT_TC : MOE_VARIANT_GEMV;
+  return MOE_OK;
+}
+
 }  // namespace moeqmm
 
 using namespace moeqmm;
@@ -71,10 +84,8 @@ extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *
     set_error("%s: null pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
-  if (variant == MOE_VARIANT_TC) {
-    set_error("%s: tensor-core variant not built", fn);
-    return MOE_ERR_UNSUPPORTED;
-  }
+  if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
+  if (variant == MOE_VARIANT_TC) return launch_geglu_tc(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
   return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
 }
 
@@ -93,15 +104,15 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
     set_error("%s: null pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
-  if (variant == MOE_VARIANT_TC) {
-    set_error("%s: tensor-core variant not built", fn);
-    return MOE_ERR_UNSUPPORTED;
-  }
+  if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
   const int64_t n = (int64_t)tiles->num_tokens * H;
   if (cudaMemsetAsync(y_acc_ws, 0, (size_t)n * sizeof(float), stream) != cudaSuccess) {
     return check_launch(fn);
   }
-  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
+  if (variant == MOE_VARIANT_TC)
+    st = launch_down_tc(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
+  else
+    st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
   if (st != MOE_OK) return st;
   return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
 }

@@ -61,6 +61,11 @@ def full_compare(d, tile_m, variant):
 @pytest.mark.parametrize("tile_m", [16, 32, 64, 128, 256])
 def test_tiny_layer_full(variant, tile_m):
     _variant_or_skip(variant)
+    if variant == mq.VARIANT_TC and tile_m > 128:
+        with pytest.raises(mq.MoeError) as ei:
+            run_layer(synth.make("tiny"), tile_m, variant)
+        assert ei.value.status == mq.MOE_ERR_UNSUPPORTED
+        return
     full_compare(synth.make("tiny"), tile_m, variant)
 
 
