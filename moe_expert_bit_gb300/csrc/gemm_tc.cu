@@ -1,7 +1,7 @@
 // tcgen05 tensor-core grouped GEMM over expert tiles, with the 4-bit affine
-// weights dequantised into shared memory (Layr-Labs/mlx PR #4, "What": a
-// gathered quantized matmul per sorted expert tile, affine 4-bit group-64
-// weights, bf16 activations).  Two modes share the kernel:
+// weights dequantised on the fly (Layr-Labs/mlx PR #4, "What": a gathered
+// quantized matmul per sorted expert tile, affine 4-bit group-64 weights,
+// bf16 activations).  Two modes share the kernel:
 //
 //   GEGLU: h[s, n] = gelu_tanh(sum_k Wg[e][n][k] x[t_s][k]) * sum_k Wu[e][n][k] x[t_s][k]
 //          (SharpAI/SwiftLM issue #236, "Still missing": the GeGLU product fused
@@ -9,21 +9,33 @@
 //   DOWN:  y_acc[t_s, n] += w_s * sum_i Wd[e][n][i] h[s][i]
 //          (weightedExpertSum / direct weighted un-sort as the GEMM epilogue)
 //
-// The weights are the MMA's M side ("swap AB"): one work unit is one expert
-// tile (<= 128 token rows, the MMA's N) times 128 weight rows, accumulated
-// over K in 64-wide k-blocks, one quantisation group per k-block.
+// The weights are the MMA's M side ("swap AB"): a work unit is one expert
+// tile (<= 128 token rows, the MMA's N rounded up to 16) times one n-block of
+// 128 weight rows, accumulated over K in 64-wide k-blocks, one quantisation
+// group each.  For GEGLU an n-block is 64 gate rows and the 64 matching up
+// rows, interleaved by 16 so that a gate row and its up row land in TMEM
+// lanes 16 apart within the same warp quarter.
+//
+// The dequantised weight tile is the MMA's A operand and lives in TMEM: the
+// dequant warps write it with tcgen05.st (a 128 x 64 bf16 k-block is 32
+// columns) and tcgen05.mma reads it from there, so weights never make a
+// round trip through shared memory.  TMEM: columns [0, 128) hold four A
+// stages, [128, 512) three fp32 accumulators of 128 columns.
 //
 // One persistent CTA per SM, 16 warps with fixed roles:
-//   warp 0      W producer: TMA of the packed nibbles (4 KB per k-block) and a
-//               bulk copy of the unit's bf16 scales and biases
+//   warp 0      W producer: TMA of the packed nibbles (128-byte row segments,
+//               four k-blocks per stage, 128-byte swizzle) and bulk copies of
+//               the unit's bf16 scales and biases
 //   warp 1      TMEM owner and MMA issuer (one thread issues tcgen05.mma)
-//   warp 2      X producer: TMA of the activation rows of the tile (B operand),
-//               gathered row by row through the sort permutation (GEGLU) or
-//               contiguous sorted rows of h (DOWN)
+//   warp 2      X producer: the tile's activation rows (B operand, shared
+//               memory, 128-byte swizzle) by TMA.  GEGLU gathers rows
+//               x[perm[s]/k] four at a time (tile::gather4); DOWN loads
+//               contiguous sorted rows of h in 16-row boxes.  Small tiles pack
+//               several k-blocks into one stage.
 //   warps 4-7   epilogue: TMEM -> registers -> GeGLU product -> h, or
-//               router-weighted fp32 reductions into y_acc
-//   warps 8-15  dequant: nibbles + scale/bias -> bf16 weights in the
-//               128-byte-swizzled K-major layout the MMA reads
+//               router-weighted fp32 vector reductions into y_acc
+//   warps 8-15  dequant, two warpgroups taking alternate k-blocks: nibbles +
+//               scale/bias -> bf16 weights -> TMEM
 // Rings of mbarriers connect the roles; every wait is bounded (a timeout
 // sets the status word to MOE_ERR_TIMEOUT and the CTA drains and exits).
 #include <cuda.h>
@@ -42,27 +54,41 @@ using namespace umma;
 
 constexpr int kThreads = 512;
 constexpr int kDeqWarp0 = 8;
-constexpr int kDeqThreads = 256;
 constexpr int kEpiWarp0 = 4;
-constexpr int kBM = 128;      // weight rows per unit (MMA M)
-constexpr int kMaxN = 128;    // token rows per unit (MMA N upper bound)
-constexpr int kNibStages = 8;
-constexpr int kAStages = 3;
-constexpr int kBStages = 4;
-constexpr int kNibBytes = kBM * 32;   // 64 nibbles per row per k-block
-constexpr int kABytes = kBM * 128;    // 64 bf16 per row per k-block
-constexpr int kBBytes = kMaxN * 128;
+constexpr int kBM = 128;      // weight rows per n-block (MMA M)
+constexpr int kMaxN = 128;    // token rows per tile (MMA N upper bound)
+constexpr int kNibKB = 4;       // k-blocks per nibble stage: 128-byte rows
+constexpr int kNibStages = 5;
+constexpr int kAStages = 4;   // TMEM A stages of 32 columns
+constexpr int kAccSets = 3;   // TMEM accumulators of 128 columns
+constexpr int kNibBytes = kBM * 32 * kNibKB;  // 128 rows x 128 bytes (4 k-blocks)
+constexpr int kBBytes = kMaxN * 128;  // one stage: kMaxN rows x 1 k-block, or fewer rows x more k-blocks
 constexpr int kAccCols = 128;
-constexpr int kTmemCols = 2 * kAccCols;
+constexpr int kTmemCols = 512;
 constexpr int kMaxK = 4096;
+constexpr int kEpiScratch = 32 * 32 * 4;  // per epilogue warp (DOWN)
+constexpr int kMaxSmem = 232448;          // opt-in shared memory per block
 
 enum Mode { GEGLU = 0, DOWN = 1 };
+
+template <int MODE>
+struct Cfg {
+  static constexpr int kBStages = 5;
+  static constexpr int kOffB = 0;
+  static constexpr int kOffNib = kOffB + kBStages * kBBytes;
+  static constexpr int kOffEpi = kOffNib + kNibStages * kNibBytes;
+  static constexpr int kOffSc = kOffEpi + (MODE == DOWN ? 4 * kEpiScratch : 0);
+};
+
+// bytes of one n-block's scales + biases: 128 rows x K/64 groups x 2 arrays x bf16
+__host__ __device__ constexpr int sc_bytes(int K) { return kBM * (K / 64) * 2 * 2; }
 
 struct Params {
   const int32_t *tiles;
   const int32_t *tile_count;
   const int32_t *perm;
   int32_t *status;
+  const uint16_t *x;       // GEGLU activations [T, H]
   const uint16_t *scales;  // [E, rows, K/64]
   const uint16_t *biases;
   const float *topk_weights;
@@ -72,29 +98,45 @@ struct Params {
   int32_t K;       // reduction length: H (GEGLU) or I (DOWN)
   int32_t N_out;   // I (GEGLU) or H (DOWN)
   int32_t rows_per_expert;  // 2I (GEGLU) or H (DOWN)
-  int32_t num_blocks;       // weight-row blocks per tile: I/64 (GEGLU) or ceil(H/128) (DOWN)
+  int32_t num_blocks;       // n-blocks per tile: I/64 (GEGLU) or ceil(H/128) (DOWN)
 };
 
 struct Smem {
   uint64_t nib_full[kNibStages], nib_empty[kNibStages];
   uint64_t a_full[kAStages], a_empty[kAStages];
-  uint64_t b_full[kBStages], b_empty[kBStages];
+  uint64_t b_full[5], b_empty[5];
   uint64_t sc_full[2], sc_empty[2];
-  uint64_t acc_full[2], acc_empty[2];
+  uint64_t acc_full[kAccSets], acc_empty[kAccSets];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
+  int32_t tok[kMaxN];
 };
 
-// byte offsets inside the 1024-aligned dynamic shared memory
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kAStages * kABytes;
-constexpr int kOffNib = kOffB + kBStages * kBBytes;
-constexpr int kOffSc = kOffNib + kNibStages * kNibBytes;
+template <int MODE>
+__host__ __device__ constexpr int smem_bytes(int K) {
+  return Cfg<MODE>::kOffSc + 2 * sc_bytes(K) + (int)sizeof(Smem) + 1024;
+}
 
-__host__ __device__ constexpr int sc_buf_bytes(int K) { return kBM * (K / 64) * 2 * 2; }
-__host__ __device__ constexpr int smem_total(int K) {
-  return kOffSc + 2 * sc_buf_bytes(K) + (int)sizeof(Smem) + 1024;
+struct Unit {
+  int e, row0, R, nb;
+};
+
+__device__ __forceinline__ Unit get_unit(const Params &p, int u) {
+  Unit U;
+  const int tile = u / p.num_blocks;
+  U.nb = u - tile * p.num_blocks;
+  U.e = p.tiles[3 * tile];
+  U.row0 = p.tiles[3 * tile + 1];
+  U.R = p.tiles[3 * tile + 2];
+  return U;
+}
+
+// smallest power of two >= max(R, 16): rows reserved per k-block in a B stage
+__device__ __forceinline__ int n_alloc_of(int R) {
+  int n = 16;
+  while (n < R) n <<= 1;
+  return n;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -116,7 +158,7 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t mask, uint32_t b
 // permute, OR-ed into the bf16 pattern of 128.0 (giving 128 + q exactly),
 // 128 is subtracted exactly, and one bf16x2 fma applies the affine map.
 __device__ __forceinline__ void dequant8(uint32_t q, __nv_bfloat162 s2, __nv_bfloat162 b2,
-                                         uint32_t (&out)[4]) {
+                                         uint32_t *out) {
   const uint32_t z = q >> 4;
   const uint32_t k128 = 0x43004300u;
 #pragma unroll
@@ -131,15 +173,10 @@ __device__ __forceinline__ void dequant8(uint32_t q, __nv_bfloat162 s2, __nv_bfl
   }
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
                : "memory");
-}
-
-__device__ __forceinline__ void red_add_f32(float *p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 template <int MODE>
@@ -149,13 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  const int G = p.K / 64;  // groups per row == k-blocks per unit
-  const int scb = sc_buf_bytes(p.K);
-  Smem &S = *reinterpret_cast<Smem *>(smem + kOffSc + 2 * scb);
-  uint8_t *ringA = smem + kOffA;
-  uint8_t *ringB = smem + kOffB;
-  uint8_t *ringN = smem + kOffNib;
-  uint8_t *ringS = smem + kOffSc;
+  using C = Cfg<MODE>;
+  constexpr int kBStages = C::kBStages;
+  const int G = p.K / 64;  // k-blocks per unit (one quantisation group each)
+  const int scb = sc_bytes(p.K);
+  Smem &S = *reinterpret_cast<Smem *>(smem + C::kOffSc + 2 * scb);
+  uint8_t *ringB = smem + C::kOffB;
+  uint8_t *ringN = smem + C::kOffNib;
+  uint8_t *ringS = smem + C::kOffSc;  // 2 buffers of one n-block's scales + biases
   volatile int *abort = &S.abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,10 +204,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNibStages; ++i) {
       mbar_init(&S.nib_full[i], 1);
-      mbar_init(&S.nib_empty[i], kDeqThreads / 32);
+      mbar_init(&S.nib_empty[i], 8);  // both dequant warpgroups
     }
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&S.a_full[i], kDeqThreads / 32);
+      mbar_init(&S.a_full[i], 4);
       mbar_init(&S.a_empty[i], 1);
     }
     for (int i = 0; i < kBStages; ++i) {
@@ -178,7 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.sc_full[i], 1);
-      mbar_init(&S.sc_empty[i], kDeqThreads / 32);
+      mbar_init(&S.sc_empty[i], 8);  // both dequant warpgroups
+    }
+    for (int i = 0; i < kAccSets; ++i) {
       mbar_init(&S.acc_full[i], 1);
       mbar_init(&S.acc_empty[i], 4);
     }
@@ -198,130 +238,147 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
+  const uint32_t tmem_acc = tmem_base + kAStages * 32;
 
   if (warp == 0) {
-    // ------------------------------------------------ W producer
+    // ------------------------------------------------ W producer: scales + packed nibbles
     if (lane == 0) {
-      uint32_t it = 0, it_sc = 0;
+      uint32_t it = 0, isc = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int tile = u / p.num_blocks, nb = u - tile * p.num_blocks;
-        const int e = p.tiles[3 * tile];
-        const int sb = it_sc & 1;
-        if (!(ok = mbar_wait(&S.sc_empty[sb], ((it_sc >> 1) & 1) ^ 1, abort))) break;
-        uint8_t *dst = ringS + sb * scb;
-        const int row_bytes = G * 2;
+      const int row_bytes = G * 2;
+      for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++isc) {
+        const Unit U = get_unit(p, u);
+        const int set = isc & 1;
+        if (!(ok = mbar_wait(&S.sc_empty[set], ((isc >> 1) & 1) ^ 1, abort))) break;
+        uint8_t *dst = ringS + set * scb;
         if (MODE == GEGLU) {
-          const int64_t rg = (int64_t)e * p.rows_per_expert + nb * 64;
-          const int64_t ru = rg + p.N_out;  // up rows start I rows later
-          const uint32_t part = 64 * row_bytes;
-          mbar_arrive_expect_tx(&S.sc_full[sb], 4 * part);
-          bulk_load(dst, p.scales + rg * G, part, &S.sc_full[sb]);
-          bulk_load(dst + part, p.scales + ru * G, part, &S.sc_full[sb]);
-          bulk_load(dst + 2 * part, p.biases + rg * G, part, &S.sc_full[sb]);
-          bulk_load(dst + 3 * part, p.biases + ru * G, part, &S.sc_full[sb]);
+          const int64_t rg = (int64_t)U.e * p.rows_per_expert + U.nb * 64;
+          const int64_t ru = rg + p.N_out;
+          const uint32_t part = 64u * row_bytes;
+          mbar_arrive_expect_tx(&S.sc_full[set], 4 * part);
+          bulk_load(dst, p.scales + rg * G, part, &S.sc_full[set]);
+          bulk_load(dst + part, p.scales + ru * G, part, &S.sc_full[set]);
+          bulk_load(dst + 2 * part, p.biases + rg * G, part, &S.sc_full[set]);
+          bulk_load(dst + 3 * part, p.biases + ru * G, part, &S.sc_full[set]);
         } else {
-          const int n0 = nb * kBM;
-          const int rows = min(kBM, p.N_out - n0);
-          const int64_t r0 = (int64_t)e * p.rows_per_expert + n0;
-          const uint32_t part = rows * row_bytes;
-          mbar_arrive_expect_tx(&S.sc_full[sb], 2 * part);
-          bulk_load(dst, p.scales + r0 * G, part, &S.sc_full[sb]);
-          bulk_load(dst + kBM * row_bytes, p.biases + r0 * G, part, &S.sc_full[sb]);
+          const int rows = min(kBM, p.N_out - U.nb * kBM);
+          const int64_t r0 = (int64_t)U.e * p.rows_per_expert + U.nb * kBM;
+          const uint32_t part = (uint32_t)rows * row_bytes;
+          mbar_arrive_expect_tx(&S.sc_full[set], 2 * part);
+          bulk_load(dst, p.scales + r0 * G, part, &S.sc_full[set]);
+          bulk_load(dst + kBM * row_bytes, p.biases + r0 * G, part, &S.sc_full[set]);
         }
-        ++it_sc;
-        for (int kb = 0; kb < G; ++kb, ++it) {
+        for (int kb0 = 0; kb0 < G; kb0 += kNibKB, ++it) {
           const int st = it % kNibStages;
           if (!(ok = mbar_wait(&S.nib_empty[st], ((it / kNibStages) & 1) ^ 1, abort))) break;
           mbar_arrive_expect_tx(&S.nib_full[st], kNibBytes);
           uint8_t *nd = ringN + st * kNibBytes;
           if (MODE == GEGLU) {
-            const int rg = e * p.rows_per_expert + nb * 64;
-            tma_load_2d(nd, &tmap_w, kb * 8, rg, &S.nib_full[st]);
-            tma_load_2d(nd + kNibBytes / 2, &tmap_w, kb * 8, rg + p.N_out, &S.nib_full[st]);
+            const int rg = U.e * p.rows_per_expert + U.nb * 64;
+            tma_load_2d(nd, &tmap_w, kb0 * 8, rg, &S.nib_full[st]);
+            tma_load_2d(nd + kNibBytes / 2, &tmap_w, kb0 * 8, rg + p.N_out, &S.nib_full[st]);
           } else {
-            tma_load_2d(nd, &tmap_w, kb * 8, e * p.rows_per_expert + nb * kBM, &S.nib_full[st]);
+            tma_load_2d(nd, &tmap_w, kb0 * 8, U.e * p.rows_per_expert + U.nb * kBM,
+                        &S.nib_full[st]);
           }
         }
       }
       // drain: wait (bounded) for copies still in flight before the CTA exits
       for (uint32_t i = (it > kNibStages ? it - kNibStages : 0); i < it; ++i)
         mbar_wait(&S.nib_full[i % kNibStages], (i / kNibStages) & 1, nullptr, 200000000ull);
-      if (it_sc > 0)
-        for (uint32_t i = (it_sc > 2 ? it_sc - 2 : 0); i < it_sc; ++i)
-          mbar_wait(&S.sc_full[i & 1], (i >> 1) & 1, nullptr, 200000000ull);
+      for (uint32_t i = (isc > 2 ? isc - 2 : 0); i < isc; ++i)
+        mbar_wait(&S.sc_full[i & 1], (i >> 1) & 1, nullptr, 200000000ull);
     }
   } else if (warp == 2) {
-    // ------------------------------------------------ X producer (B operand rows)
+    // ------------------------------------------------ X producer: B operand rows
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const int tile = u / p.num_blocks;
-      const int row0 = p.tiles[3 * tile + 1], R = p.tiles[3 * tile + 2];
-      int src_row[kMaxN / 32];
-#pragma unroll
-      for (int m = 0; m < kMaxN / 32; ++m) {
-        const int j = lane + 32 * m;
-        if (MODE == GEGLU)
-          src_row[m] = (j < R) ? p.perm[row0 + j] / p.top_k : 0;
-        else
-          src_row[m] = row0 + 16 * j;  // 16-row boxes of sorted h
-      }
-      const int nbox = (MODE == GEGLU) ? R : (R + 15) / 16;
-      const uint32_t bytes = (MODE == GEGLU) ? R * 128u : nbox * 16u * 128u;
-      for (int kb = 0; kb < G; ++kb, ++it) {
-        const int st = it % kBStages;
-        if (!(ok = mbar_wait(&S.b_empty[st], ((it / kBStages) & 1) ^ 1, abort))) break;
-        if (lane == 0) mbar_arrive_expect_tx(&S.b_full[st], bytes);
+      const Unit U = get_unit(p, u);
+      const int na = n_alloc_of(U.R);
+      const int kbps = kMaxN / na;  // k-blocks per stage
+      const int nst = (G + kbps - 1) / kbps;
+      if (MODE == GEGLU) {
         __syncwarp();
-        uint8_t *bd = ringB + st * kBBytes;
-#pragma unroll
-        for (int m = 0; m < kMaxN / 32; ++m) {
-          const int j = lane + 32 * m;
-          if (j < nbox) {
-            if (MODE == GEGLU)
-              tma_load_2d(bd + j * 128, &tmap_x, kb * 64, src_row[m], &S.b_full[st]);
-            else
-              tma_load_2d(bd + j * 16 * 128, &tmap_x, kb * 64, src_row[m], &S.b_full[st]);
+        for (int r = lane; r < U.R; r += 32) S.tok[r] = p.perm[U.row0 + r] / p.top_k;
+        __syncwarp();
+      }
+      for (int si = 0; si < nst; ++si, ++it) {
+        const int sb = it % kBStages;
+        ok = mbar_wait(&S.b_empty[sb], ((it / kBStages) & 1) ^ 1, abort);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;  // keep the warp converged
+        const int kb0 = si * kbps;
+        const int nk = min(kbps, G - kb0);
+        uint8_t *stage = ringB + sb * kBBytes;
+        if (MODE == GEGLU) {
+          // gathered rows, four per TMA (one-row boxes); the last group repeats a valid row
+          const int ng = (U.R + 3) / 4;
+          if (lane == 0) mbar_arrive_expect_tx(&S.b_full[sb], (uint32_t)(nk * ng * 512));
+          __syncwarp();
+          for (int i = lane; i < nk * ng; i += 32) {
+            const int kk = i / ng, g4 = i - kk * ng;
+            const int j = 4 * g4;
+            tma_gather4(stage + kk * na * 128 + j * 128, &tmap_x, (kb0 + kk) * 64,
+                        S.tok[j], S.tok[min(j + 1, U.R - 1)], S.tok[min(j + 2, U.R - 1)],
+                        S.tok[min(j + 3, U.R - 1)], &S.b_full[sb]);
+          }
+        } else {
+          const int nbox = na / 16;
+          if (lane == 0) mbar_arrive_expect_tx(&S.b_full[sb], (uint32_t)(nk * na * 128));
+          __syncwarp();
+          for (int i = lane; i < nk * nbox; i += 32) {
+            const int kk = i / nbox, bx = i - kk * nbox;
+            tma_load_2d(stage + kk * na * 128 + bx * 2048, &tmap_x, (kb0 + kk) * 64,
+                        U.row0 + bx * 16, &S.b_full[sb]);
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0)
+    if (lane == 0) {
       for (uint32_t i = (it > kBStages ? it - kBStages : 0); i < it; ++i)
         mbar_wait(&S.b_full[i % kBStages], (i / kBStages) & 1, nullptr, 200000000ull);
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t ia = 0, ib = 0, iacc = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-        const int tile = u / p.num_blocks;
-        const int R = p.tiles[3 * tile + 2];
-        const uint32_t N = (uint32_t)max(16, (R + 15) & ~15);
+        const Unit U = get_unit(p, u);
+        const uint32_t N = (uint32_t)max(16, (U.R + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(kBM, N);
-        const int buf = iacc & 1;
-        if (!(ok = mbar_wait(&S.acc_empty[buf], ((iacc >> 1) & 1) ^ 1, abort))) break;
+        const int na = n_alloc_of(U.R);
+        const int kbps = kMaxN / na;
+        const int set = iacc % kAccSets;
+        if (!(ok = mbar_wait(&S.acc_empty[set], ((iacc / kAccSets) & 1) ^ 1, abort))) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + buf * kAccCols;
-        for (int kb = 0; kb < G; ++kb, ++ia, ++ib) {
-          const int sa = ia % kAStages, sbb = ib % kBStages;
-          if (!(ok = mbar_wait(&S.a_full[sa], (ia / kAStages) & 1, abort))) break;
-          if (!(ok = mbar_wait(&S.b_full[sbb], (ib / kBStages) & 1, abort))) break;
-          tc_fence_after();
-          const uint32_t a0 = smem_addr(ringA + sa * kABytes);
-          const uint32_t b0 = smem_addr(ringB + sbb * kBBytes);
-#pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16) {
-            umma_f16(d_tmem, smem_desc_k128(a0 + 32 * k16), smem_desc_k128(b0 + 32 * k16), idesc,
-                     (kb | k16) != 0);
+        const uint32_t d_tmem = tmem_acc + (uint32_t)(set * kAccCols);
+        int sb = 0;
+        for (int kb = 0; kb < G; ++kb, ++ia) {
+          const int kk = kb % kbps;
+          if (kk == 0) {
+            sb = ib % kBStages;
+            if (!(ok = mbar_wait(&S.b_full[sb], (ib / kBStages) & 1, abort))) break;
           }
+          const int sa = ia % kAStages;
+          if (!(ok = mbar_wait(&S.a_full[sa], (ia / kAStages) & 1, abort))) break;
+          tc_fence_after();
+          const uint32_t a_tmem = tmem_base + (uint32_t)(sa * 32);
+          const uint32_t b0 = smem_addr(ringB + sb * kBBytes) + (uint32_t)(kk * na * 128);
+#pragma unroll
+          for (int k16 = 0; k16 < 4; ++k16)
+            umma_f16_ta(d_tmem, a_tmem + 8 * k16, smem_desc_k128(b0 + 32 * k16), idesc,
+                        (kb | k16) != 0);
           umma_commit(&S.a_empty[sa]);
-          umma_commit(&S.b_empty[sbb]);
+          if (kk == kbps - 1 || kb == G - 1) {
+            umma_commit(&S.b_empty[sb]);
+            ++ib;
+          }
         }
         if (!ok) break;
-        umma_commit(&S.acc_full[buf]);
+        umma_commit(&S.acc_full[set]);
         ++iacc;
       }
       // every MMA issued by this thread has completed before TMEM is released
@@ -332,21 +389,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // ------------------------------------------------ epilogue
     const int q = warp - kEpiWarp0;  // TMEM lane quarter of this warp
+    float *scratch = reinterpret_cast<float *>(smem + C::kOffEpi + q * kEpiScratch);
     uint32_t iacc = 0;
     for (int u = blockIdx.x; u < total_units; u += gridDim.x, ++iacc) {
-      const int tile = u / p.num_blocks, nb = u - tile * p.num_blocks;
-      const int row0 = p.tiles[3 * tile + 1], R = p.tiles[3 * tile + 2];
-      const int buf = iacc & 1;
-      if (!mbar_wait(&S.acc_full[buf], (iacc >> 1) & 1, abort)) break;
+      const Unit U = get_unit(p, u);
+      const int set = iacc % kAccSets;
+      if (!mbar_wait(&S.acc_full[set], (iacc / kAccSets) & 1, abort)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * kAccCols;
-      for (int c0 = 0; c0 < R; c0 += 32) {
+      const uint32_t tbase = tmem_acc + ((uint32_t)(32 * q) << 16) + (uint32_t)(set * kAccCols);
+      for (int c0 = 0; c0 < U.R; c0 += 32) {
         uint32_t v[32];
         tmem_ld_32x32b_x32(tbase + c0, v);
         tmem_ld_wait();
         if (MODE == GEGLU) {
           // lanes 0-15 hold gate rows, lanes 16-31 the matching up rows
-          const int n = nb * 64 + 16 * q + (lane & 15);
+          const int n = U.nb * 64 + 16 * q + (lane & 15);
           const int odd = lane >> 4;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -354,88 +411,106 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
             const float g = odd ? other : mine;
             const float uu = odd ? mine : other;
-            if ((j & 1) == odd && c0 + j < R) {
+            if ((j & 1) == odd && c0 + j < U.R) {
               const float hv = gelu_tanh(g) * uu;
-              p.h[(int64_t)(row0 + c0 + j) * p.N_out + n] =
+              p.h[(int64_t)(U.row0 + c0 + j) * p.N_out + n] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
           }
         } else {
-          const int n = nb * kBM + 32 * q + lane;
-          const int col = c0 + lane;
+          // token and router weight of column c0 + lane
           int tok = 0;
           float w = 0.f;
-          if (col < R) {
-            const int a = p.perm[row0 + col];
+          if (c0 + lane < U.R) {
+            const int a = p.perm[U.row0 + c0 + lane];
             tok = a / p.top_k;
             w = p.topk_weights[a];
           }
+          // transpose through shared memory: [column][32 rows]
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 32; ++j) scratch[j * 32 + lane] = __uint_as_float(v[j]);
+          __syncwarp();
+          const int jj = lane >> 3, m = lane & 7;
+          const int n = U.nb * kBM + 32 * q + 4 * m;
+#pragma unroll
+          for (int pass = 0; pass < 8; ++pass) {
+            const int j = pass * 4 + jj;
+            const float4 f = *reinterpret_cast<const float4 *>(scratch + j * 32 + 4 * m);
             const int tj = __shfl_sync(0xffffffffu, tok, j);
             const float wj = __shfl_sync(0xffffffffu, w, j);
-            if (c0 + j < R && n < p.N_out)
-              red_add_f32(p.y_acc + (int64_t)tj * p.N_out + n, wj * __uint_as_float(v[j]));
+            if (c0 + j < U.R && n < p.N_out)
+              red_add_v4(p.y_acc + (int64_t)tj * p.N_out + n, wj * f.x, wj * f.y, wj * f.z,
+                         wj * f.w);
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty[buf]);
+      if (lane == 0) mbar_arrive(&S.acc_empty[set]);
     }
   } else if (warp >= kDeqWarp0) {
-    // ------------------------------------------------ dequant
-    const int t = threadIdx.x - kDeqWarp0 * 32;
-    const int r = t >> 1, half = t & 1;
+    // ------------------------------------------------ dequant (two warpgroups)
+    const int grp = (warp - kDeqWarp0) >> 2;  // takes the k-blocks of its parity
+    const int wq = warp & 3;                  // TMEM lane quarter
+    const int r = 32 * wq + lane;             // A row == TMEM lane
     int nibrow;
     if (MODE == GEGLU) {
-      const int qq = r >> 5, i = r & 31;
-      nibrow = (i < 16) ? (16 * qq + i) : (64 + 16 * qq + (i - 16));
+      const int i = lane;
+      nibrow = (i < 16) ? (16 * wq + i) : (64 + 16 * wq + (i - 16));
     } else {
       nibrow = r;
     }
-    const uint32_t a_row_off = (uint32_t)r * 128u;
-    const uint32_t sw = (uint32_t)(r & 7);
-    uint32_t in = 0, ia = 0, isc = 0;
+    const uint32_t a_lane = (uint32_t)(32 * wq) << 16;
+    const uint32_t sw = (uint32_t)(nibrow & 7);  // 128-byte swizzle of the nibble rows
+    uint32_t in = 0, isc = 0, ist = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
-      const int sb = isc & 1;
-      if (!(ok = mbar_wait(&S.sc_full[sb], (isc >> 1) & 1, abort))) break;
-      const uint16_t *srow = reinterpret_cast<const uint16_t *>(ringS + sb * scb) + nibrow * G;
-      const uint16_t *brow = srow + kBM * G;
-      for (int kb = 0; kb < G; ++kb, ++in, ++ia) {
-        const int sn = in % kNibStages;
-        if (!(ok = mbar_wait(&S.nib_full[sn], (in / kNibStages) & 1, abort))) break;
-        const uint4 qv =
-            *reinterpret_cast<const uint4 *>(ringN + sn * kNibBytes + nibrow * 32 + half * 16);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.nib_empty[sn]);
-        const uint16_t s16 = srow[kb], b16 = brow[kb];
-        const uint32_t s2u = (uint32_t)s16 | ((uint32_t)s16 << 16);
-        const uint32_t b2u = (uint32_t)b16 | ((uint32_t)b16 << 16);
-        const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
-        const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&b2u);
-        uint32_t w0[4], w1[4], w2[4], w3[4];
-        dequant8(qv.x, s2, b2, w0);
-        dequant8(qv.y, s2, b2, w1);
-        dequant8(qv.z, s2, b2, w2);
-        dequant8(qv.w, s2, b2, w3);
-        const int sa = ia % kAStages;
-        if (!(ok = mbar_wait(&S.a_empty[sa], ((ia / kAStages) & 1) ^ 1, abort))) break;
-        const uint32_t abase = smem_addr(ringA + sa * kABytes) + a_row_off;
-        const uint32_t c = 4u * half;  // first 16-byte chunk of this half row
-        st_shared_v4(abase + (((c + 0) ^ sw) << 4), w0[0], w0[1], w0[2], w0[3]);
-        st_shared_v4(abase + (((c + 1) ^ sw) << 4), w1[0], w1[1], w1[2], w1[3]);
-        st_shared_v4(abase + (((c + 2) ^ sw) << 4), w2[0], w2[1], w2[2], w2[3]);
-        st_shared_v4(abase + (((c + 3) ^ sw) << 4), w3[0], w3[1], w3[2], w3[3]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.a_full[sa]);
+    for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x, ++isc) {
+      const int set = isc & 1;
+      if (!(ok = mbar_wait(&S.sc_full[set], (isc >> 1) & 1, abort))) break;
+      const uint16_t *sc = reinterpret_cast<const uint16_t *>(ringS + set * scb) + nibrow * G;
+      for (int kb = 0; kb < G; ++kb, ++in) {
+        const int kk = kb % kNibKB;
+        const int sn = ist % kNibStages;
+        // both warpgroups wait for every stage, so that their arrivals on the
+        // empty barrier always belong to the stage's current phase
+        if (kk == 0 && !(ok = mbar_wait(&S.nib_full[sn], (ist / kNibStages) & 1, abort))) break;
+        if ((int)(in & 1) == grp) {
+          const uint8_t *row = ringN + sn * kNibBytes + nibrow * 128;
+          const uint4 q0 = *reinterpret_cast<const uint4 *>(row + (((2 * kk) ^ sw) << 4));
+          const uint4 q1 = *reinterpret_cast<const uint4 *>(row + (((2 * kk + 1) ^ sw) << 4));
+          const uint16_t s16 = sc[kb], b16 = sc[kBM * G + kb];
+          const uint32_t s2u = (uint32_t)s16 | ((uint32_t)s16 << 16);
+          const uint32_t b2u = (uint32_t)b16 | ((uint32_t)b16 << 16);
+          const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&b2u);
+          uint32_t w[32];
+          dequant8(q0.x, s2, b2, w + 0);
+          dequant8(q0.y, s2, b2, w + 4);
+          dequant8(q0.z, s2, b2, w + 8);
+          dequant8(q0.w, s2, b2, w + 12);
+          dequant8(q1.x, s2, b2, w + 16);
+          dequant8(q1.y, s2, b2, w + 20);
+          dequant8(q1.z, s2, b2, w + 24);
+          dequant8(q1.w, s2, b2, w + 28);
+          const int sa = in % kAStages;
+          if (!(ok = mbar_wait(&S.a_empty[sa], ((in / kAStages) & 1) ^ 1, abort))) break;
+          tc_fence_after();
+          tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)(sa * 32), w);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.a_full[sa]);
+        }
+        if (kk == kNibKB - 1 || kb == G - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&S.nib_empty[sn]);
+          ++ist;
+        }
       }
       if (!ok) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.sc_empty[sb]);
-      ++isc;
+      if (lane == 0) mbar_arrive(&S.sc_empty[set]);
     }
   }
 
@@ -494,15 +569,18 @@ static int num_sms() {
 
 template <int MODE>
 static moe_status launch(const CUtensorMap &mw, const CUtensorMap &mx, const Params &p,
-                         int max_units, cudaStream_t stream, const char *what) {
-  const int smem = smem_total(p.K);
-  static int configured_smem[2] = {0, 0};
-  if (configured_smem[MODE] < smem) {
+                         const moe_tiles_t &t, cudaStream_t stream, const char *what) {
+  const int smem = smem_bytes<MODE>(p.K);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int configured[64];
+  if (dev < 0 || dev >= 64 || configured[dev] < smem) {
     if (cudaFuncSetAttribute(gemm_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
       return check_launch(what);
-    configured_smem[MODE] = smem;
+    if (dev >= 0 && dev < 64) configured[dev] = smem;
   }
+  const int max_units = t.max_tiles * p.num_blocks;
   int grid = num_sms();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
@@ -515,6 +593,8 @@ static moe_status launch(const CUtensorMap &mw, const CUtensorMap &mx, const Par
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m) {
   if (tile_m > tc::kMaxN) return MOE_ERR_UNSUPPORTED;
   if (H > tc::kMaxK || I > tc::kMaxK) return MOE_ERR_UNSUPPORTED;
+  if (tc::smem_bytes<tc::GEGLU>(H) > tc::kMaxSmem || tc::smem_bytes<tc::DOWN>(I) > tc::kMaxSmem)
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -524,7 +604,7 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
   const char *what = "moe_gather_qmm_geglu (tensor cores)";
   CUtensorMap mw, mx;
   if (!tc::make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wgu, H / 8,
-                       (uint64_t)t.num_experts * 2 * I, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                       (uint64_t)t.num_experts * 2 * I, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, t.num_tokens, 64, 1,
                        CU_TENSOR_MAP_SWIZZLE_128B)) {
     set_error("%s: tensor map encoding failed", what);
@@ -538,13 +618,14 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
   p.status = t.status;
   p.scales = Sgu;
   p.biases = Bgu;
+  p.x = x;
   p.h = h;
   p.top_k = t.top_k;
   p.K = H;
   p.N_out = I;
   p.rows_per_expert = 2 * I;
   p.num_blocks = I / 64;
-  return tc::launch<tc::GEGLU>(mw, mx, p, t.max_tiles * p.num_blocks, stream, what);
+  return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
 }
 
 moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
@@ -553,7 +634,7 @@ moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_
   const char *what = "moe_gather_qmm_down_unsort (tensor cores)";
   CUtensorMap mw, mx;
   if (!tc::make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wd, I / 8,
-                       (uint64_t)t.num_experts * H, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                       (uint64_t)t.num_experts * H, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !tc::make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hin, I, t.num_assignments, 64,
                        16, CU_TENSOR_MAP_SWIZZLE_128B)) {
     set_error("%s: tensor map encoding failed", what);
@@ -574,7 +655,7 @@ moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_
   p.N_out = H;
   p.rows_per_expert = H;
   p.num_blocks = (H + tc::kBM - 1) / tc::kBM;
-  return tc::launch<tc::DOWN>(mw, mx, p, t.max_tiles * p.num_blocks, stream, what);
+  return tc::launch<tc::DOWN>(mw, mx, p, t, stream, what);
 }
 
 }  // namespace moeqmm

@@ -1,165 +1,306 @@
-// CUDA-core weight-streaming kernels for the two projections (the GEMV-style
-// variant).  One warp owns one output row of one expert tile and streams
-// that row's packed nibbles once, applying each dequantised weight to the
-// tile's activation rows (up to kRows at a time, staged in shared memory).
-// Suited to decode, where a tile holds one or two rows and the layer is a
-// pure weight stream.
+// Weight-streaming kernels for the two projections when expert tiles are
+// small (decode): the GEMV-style variant.  The layer is then a pure stream of
+// packed 4-bit weights from HBM, so what counts is the work per weight on
+// the CUDA cores, not matrix throughput.
 //
 //   gate/up:  h[s, n] = gelu_tanh(sum_k Wg[e][n][k] x_s[k]) * sum_k Wu[e][n][k] x_s[k]
 //   down:     y_acc[t, n] += w_a * sum_i Wd[e][n][i] h[s, i],  a = perm[s], t = a / top_k
 // with w = scale * q + bias per 64-group (Layr-Labs/mlx PR #4, "What";
 // SharpAI/SwiftLM issue #236, "Still missing" and "Already on main").
+//
+// Per 64-wide group g of one weight row the dot product splits as
+//   sum_k w_k x_k = s_g * D_g + (b_g - 128 s_g) * X_g,
+//   D_g = sum_k (128 + q_k) x_k,   X_g = sum_k x_k,
+// and 128 + q is exact in bf16: OR-ing a nibble into the bf16 pattern of
+// 128.0 produces it, and one lop3 on a shifted packed word produces two of
+// them at once (nibbles j and j+4).  D_g is one warp-level bf16 MMA
+// (m16n8k16, fp32 accumulate) per 16 k: the MMA is used as the dot-product
+// engine so that the CUDA cores only unpack nibbles (under one instruction
+// per weight) and fold each group once.  The k order inside an MMA is a
+// permutation of the group's k; the activations are staged in shared memory
+// in the same permuted order, which leaves the sum unchanged.
+//
+// A warp owns 16 weight rows (the MMA's M) and up to 4 activation rows per
+// pass (half of the MMA's N).  Its rows are loaded whole into shared memory
+// with bulk copies, so that DRAM sees long sequential runs, and stay there
+// while the passes over the tile's activation rows run.  For gate/up the 16 rows are 8 gate rows and the 8 matching up rows, so
+// each lane ends with a gate value and its up value side by side.
 #include "common.cuh"
 #include "kernels.h"
+#include "umma.cuh"
 
 namespace moeqmm {
 
-constexpr int kGemvWarps = 8;
-constexpr int kGemvThreads = kGemvWarps * 32;
-constexpr int kRows = 4;  // activation rows per pass
+constexpr int kTok = 4;  // activation rows staged per pass (MMA columns 4-7 repeat row 3)
 
-// 8 consecutive bf16 (one uint4) -> fp32
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+  return d;
+}
+
+// bf16x2 {128 + q_p (low half), 128 + q_{p+4} (high half)} of one packed word
+__device__ __forceinline__ uint32_t pair128(uint32_t word, int p) {
+  return lop_and_or(word >> (4 * p), 0x000F000Fu, 0x43004300u);
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ float bf16f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// In place: each 16-byte block c (activations 8c'..8c'+7 of group g, c' = c % 8) becomes the
+// MMA B fragments of lane slot t = c'/2 for m = 2(c'%2) + {0,1}: {x0,x4 | x1,x5} and
+// {x2,x6 | x3,x7}; the block's sum goes into the group sum.  Rows >= R are zeroed.
+// Run by `nthreads` threads (a multiple of 32, starting at thread 0).
+__device__ __forceinline__ void permute_rows(uint8_t *xb, float *xs, int xrb, int G, int R,
+                                             int nthreads) {
+  for (int i = threadIdx.x; i < kTok * G * 8; i += nthreads) {
+    const int j = i / (G * 8), rem = i - j * G * 8, g = rem >> 3;
+    uint4 *blk = reinterpret_cast<uint4 *>(xb + (size_t)j * xrb + rem * 16);
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    if (j < R) q = *blk;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    auto el = [&](int e) -> uint32_t { return (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu); };
+    float part = 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    f[2 * i] = __uint_as_float(w[i] << 16);
-    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    for (int e = 0; e < 8; ++e) part += __uint_as_float(el(e) << 16);
+    uint4 o;
+    o.x = el(0) | (el(4) << 16);
+    o.y = el(1) | (el(5) << 16);
+    o.z = el(2) | (el(6) << 16);
+    o.w = el(3) | (el(7) << 16);
+    *blk = o;
+    // the 8 blocks of one (row, group) are 8 consecutive lanes
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    part += __shfl_xor_sync(0xffffffffu, part, 4);
+    if ((rem & 7) == 0) xs[j * G + g] = part;
   }
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
+// Dot products of a warp's 16 weight rows with the staged activation rows.
+//   wrows: the warp's 16 packed weight rows in shared memory (rows 0-7: MMA rows g,
+//          rows 8-15: MMA rows g + 8), row stride ws
+//   scA / scB: scale rows of MMA rows g and g+8 in shared memory (biases at +bofs)
+// acc[0], acc[1]: row g with activation rows 2t, 2t+1; acc[2], acc[3]: row g+8.
+__device__ __forceinline__ void warp_rows_dot(const uint8_t *wrows, int ws, const uint16_t *scA,
+                                              const uint16_t *scB, int bofs, const uint8_t *xb,
+                                              int xrb, const float *xs, int G, float (&acc)[4]) {
+  const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
+  // B column gq = activation row gq; columns past the staged rows repeat the last one
+  const uint8_t *xrow = xb + (size_t)min(gq, kTok - 1) * xrb + t * 32;
+  const float *xs0 = xs + min(2 * t, kTok - 1) * G, *xs1 = xs + min(2 * t + 1, kTok - 1) * G;
+  const uint8_t *rA = wrows + gq * ws + t * 8, *rB = rA + 8 * ws;
+#pragma unroll 2
+  for (int g = 0; g < G; ++g) {
+    const uint2 A = *reinterpret_cast<const uint2 *>(rA + g * 32);
+    const uint2 B = *reinterpret_cast<const uint2 *>(rB + g * 32);
+    const uint2 *xf = reinterpret_cast<const uint2 *>(xrow + g * 128);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-  return v;
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t wA = (m >> 1) ? A.y : A.x;
+      const uint32_t wB = (m >> 1) ? B.y : B.x;
+      const int p0 = 2 * (m & 1);
+      const uint32_t a[4] = {pair128(wA, p0), pair128(wB, p0), pair128(wA, p0 + 1),
+                             pair128(wB, p0 + 1)};
+      const uint2 f = xf[m];
+      mma_bf16_16816(d, a, f.x, f.y, d);
+    }
+    const float s_a = bf16f(scA[g]), s_b = bf16f(scB[g]);
+    const float c_a = fmaf(-128.f, s_a, bf16f(scA[bofs + g]));
+    const float c_b = fmaf(-128.f, s_b, bf16f(scB[bofs + g]));
+    const float x0 = xs0[g], x1 = xs1[g];
+    acc[0] = fmaf(s_a, d[0], fmaf(c_a, x0, acc[0]));
+    acc[1] = fmaf(s_a, d[1], fmaf(c_a, x1, acc[1]));
+    acc[2] = fmaf(s_b, d[2], fmaf(c_b, x0, acc[2]));
+    acc[3] = fmaf(s_b, d[3], fmaf(c_b, x1, acc[3]));
+  }
 }
 
-// grid: (max_tiles, ceil(I / kGemvWarps)); dynamic smem: kRows * H bf16
-__global__ void __launch_bounds__(kGemvThreads)
-    geglu_gemv_kernel(const uint16_t *__restrict__ x, const uint32_t *__restrict__ Wgu,
-                      const uint16_t *__restrict__ Sgu, const uint16_t *__restrict__ Bgu,
-                      const int32_t *__restrict__ tiles, const int32_t *__restrict__ tile_count,
-                      const int32_t *__restrict__ perm, const int32_t *__restrict__ status,
-                      int32_t top_k, int32_t H, int32_t I, uint16_t *__restrict__ h) {
-  extern __shared__ __align__(16) uint16_t xs[];  // [kRows][H]
+// The persistent kernel: one CTA per SM walks a contiguous range of work
+// chunks (a chunk = 16 weight rows of one expert tile: 8 gate rows + their 8 up
+// rows, or 16 down rows).  A producer warp streams each chunk's packed rows and
+// scale/bias rows into a ring of shared-memory buffers with 1-D bulk copies
+// (every row is contiguous in global memory); 8 compute warps take chunks in
+// turn.  When the range moves to the next tile, the compute warps stage that
+// tile's activation rows (kTok per pass) in MMA fragment order.
+constexpr int kComputeWarps = 8;
+constexpr int kPersistThreads = (kComputeWarps + 1) * 32;
+
+struct PLayout {
+  int G, ws, xrb, chunk_bytes, sc_off, nbuf, off_x, off_xs, off_bar, total;
+  __host__ __device__ PLayout(int K, int nbuf_) {
+    G = K / 64;
+    ws = K / 2;                      // packed weight rows, contiguous as in global memory
+    xrb = G * 128 + 16;              // activation row stride (fragment order)
+    sc_off = 16 * ws;                // scales [16][G], then biases [16][G]
+    chunk_bytes = (sc_off + 16 * G * 4 + 127) & ~127;
+    nbuf = nbuf_;
+    off_x = nbuf * chunk_bytes;
+    off_xs = off_x + kTok * xrb;
+    off_bar = (off_xs + kTok * G * 4 + 15) & ~15;
+    total = off_bar + (2 * nbuf + 1) * 8;
+  }
+};
+
+__host__ __device__ inline int persist_nbuf(int K) {
+  // as many chunk buffers as fit next to one activation buffer, at most 16
+  for (int nb = 16; nb > 2; --nb)
+    if (PLayout(K, nb).total <= 227 * 1024) return nb;
+  return 2;
+}
+
+__device__ __forceinline__ void named_sync_compute() {
+  asm volatile("bar.sync 1, %0;" ::"r"(kComputeWarps * 32) : "memory");
+}
+
+template <int MODE>  // 0: gate/up + GeGLU -> h; 1: down + weighted scatter -> y_acc
+__global__ void __launch_bounds__(kPersistThreads, 1)
+    gemv_persist_kernel(const uint16_t *__restrict__ act, const uint32_t *__restrict__ Wq,
+                        const uint16_t *__restrict__ Sc, const uint16_t *__restrict__ Bi,
+                        const int32_t *__restrict__ tiles, const int32_t *__restrict__ tile_count,
+                        const int32_t *__restrict__ perm, const float *__restrict__ topk_weights,
+                        int32_t *__restrict__ status, int32_t top_k, int32_t H, int32_t I,
+                        int32_t nbuf, uint16_t *__restrict__ h, float *__restrict__ y_acc) {
+  using namespace umma;
+  extern __shared__ __align__(128) uint8_t gsm[];
   if (load_status(status) != 0) return;
-  const int tile = blockIdx.x;
-  if (tile >= *tile_count) return;
-  const int e = tiles[3 * tile], row0 = tiles[3 * tile + 1], rows = tiles[3 * tile + 2];
+  const int K = MODE == 0 ? H : I;
+  const PLayout L(K, nbuf);
+  const int G = L.G;
+  const int CPT = MODE == 0 ? I / 8 : H / 16;  // chunks per tile
+  const int rows_per_expert = MODE == 0 ? 2 * I : H;
+  const int n_tiles = *tile_count;
+  const int total = n_tiles * CPT;
+  const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
+  const int c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  if (c0 >= c1) return;
+  uint8_t *xb = gsm + L.off_x;
+  float *xs = reinterpret_cast<float *>(gsm + L.off_xs);
+  uint64_t *full = reinterpret_cast<uint64_t *>(gsm + L.off_bar);
+  uint64_t *empty = full + nbuf;
+  uint64_t *xbar = empty + nbuf;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.y * kGemvWarps + warp;
-  const int words = H / 8, groups = H / 64;
-  const int64_t rg = (int64_t)e * 2 * I + n;  // gate row
-  const int64_t ru = rg + I;                  // up row
-  for (int r0 = 0; r0 < rows; r0 += kRows) {
-    const int R = min(kRows, rows - r0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < R * words; i += kGemvThreads) {  // 16-byte chunks
-      const int r = i / words, c = i - r * words;
-      const int t = perm[row0 + r0 + r] / top_k;
-      reinterpret_cast<uint4 *>(xs + (size_t)r * H)[c] =
-          reinterpret_cast<const uint4 *>(x + (size_t)t * H)[c];
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nbuf; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
     }
-    __syncthreads();
-    if (n >= I) continue;
-    float ag[kRows], au[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) ag[r] = au[r] = 0.f;
-    for (int w = lane; w < words; w += 32) {
-      const uint32_t qg = Wgu[rg * words + w], qu = Wgu[ru * words + w];
-      const int g = w >> 3;
-      const float sg = bf16_bits_to_float(Sgu[rg * groups + g]);
-      const float bg = bf16_bits_to_float(Bgu[rg * groups + g]);
-      const float su = bf16_bits_to_float(Sgu[ru * groups + g]);
-      const float bu = bf16_bits_to_float(Bgu[ru * groups + g]);
-      float wg[8], wu[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        wg[j] = fmaf(sg, (float)((qg >> (4 * j)) & 15u), bg);
-        wu[j] = fmaf(su, (float)((qu >> (4 * j)) & 15u), bu);
+    mbar_init(xbar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  volatile int never = 0;
+
+  // Work order (shared by producer and consumers): tiles of the range in order; per tile
+  // ceil(R / kTok) passes; per pass the range's chunks of that tile.
+  if (warp == kComputeWarps) {
+    // ------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = c0 / CPT; ok && tile * CPT < c1; ++tile) {
+        const int e = tiles[3 * tile], R = tiles[3 * tile + 2];
+        const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
+        for (int r0 = 0; ok && r0 < R; r0 += kTok) {
+          for (int j = j0; j < j1; ++j, ++it) {
+            const int b = it % nbuf;
+            if (!(ok = mbar_wait(&empty[b], ((it / nbuf) & 1) ^ 1, &never))) break;
+            uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
+            const uint32_t rbytes = (uint32_t)K / 2, sbytes = 8u * G * 2;
+            mbar_arrive_expect_tx(&full[b], 16 * rbytes + 4 * sbytes);
+            // rows 0-7 and 8-15 of the chunk: gate rows and their up rows (two runs of 8
+            // consecutive rows), or 16 consecutive down rows (one run)
+            const int64_t ra = (int64_t)e * rows_per_expert + (MODE == 0 ? 8 * j : 16 * j);
+            const int64_t rb = MODE == 0 ? ra + I : ra + 8;
+            uint16_t *sc = reinterpret_cast<uint16_t *>(buf + L.sc_off);
+            if (MODE == 0) {
+              bulk_load(buf, Wq + ra * (K / 8), 8 * rbytes, &full[b]);
+              bulk_load(buf + 8 * L.ws, Wq + rb * (K / 8), 8 * rbytes, &full[b]);
+              bulk_load(sc, Sc + ra * G, sbytes, &full[b]);
+              bulk_load(sc + 8 * G, Sc + rb * G, sbytes, &full[b]);
+              bulk_load(sc + 16 * G, Bi + ra * G, sbytes, &full[b]);
+              bulk_load(sc + 24 * G, Bi + rb * G, sbytes, &full[b]);
+            } else {
+              bulk_load(buf, Wq + ra * (K / 8), 16 * rbytes, &full[b]);
+              bulk_load(sc, Sc + ra * G, 2 * sbytes, &full[b]);
+              bulk_load(sc + 16 * G, Bi + ra * G, 2 * sbytes, &full[b]);
+            }
+          }
+        }
       }
+      if (!ok) raise_status(status, MOE_ERR_TIMEOUT);
+      // drain: copies still in flight complete before the CTA exits
+      for (uint32_t i = (it > (uint32_t)nbuf ? it - nbuf : 0); i < it; ++i)
+        mbar_wait(&full[i % nbuf], (i / nbuf) & 1, nullptr, 200000000ull);
+    }
+    return;
+  }
+
+  // ------------------------------------------------ compute warps
+  const int gq = lane >> 2, t = lane & 3;
+  uint32_t it = 0, xphase = 0;
+  bool ok = true;
+  for (int tile = c0 / CPT; tile * CPT < c1; ++tile) {
+    const int e = tiles[3 * tile], row0 = tiles[3 * tile + 1], R = tiles[3 * tile + 2];
+    const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
+    for (int r0 = 0; r0 < R; r0 += kTok, xphase ^= 1) {
+      const int Rp = min(kTok, R - r0);
+      named_sync_compute();  // every warp is done with the previous activations
+      if (threadIdx.x == 0) {
+        const uint32_t xbytes = (uint32_t)K * 2;
+        mbar_arrive_expect_tx(xbar, Rp * xbytes);
+        for (int jr = 0; jr < Rp; ++jr) {
+          const int64_t src_row = MODE == 0 ? perm[row0 + r0 + jr] / top_k : row0 + r0 + jr;
+          bulk_load(xb + (size_t)jr * L.xrb, act + src_row * K, xbytes, xbar);
+        }
+      }
+      ok = mbar_wait(xbar, xphase, &never) && ok;
+      permute_rows(xb, xs, L.xrb, G, Rp, kComputeWarps * 32);
+      named_sync_compute();
+      for (int j = j0; j < j1; ++j, ++it) {
+        if ((int)(it % kComputeWarps) != warp) continue;
+        const int b = it % nbuf;
+        ok = mbar_wait(&full[b], (it / nbuf) & 1, &never) && ok;
+        ok = __all_sync(0xffffffffu, ok);
+        const uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(buf + L.sc_off);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok) warp_rows_dot(buf, L.ws, sc + gq * G, sc + (8 + gq) * G, 16 * G, xb, L.xrb, xs, G, acc);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[b]);
+        if (!ok) continue;
 #pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        if (r < R) {
-          float xf[8];
-          bf16x8_to_f32(reinterpret_cast<const uint4 *>(xs + (size_t)r * H)[w], xf);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            ag[r] = fmaf(wg[j], xf[j], ag[r]);
-            au[r] = fmaf(wu[j], xf[j], au[r]);
+        for (int c = 0; c < 2; ++c) {
+          const int jr = 2 * t + c;
+          if (jr >= Rp) continue;
+          if (MODE == 0) {
+            const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
+            h[(int64_t)(row0 + r0 + jr) * I + n] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
+          } else {
+            const int a = perm[row0 + r0 + jr];
+            const float w = topk_weights[a];
+            float *yrow = y_acc + (int64_t)(a / top_k) * H + 16 * j;
+            atomicAdd(yrow + gq, w * acc[c]);
+            atomicAdd(yrow + gq + 8, w * acc[2 + c]);
           }
         }
       }
     }
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const float g = warp_sum(ag[r]), u = warp_sum(au[r]);
-      if (lane == r && r < R) {
-        const float hv = gelu_tanh(g) * u;
-        h[(int64_t)(row0 + r0 + r) * I + n] = __bfloat16_as_ushort(__float2bfloat16_rn(hv));
-      }
-    }
   }
-}
-
-// grid: (max_tiles, ceil(H / kGemvWarps)); dynamic smem: kRows * I bf16
-__global__ void __launch_bounds__(kGemvThreads)
-    down_gemv_kernel(const uint16_t *__restrict__ hin, const uint32_t *__restrict__ Wd,
-                     const uint16_t *__restrict__ Sd, const uint16_t *__restrict__ Bd,
-                     const int32_t *__restrict__ tiles, const int32_t *__restrict__ tile_count,
-                     const int32_t *__restrict__ perm, const float *__restrict__ topk_weights,
-                     const int32_t *__restrict__ status, int32_t top_k, int32_t H, int32_t I,
-                     float *__restrict__ y_acc) {
-  extern __shared__ __align__(16) uint16_t hs[];  // [kRows][I]
-  if (load_status(status) != 0) return;
-  const int tile = blockIdx.x;
-  if (tile >= *tile_count) return;
-  const int e = tiles[3 * tile], row0 = tiles[3 * tile + 1], rows = tiles[3 * tile + 2];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.y * kGemvWarps + warp;
-  const int words = I / 8, groups = I / 64;
-  const int64_t rd = (int64_t)e * H + n;
-  for (int r0 = 0; r0 < rows; r0 += kRows) {
-    const int R = min(kRows, rows - r0);
-    __syncthreads();
-    for (int i = threadIdx.x; i < R * words; i += kGemvThreads) {
-      const int r = i / words, c = i - r * words;
-      reinterpret_cast<uint4 *>(hs + (size_t)r * I)[c] =
-          reinterpret_cast<const uint4 *>(hin + (size_t)(row0 + r0 + r) * I)[c];
-    }
-    __syncthreads();
-    if (n >= H) continue;
-    float acc[kRows];
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) acc[r] = 0.f;
-    for (int w = lane; w < words; w += 32) {
-      const uint32_t q = Wd[rd * words + w];
-      const int g = w >> 3;
-      const float s = bf16_bits_to_float(Sd[rd * groups + g]);
-      const float b = bf16_bits_to_float(Bd[rd * groups + g]);
-      float wv[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) wv[j] = fmaf(s, (float)((q >> (4 * j)) & 15u), b);
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        if (r < R) {
-          float hf[8];
-          bf16x8_to_f32(reinterpret_cast<const uint4 *>(hs + (size_t)r * I)[w], hf);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[r] = fmaf(wv[j], hf[j], acc[r]);
-        }
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kRows; ++r) {
-      const float o = warp_sum(acc[r]);
-      if (lane == r && r < R) {
-        const int a = perm[row0 + r0 + r];
-        const int t = a / top_k;
-        atomicAdd(&y_acc[(int64_t)t * H + n], topk_weights[a] * o);
-      }
-    }
-  }
+  if (!ok) raise_status(status, MOE_ERR_TIMEOUT);
 }
 
 // y = bf16(y_acc), four elements per thread step
@@ -178,31 +319,59 @@ __global__ void cast_bf16_kernel(const float *__restrict__ y_acc, uint16_t *__re
   }
 }
 
+static moe_status set_smem(const void *fn, size_t smem) {
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+static int sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+bool gemv_supported(int32_t H, int32_t I) {
+  return PLayout(H, 2).total <= 227 * 1024 && PLayout(I, 2).total <= 227 * 1024;
+}
+
+template <int MODE>
+static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const uint16_t *Sc,
+                                 const uint16_t *Bi, const moe_tiles_t &t, const float *tw,
+                                 int32_t H, int32_t I, uint16_t *h, float *y_acc,
+                                 cudaStream_t stream, const char *what) {
+  const int K = MODE == 0 ? H : I;
+  const int nbuf = persist_nbuf(K);
+  const size_t smem = PLayout(K, nbuf).total;
+  if (set_smem((const void *)gemv_persist_kernel<MODE>, smem) != MOE_OK) return check_launch(what);
+  const int64_t max_chunks = (int64_t)t.max_tiles * (MODE == 0 ? I / 8 : H / 16);
+  int grid = sm_count();
+  if (max_chunks < grid) grid = (int)max_chunks;
+  gemv_persist_kernel<MODE><<<grid, kPersistThreads, smem, stream>>>(
+      act, Wq, Sc, Bi, t.tiles, t.tile_count, t.perm, tw, t.status, t.top_k, H, I, nbuf, h,
+      y_acc);
+  return check_launch(what);
+}
+
 moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
                              uint16_t *h, cudaStream_t stream) {
-  const size_t smem = (size_t)kRows * H * sizeof(uint16_t);
-  if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(geglu_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  }
-  dim3 grid(t.max_tiles, (I + kGemvWarps - 1) / kGemvWarps);
-  geglu_gemv_kernel<<<grid, kGemvThreads, smem, stream>>>(x, Wgu, Sgu, Bgu, t.tiles, t.tile_count,
-                                                          t.perm, t.status, t.top_k, H, I, h);
-  return check_launch("moe_gather_qmm_geglu (gemv)");
+  return launch_persist<0>(x, Wgu, Sgu, Bgu, t, nullptr, H, I, h, nullptr, stream,
+                           "moe_gather_qmm_geglu (gemv)");
 }
 
 moe_status launch_down_gemv(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                             int32_t H, int32_t I, float *y_acc, cudaStream_t stream) {
-  const size_t smem = (size_t)kRows * I * sizeof(uint16_t);
-  if (smem > 48 * 1024) {
-    cudaFuncSetAttribute(down_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  }
-  dim3 grid(t.max_tiles, (H + kGemvWarps - 1) / kGemvWarps);
-  down_gemv_kernel<<<grid, kGemvThreads, smem, stream>>>(hin, Wd, Sd, Bd, t.tiles, t.tile_count,
-                                                         t.perm, topk_weights, t.status, t.top_k,
-                                                         H, I, y_acc);
-  return check_launch("moe_gather_qmm_down_unsort (gemv)");
+  return launch_persist<1>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, stream,
+                           "moe_gather_qmm_down_unsort (gemv)");
 }
 
 moe_status launch_cast_bf16(const float *y_acc, uint16_t *y, int64_t n, const int32_t *status,

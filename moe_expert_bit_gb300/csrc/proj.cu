@@ -54,7 +54,10 @@ static moe_status validate_dims(const char *fn, int32_t H, int32_t I, int32_t va
   return MOE_OK;
 }
 
-// MOE_VARIANT_AUTO: the tensor-core GEMM wherever it supports the shape.
+// MOE_VARIANT_AUTO: the weight-streaming GEMV when expert tiles are small
+// (at most 16 rows per expert on average: decode-sized calls, where the layer
+// is a pure weight stream), else the tensor-core GEMM where it supports the
+// shape.
 static moe_status resolve_variant(const char *fn, const moe_tiles_t *t, int32_t H, int32_t I,
                                   int32_t *variant) {
   const bool tc_ok = tc_supported(H, I, t->tile_m) == MOE_OK;
@@ -63,7 +66,22 @@ static moe_status resolve_variant(const char *fn, const moe_tiles_t *t, int32_t 
               "(got tile_m=%d H=%d I=%d)", fn, t->tile_m, H, I);
     return MOE_ERR_UNSUPPORTED;
   }
-  if (*variant == MOE_VARIANT_AUTO) *variant = tc_ok ? MOE_VARIANT_TC : MOE_VARIANT_GEMV;
+  const bool gemv_ok = gemv_supported(H, I);
+  if (*variant == MOE_VARIANT_GEMV && !gemv_ok) {
+    set_error("%s: weight-streaming variant needs its shared-memory tile to fit (H=%d I=%d)", fn,
+              H, I);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (*variant == MOE_VARIANT_AUTO) {
+    const int64_t A = t->num_assignments;
+    const int64_t experts = A < t->num_experts ? A : t->num_experts;
+    const bool small_tiles = A <= 16 * experts;
+    if (!tc_ok && !gemv_ok) {
+      set_error("%s: no kernel variant supports H=%d I=%d tile_m=%d", fn, H, I, t->tile_m);
+      return MOE_ERR_UNSUPPORTED;
+    }
+    *variant = (tc_ok && (!small_tiles || !gemv_ok)) ? MOE_VARIANT_TC : MOE_VARIANT_GEMV;
+  }
   return MOE_OK;
 }
 
