@@ -93,6 +93,41 @@ __device__ __forceinline__ void permute_rows(uint8_t *xb, float *xs, int xrb, in
 //          rows 8-15: MMA rows g + 8), row stride ws
 //   scA / scB: scale rows of MMA rows g and g+8 in shared memory (biases at +bofs)
 // acc[0], acc[1]: row g with activation rows 2t, 2t+1; acc[2], acc[3]: row g+8.
+// Two groups per iteration, each as two independent MMA chains, keep four chains in flight.
+__device__ __forceinline__ void group_mma(const uint8_t *rA, const uint8_t *rB, const uint8_t *xrow,
+                                          int g, float (&d0)[4], float (&d1)[4]) {
+  const uint2 A = *reinterpret_cast<const uint2 *>(rA + g * 32);
+  const uint2 B = *reinterpret_cast<const uint2 *>(rB + g * 32);
+  const uint2 *xf = reinterpret_cast<const uint2 *>(xrow + g * 128);
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t wA = (m >> 1) ? A.y : A.x;
+    const uint32_t wB = (m >> 1) ? B.y : B.x;
+    const int p0 = 2 * (m & 1);
+    const uint32_t a[4] = {pair128(wA, p0), pair128(wB, p0), pair128(wA, p0 + 1),
+                           pair128(wB, p0 + 1)};
+    const uint2 f = xf[m];
+    if (m < 2)
+      mma_bf16_16816(d0, a, f.x, f.y, d0);
+    else
+      mma_bf16_16816(d1, a, f.x, f.y, d1);
+  }
+}
+
+__device__ __forceinline__ void group_fold(const uint16_t *scA, const uint16_t *scB, int bofs,
+                                           const float *xs0, const float *xs1, int g,
+                                           const float (&d0)[4], const float (&d1)[4],
+                                           float (&acc)[4]) {
+  const float s_a = bf16f(scA[g]), s_b = bf16f(scB[g]);
+  const float c_a = fmaf(-128.f, s_a, bf16f(scA[bofs + g]));
+  const float c_b = fmaf(-128.f, s_b, bf16f(scB[bofs + g]));
+  const float x0 = xs0[g], x1 = xs1[g];
+  acc[0] = fmaf(s_a, d0[0] + d1[0], fmaf(c_a, x0, acc[0]));
+  acc[1] = fmaf(s_a, d0[1] + d1[1], fmaf(c_a, x1, acc[1]));
+  acc[2] = fmaf(s_b, d0[2] + d1[2], fmaf(c_b, x0, acc[2]));
+  acc[3] = fmaf(s_b, d0[3] + d1[3], fmaf(c_b, x1, acc[3]));
+}
+
 __device__ __forceinline__ void warp_rows_dot(const uint8_t *wrows, int ws, const uint16_t *scA,
                                               const uint16_t *scB, int bofs, const uint8_t *xb,
                                               int xrb, const float *xs, int G, float (&acc)[4]) {
@@ -101,30 +136,20 @@ __device__ __forceinline__ void warp_rows_dot(const uint8_t *wrows, int ws, cons
   const uint8_t *xrow = xb + (size_t)min(gq, kTok - 1) * xrb + t * 32;
   const float *xs0 = xs + min(2 * t, kTok - 1) * G, *xs1 = xs + min(2 * t + 1, kTok - 1) * G;
   const uint8_t *rA = wrows + gq * ws + t * 8, *rB = rA + 8 * ws;
-#pragma unroll 2
-  for (int g = 0; g < G; ++g) {
-    const uint2 A = *reinterpret_cast<const uint2 *>(rA + g * 32);
-    const uint2 B = *reinterpret_cast<const uint2 *>(rB + g * 32);
-    const uint2 *xf = reinterpret_cast<const uint2 *>(xrow + g * 128);
-    float d[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-      const uint32_t wA = (m >> 1) ? A.y : A.x;
-      const uint32_t wB = (m >> 1) ? B.y : B.x;
-      const int p0 = 2 * (m & 1);
-      const uint32_t a[4] = {pair128(wA, p0), pair128(wB, p0), pair128(wA, p0 + 1),
-                             pair128(wB, p0 + 1)};
-      const uint2 f = xf[m];
-      mma_bf16_16816(d, a, f.x, f.y, d);
-    }
-    const float s_a = bf16f(scA[g]), s_b = bf16f(scB[g]);
-    const float c_a = fmaf(-128.f, s_a, bf16f(scA[bofs + g]));
-    const float c_b = fmaf(-128.f, s_b, bf16f(scB[bofs + g]));
-    const float x0 = xs0[g], x1 = xs1[g];
-    acc[0] = fmaf(s_a, d[0], fmaf(c_a, x0, acc[0]));
-    acc[1] = fmaf(s_a, d[1], fmaf(c_a, x1, acc[1]));
-    acc[2] = fmaf(s_b, d[2], fmaf(c_b, x0, acc[2]));
-    acc[3] = fmaf(s_b, d[3], fmaf(c_b, x1, acc[3]));
+  int g = 0;
+#pragma unroll 1
+  for (; g + 1 < G; g += 2) {
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+    float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
+    group_mma(rA, rB, xrow, g, p0, p1);
+    group_mma(rA, rB, xrow, g + 1, q0, q1);
+    group_fold(scA, scB, bofs, xs0, xs1, g, p0, p1, acc);
+    group_fold(scA, scB, bofs, xs0, xs1, g + 1, q0, q1, acc);
+  }
+  if (g < G) {
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+    group_mma(rA, rB, xrow, g, p0, p1);
+    group_fold(scA, scB, bofs, xs0, xs1, g, p0, p1, acc);
   }
 }
 
@@ -132,11 +157,14 @@ __device__ __forceinline__ void warp_rows_dot(const uint8_t *wrows, int ws, cons
 // chunks (a chunk = 16 weight rows of one expert tile: 8 gate rows + their 8 up
 // rows, or 16 down rows).  A producer warp streams each chunk's packed rows and
 // scale/bias rows into a ring of shared-memory buffers with 1-D bulk copies
-// (every row is contiguous in global memory); 8 compute warps take chunks in
-// turn.  When the range moves to the next tile, the compute warps stage that
+// (every row is contiguous in global memory); up to 16 compute warps take
+// chunks in turn.  When the range moves to the next tile, the compute warps stage that
 // tile's activation rows (kTok per pass) in MMA fragment order.
-constexpr int kComputeWarps = 8;
-constexpr int kPersistThreads = (kComputeWarps + 1) * 32;
+// Compute warps per CTA: min(16, ring buffers).  A warp takes chunks w, w + W, ... and
+// chunk i uses buffer i % nbuf; with W <= nbuf the previous use of a buffer always
+// belongs to a chunk that landed before this warp's previous chunk, so a parity wait on
+// the buffer's barrier can never run a full phase ahead.
+constexpr int kMaxComputeWarps = 16;
 
 struct PLayout {
   int G, ws, xrb, chunk_bytes, sc_off, nbuf, off_x, off_xs, off_bar, total;
@@ -161,12 +189,12 @@ __host__ __device__ inline int persist_nbuf(int K) {
   return 2;
 }
 
-__device__ __forceinline__ void named_sync_compute() {
-  asm volatile("bar.sync 1, %0;" ::"r"(kComputeWarps * 32) : "memory");
+__device__ __forceinline__ void named_sync_compute(int nthreads) {
+  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
 }
 
 template <int MODE>  // 0: gate/up + GeGLU -> h; 1: down + weighted scatter -> y_acc
-__global__ void __launch_bounds__(kPersistThreads, 1)
+__global__ void __launch_bounds__((kMaxComputeWarps + 1) * 32, 1)
     gemv_persist_kernel(const uint16_t *__restrict__ act, const uint32_t *__restrict__ Wq,
                         const uint16_t *__restrict__ Sc, const uint16_t *__restrict__ Bi,
                         const int32_t *__restrict__ tiles, const int32_t *__restrict__ tile_count,
@@ -192,6 +220,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   uint64_t *empty = full + nbuf;
   uint64_t *xbar = empty + nbuf;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwc = (int)(blockDim.x >> 5) - 1;  // compute warps; the last warp produces
   if (threadIdx.x == 0) {
     for (int i = 0; i < nbuf; ++i) {
       mbar_init(&full[i], 1);
@@ -205,7 +234,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
 
   // Work order (shared by producer and consumers): tiles of the range in order; per tile
   // ceil(R / kTok) passes; per pass the range's chunks of that tile.
-  if (warp == kComputeWarps) {
+  if (warp == nwc) {
     // ------------------------------------------------ producer
     if (lane == 0) {
       uint32_t it = 0;
@@ -257,7 +286,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
     for (int r0 = 0; r0 < R; r0 += kTok, xphase ^= 1) {
       const int Rp = min(kTok, R - r0);
-      named_sync_compute();  // every warp is done with the previous activations
+      named_sync_compute(nwc * 32);  // every warp is done with the previous activations
       if (threadIdx.x == 0) {
         const uint32_t xbytes = (uint32_t)K * 2;
         mbar_arrive_expect_tx(xbar, Rp * xbytes);
@@ -267,10 +296,10 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         }
       }
       ok = mbar_wait(xbar, xphase, &never) && ok;
-      permute_rows(xb, xs, L.xrb, G, Rp, kComputeWarps * 32);
-      named_sync_compute();
+      permute_rows(xb, xs, L.xrb, G, Rp, nwc * 32);
+      named_sync_compute(nwc * 32);
       for (int j = j0; j < j1; ++j, ++it) {
-        if ((int)(it % kComputeWarps) != warp) continue;
+        if ((int)(it % nwc) != warp) continue;
         const int b = it % nbuf;
         ok = mbar_wait(&full[b], (it / nbuf) & 1, &never) && ok;
         ok = __all_sync(0xffffffffu, ok);
@@ -354,7 +383,8 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   const int64_t max_chunks = (int64_t)t.max_tiles * (MODE == 0 ? I / 8 : H / 16);
   int grid = sm_count();
   if (max_chunks < grid) grid = (int)max_chunks;
-  gemv_persist_kernel<MODE><<<grid, kPersistThreads, smem, stream>>>(
+  const int nwc = nbuf < kMaxComputeWarps ? nbuf : kMaxComputeWarps;
+  gemv_persist_kernel<MODE><<<grid, (nwc + 1) * 32, smem, stream>>>(
       act, Wq, Sc, Bi, t.tiles, t.tile_count, t.perm, tw, t.status, t.top_k, H, I, nbuf, h,
       y_acc);
   return check_launch(what);
