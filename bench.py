@@ -274,9 +274,8 @@ def main():
 
     def step(ev=None):
         # the four library calls; events (if given) bracket the gate/up launch
-        mq.moe_sort_assignments(ids, E, r.sorted_ids, r.perm, r.counts, r.status, stream)
-        mq.moe_build_expert_tiles(r.sorted_ids, E, args.tile_m, r.offsets, r.tiles, r.tile_count,
-                                  r.status, stream)
+        mq.moe_sort_and_build_tiles(ids, E, args.tile_m, r.sorted_ids, r.perm, r.counts,
+                                    r.offsets, r.tiles, r.tile_count, r.status, stream)
         if ev is not None:
             ev[0].record(stream)
         mq.moe_gather_qmm_geglu(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.h, variant, stream)
@@ -356,7 +355,10 @@ def main():
     geglu_avg = sum(geglu_ms) / len(geglu_ms)
     geglu_bytes = touched * gu_b + T * H * 2 + A * I * 2
     achieved = geglu_bytes / (geglu_avg * 1e-3) / 1e9
-    launches_per_step = 5
+    # route (1) + gate/up (1) + down (1) + cast (1 unless fused into the down kernel)
+    fused_cast = variant != mq.VARIANT_TC and T * H <= (1 << 20) and not (
+        variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
+    launches_per_step = 3 if fused_cast else 4
     line = {
         "metric": "MoE layer assignments/s", "value": world * A / (ms * 1e-3),
         "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -372,9 +374,10 @@ def main():
                            "weight_bytes": w_bytes, "flops": flops,
                            "bound": "hbm" if w_bytes / (hbm * 1e9) >= flops / (tf_burst * 1e12)
                            else "tensor", "peaks": peak_src},
-        "kernels_us": {"route (sort + tiles)": 1e3 * statistics.median(route_ms),
+        "kernels_us": {"route (sort + tiles, one launch)": 1e3 * statistics.median(route_ms),
                        "gather_qmm_geglu": 1e3 * statistics.median(geglu_ms),
                        "gather_qmm_down_unsort (+zero, cast)": 1e3 * statistics.median(down_ms)},
+        "gpu_launches_note": "memset of the y accumulator (a copy-engine node) not counted",
         "roofline": {"kernel": "gather_qmm_geglu", "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peak_src} (copy bandwidth)",

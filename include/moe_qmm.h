@@ -112,8 +112,9 @@ typedef struct {
 size_t moe_max_tiles(int32_t num_assignments, int32_t num_experts, int32_t tile_m);
 
 /*
- * Bytes of fp32 workspace that moe_gather_qmm_down_unsort needs for T
- * tokens of width H (the y accumulator, [T, H] fp32).  0 for invalid sizes.
+ * Bytes of workspace that moe_gather_qmm_down_unsort needs for T tokens of
+ * width H: the y accumulator ([T, H] fp32) followed by 16 bytes for a
+ * completion counter.  0 for invalid sizes.
  */
 size_t moe_workspace_bytes(int32_t num_tokens, int32_t hidden);
 
@@ -157,6 +158,18 @@ moe_status moe_build_expert_tiles(const int32_t *sorted_ids, int32_t num_assignm
                                   int32_t num_experts, int32_t tile_m, int32_t max_tiles,
                                   int32_t *offsets, int32_t *tiles, int32_t *tile_count,
                                   int32_t *status, cudaStream_t stream);
+
+/*
+ * Steps a1 and a2 in one launch: exactly moe_sort_assignments followed by
+ * moe_build_expert_tiles on the same buffers (same outputs, same status
+ * codes, same argument rules), one single-CTA kernel instead of two.  Saves
+ * a launch and a pass over the sorted ids for decode-sized calls.
+ */
+moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t num_tokens, int32_t top_k,
+                                    int32_t num_experts, int32_t tile_m, int32_t max_tiles,
+                                    int32_t *sorted_ids, int32_t *perm, int32_t *counts,
+                                    int32_t *offsets, int32_t *tiles, int32_t *tile_count,
+                                    int32_t *status, cudaStream_t stream);
 
 /*
  * Steps a3-a6 -- gathered 4-bit gate/up projection with the GeGLU product
@@ -212,7 +225,7 @@ moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
  *   Same arguments and result as moe_gather_qmm_down_unsort, minus y_acc_ws.
  *   The fp32 accumulator is a fixed array of MOE_NOALLOC_MAX_Y_ELEMENTS floats
  *   (16 MiB) of device memory inside the library, which every GPU that loads
- *   the library holds until the process exits.  T * H above that maximum
+ *   the library holds until the process exits.  T * H + 4 above that maximum
  *   returns MOE_ERR_UNSUPPORTED before any launch.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
@@ -222,7 +235,7 @@ moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
  *   threads) race on it -- serialise them.
  * No cudaMalloc, cudaFree or allocating library routine is called.
  */
-#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304
+#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304 /* floats; T * H + 4 must not exceed it */
 moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_t *Wd,
                                               const moe_bf16_t *Sd, const moe_bf16_t *Bd,
                                               const moe_tiles_t *tiles, const float *topk_weights,

@@ -34,7 +34,8 @@ MAX_EXPERTS = 256
 # every symbol include/moe_qmm.h declares
 ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
-               "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc")
+               "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc",
+               "moe_sort_and_build_tiles")
 NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
@@ -77,13 +78,16 @@ def load(build_if_needed: bool = True):
         lib.moe_workspace_bytes.restype = ctypes.c_size_t
         lib.moe_sort_assignments.argtypes = [p, i32, i32, i32, p, p, p, p, p]
         lib.moe_build_expert_tiles.argtypes = [p, i32, i32, i32, i32, p, p, p, p, p]
+        lib.moe_sort_and_build_tiles.argtypes = [p, i32, i32, i32, i32, i32, p, p, p, p, p, p,
+                                                 p, p]
         lib.moe_gather_qmm_geglu.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32, i32,
                                              p, p]
         lib.moe_gather_qmm_down_unsort.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), p, i32,
                                                    i32, i32, p, p, p]
         lib.moe_gather_qmm_down_unsort_noalloc.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles),
                                                            p, i32, i32, i32, p, p]
-        for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_gather_qmm_geglu",
+        for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_sort_and_build_tiles",
+                   "moe_gather_qmm_geglu",
                    "moe_gather_qmm_down_unsort", "moe_gather_qmm_down_unsort_noalloc"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.moe_last_error_string.argtypes = []
@@ -144,6 +148,20 @@ def moe_build_expert_tiles(sorted_ids, num_experts, tile_m, offsets, tiles, tile
     max_tiles = tiles.numel() // 3
     _check(load().moe_build_expert_tiles(
         _ptr(sorted_ids, torch.int32, "sorted_ids"), A, num_experts, tile_m, max_tiles,
+        _ptr(offsets, torch.int32, "offsets", num_experts + 1), _ptr(tiles, torch.int32, "tiles"),
+        _ptr(tile_count, torch.int32, "tile_count", 1), _ptr(status, torch.int32, "status", 1),
+        _stream(stream)))
+
+
+def moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, sorted_ids, perm, counts, offsets,
+                             tiles, tile_count, status, stream=None):
+    """moe_sort_assignments + moe_build_expert_tiles in one launch (same outputs)."""
+    T, k = topk_ids.shape
+    A = T * k
+    _check(load().moe_sort_and_build_tiles(
+        _ptr(topk_ids, torch.int32, "topk_ids"), T, k, num_experts, tile_m, tiles.numel() // 3,
+        _ptr(sorted_ids, torch.int32, "sorted_ids", A), _ptr(perm, torch.int32, "perm", A),
+        _ptr(counts, torch.int32, "counts", num_experts),
         _ptr(offsets, torch.int32, "offsets", num_experts + 1), _ptr(tiles, torch.int32, "tiles"),
         _ptr(tile_count, torch.int32, "tile_count", 1), _ptr(status, torch.int32, "status", 1),
         _stream(stream)))
@@ -213,14 +231,14 @@ class MoeLayerBuffers:
     def __init__(self, T, k, E, H, I, tile_m, device="cuda"):
         self.routing = Routing(T, k, E, tile_m, device)
         self.h = torch.empty(T * k, I, dtype=torch.bfloat16, device=device)
-        self.y_acc = torch.empty(moe_workspace_bytes(T, H) // 4, dtype=torch.float32,
+        self.y_acc = torch.empty((moe_workspace_bytes(T, H) + 3) // 4, dtype=torch.float32,
                                  device=device)
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.H, self.I = H, I
 
 
 def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, variant=VARIANT_AUTO,
-              buffers=None, stream=None):
+              buffers=None, stream=None, fused_route=False):
     """Run the four calls on one stream.  ``weights``: dict of Wgu, Sgu, Bgu, Wd, Sd, Bd
     device tensors (uint32 data as int32, bf16 scales/biases).  Returns the buffers."""
     T, k = topk_ids.shape
@@ -229,9 +247,14 @@ def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, varia
     b = buffers or MoeLayerBuffers(T, k, num_experts, H, I, tile_m, device=x.device)
     r = b.routing
     r.status.zero_()
-    moe_sort_assignments(topk_ids, num_experts, r.sorted_ids, r.perm, r.counts, r.status, stream)
-    moe_build_expert_tiles(r.sorted_ids, num_experts, tile_m, r.offsets, r.tiles, r.tile_count,
-                           r.status, stream)
+    if fused_route:
+        moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, r.sorted_ids, r.perm, r.counts,
+                                 r.offsets, r.tiles, r.tile_count, r.status, stream)
+    else:
+        moe_sort_assignments(topk_ids, num_experts, r.sorted_ids, r.perm, r.counts, r.status,
+                             stream)
+        moe_build_expert_tiles(r.sorted_ids, num_experts, tile_m, r.offsets, r.tiles,
+                               r.tile_count, r.status, stream)
     moe_gather_qmm_geglu(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I, b.h, variant,
                          stream)
     moe_gather_qmm_down_unsort(b.h, weights["Wd"], weights["Sd"], weights["Bd"], r, topk_weights,

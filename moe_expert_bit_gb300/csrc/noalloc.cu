@@ -63,7 +63,7 @@ extern "C" moe_status moe_gather_qmm_down_unsort_noalloc(
     return MOE_ERR_INVALID_ARG;
   }
   if (tiles->num_tokens > 0 && H > 0 &&
-      (int64_t)tiles->num_tokens * H > (int64_t)MOE_NOALLOC_MAX_Y_ELEMENTS) {
+      moe_workspace_bytes(tiles->num_tokens, H) > sizeof(float) * MOE_NOALLOC_MAX_Y_ELEMENTS) {
     set_error("%s: T*H = %lld exceeds the built-in accumulator of %d fp32 elements; "
               "use moe_gather_qmm_down_unsort with a caller workspace",
               fn, (long long)tiles->num_tokens * H, MOE_NOALLOC_MAX_Y_ELEMENTS);

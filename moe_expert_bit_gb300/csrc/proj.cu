@@ -123,14 +123,21 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
     return MOE_ERR_INVALID_ARG;
   }
   if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
+  // zero the accumulator and the completion counter that follows it
   const int64_t n = (int64_t)tiles->num_tokens * H;
-  if (cudaMemsetAsync(y_acc_ws, 0, (size_t)n * sizeof(float), stream) != cudaSuccess) {
+  if (cudaMemsetAsync(y_acc_ws, 0, moe_workspace_bytes(tiles->num_tokens, H), stream) !=
+      cudaSuccess) {
     return check_launch(fn);
   }
-  if (variant == MOE_VARIANT_TC)
+  if (variant == MOE_VARIANT_TC) {
     st = launch_down_tc(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
-  else
-    st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
-  if (st != MOE_OK) return st;
+    if (st != MOE_OK) return st;
+    return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
+  }
+  // small outputs: the last CTA of the down kernel does the cast (one launch fewer)
+  const bool fuse_cast = n <= (int64_t(1) << 20);
+  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, y,
+                        fuse_cast ? n : 0, stream);
+  if (st != MOE_OK || fuse_cast) return st;
   return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
 }

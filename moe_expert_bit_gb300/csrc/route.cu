@@ -48,16 +48,21 @@ constexpr int kSortWarps = kSortThreads / 32;
 //          lanes gives each element's rank; per-warp counts are scanned across
 //          the 32 warps per expert and added to a running cursor, so slots
 //          follow ascending a within every expert.
-__global__ void __launch_bounds__(kSortThreads)
-    sort_assignments_kernel(const int32_t *__restrict__ ids, int32_t A, int32_t E,
-                            int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
-                            int32_t *__restrict__ counts, int32_t *__restrict__ status) {
-  __shared__ int32_t s_hist[MOE_MAX_EXPERTS];
-  __shared__ int32_t s_cursor[MOE_MAX_EXPERTS];
-  __shared__ int32_t s_warp[kSortWarps][MOE_MAX_EXPERTS];
-  __shared__ int32_t s_bad;
+struct SortSmem {
+  int32_t hist[MOE_MAX_EXPERTS];
+  int32_t cursor[MOE_MAX_EXPERTS];
+  int32_t warp[kSortWarps][MOE_MAX_EXPERTS];
+  int32_t bad;
+};
+
+// Returns false (status raised) if an id is out of range.  Block of kSortThreads threads.
+__device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t A, int32_t E,
+                          int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
+                          int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+  int32_t *s_hist = sm.hist, *s_cursor = sm.cursor;
+  int32_t(*s_warp)[MOE_MAX_EXPERTS] = sm.warp;
+  int32_t &s_bad = sm.bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (load_status(status) != 0) return;
 
   for (int e = tid; e < E; e += kSortThreads) s_hist[e] = 0;
   for (int i = tid; i < kSortWarps * MOE_MAX_EXPERTS; i += kSortThreads) (&s_warp[0][0])[i] = 0;
@@ -74,7 +79,7 @@ __global__ void __launch_bounds__(kSortThreads)
   __syncthreads();
   if (s_bad) {
     if (tid == 0) raise_status(status, MOE_ERR_RANGE);
-    return;
+    return false;
   }
 
   // exclusive scan over E <= 256 experts by warp 0: 8 consecutive experts per lane
@@ -136,9 +141,24 @@ __global__ void __launch_bounds__(kSortThreads)
       for (int w = 0; w < kSortWarps; ++w) s_warp[w][ex] = 0;
     __syncthreads();
   }
+  return true;
+}
+
+__global__ void __launch_bounds__(kSortThreads)
+    sort_assignments_kernel(const int32_t *__restrict__ ids, int32_t A, int32_t E,
+                            int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
+                            int32_t *__restrict__ counts, int32_t *__restrict__ status) {
+  __shared__ SortSmem sm;
+  if (load_status(status) != 0) return;
+  sort_body(sm, ids, A, E, sorted_ids, perm, counts, status);
 }
 
 constexpr int kTileThreads = 512;
+
+struct TileSmem {
+  int32_t off[MOE_MAX_EXPERTS + 1];
+  int32_t tstart[MOE_MAX_EXPERTS + 1];
+};
 
 __device__ __forceinline__ int32_t lower_bound_dev(const int32_t *v, int32_t n, int32_t key) {
   int32_t lo = 0, hi = n;
@@ -153,21 +173,17 @@ __device__ __forceinline__ int32_t lower_bound_dev(const int32_t *v, int32_t n, 
 }
 
 // Offsets, tile counts, exclusive scan and strided descriptor emission, one CTA.
-__global__ void __launch_bounds__(kTileThreads)
-    build_expert_tiles_kernel(const int32_t *__restrict__ sorted_ids, int32_t A, int32_t E,
-                              int32_t BM, int32_t *__restrict__ offsets,
-                              int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
-                              int32_t *__restrict__ status) {
-  __shared__ int32_t s_off[MOE_MAX_EXPERTS + 1];
-  __shared__ int32_t s_tstart[MOE_MAX_EXPERTS + 1];
+// Block of any multiple of 32 threads (>= 32).
+__device__ void build_body(TileSmem &sm, const int32_t *__restrict__ sorted_ids, int32_t A,
+                           int32_t E, int32_t BM, int32_t *__restrict__ offsets,
+                           int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
+                           int32_t *__restrict__ status) {
+  int32_t *s_off = sm.off, *s_tstart = sm.tstart;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (load_status(status) != 0) {
-    if (tid == 0) *tile_count = 0;
-    return;
-  }
+  const int nthr = blockDim.x;
   // self-check: every id in range and every adjacent pair in order
   int range_bad = 0, order_bad = 0;
-  for (int s = tid; s < A; s += kTileThreads) {
+  for (int s = tid; s < A; s += nthr) {
     int32_t v = sorted_ids[s];
     range_bad |= (v < 0 || v >= E);
     if (s + 1 < A) order_bad |= (v > sorted_ids[s + 1]);
@@ -182,7 +198,7 @@ __global__ void __launch_bounds__(kTileThreads)
     return;
   }
   // per-expert sorted range by binary search
-  for (int e = tid; e <= E; e += kTileThreads) s_off[e] = (e == E) ? A : lower_bound_dev(sorted_ids, A, e);
+  for (int e = tid; e <= E; e += nthr) s_off[e] = (e == E) ? A : lower_bound_dev(sorted_ids, A, e);
   __syncthreads();
   // tiles per expert, exclusive scan by warp 0 (8 experts per lane)
   if (warp == 0) {
@@ -211,10 +227,10 @@ __global__ void __launch_bounds__(kTileThreads)
     if (lane == 31) s_tstart[E] = incl;
   }
   __syncthreads();
-  for (int e = tid; e <= E; e += kTileThreads) offsets[e] = s_off[e];
+  for (int e = tid; e <= E; e += nthr) offsets[e] = s_off[e];
   const int32_t total = s_tstart[E];
   // strided emission: tile i belongs to the last expert whose first tile is <= i
-  for (int i = tid; i < total; i += kTileThreads) {
+  for (int i = tid; i < total; i += nthr) {
     int32_t lo = 0, hi = E;  // largest e in [0, E) with s_tstart[e] <= i
     while (hi - lo > 1) {
       int32_t mid = (lo + hi) >> 1;
@@ -233,6 +249,41 @@ __global__ void __launch_bounds__(kTileThreads)
   if (tid == 0) *tile_count = total;
 }
 
+__global__ void __launch_bounds__(kTileThreads)
+    build_expert_tiles_kernel(const int32_t *__restrict__ sorted_ids, int32_t A, int32_t E,
+                              int32_t BM, int32_t *__restrict__ offsets,
+                              int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
+                              int32_t *__restrict__ status) {
+  __shared__ TileSmem sm;
+  if (load_status(status) != 0) {
+    if (threadIdx.x == 0) *tile_count = 0;
+    return;
+  }
+  build_body(sm, sorted_ids, A, E, BM, offsets, tiles, tile_count, status);
+}
+
+// Steps a1 and a2 in one launch: the sort, then (after a block barrier, which also
+// makes this block's global writes of sorted_ids visible to it) the tile builder.
+__global__ void __launch_bounds__(kSortThreads)
+    route_kernel(const int32_t *__restrict__ ids, int32_t A, int32_t E, int32_t BM,
+                 int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
+                 int32_t *__restrict__ counts, int32_t *__restrict__ offsets,
+                 int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
+                 int32_t *__restrict__ status) {
+  __shared__ SortSmem ssm;
+  __shared__ TileSmem tsm;
+  if (load_status(status) != 0) {
+    if (threadIdx.x == 0) *tile_count = 0;
+    return;
+  }
+  if (!sort_body(ssm, ids, A, E, sorted_ids, perm, counts, status)) {
+    if (threadIdx.x == 0) *tile_count = 0;
+    return;
+  }
+  __syncthreads();
+  build_body(tsm, sorted_ids, A, E, BM, offsets, tiles, tile_count, status);
+}
+
 }  // namespace moeqmm
 
 using namespace moeqmm;
@@ -248,7 +299,8 @@ size_t moe_max_tiles(int32_t A, int32_t E, int32_t BM) {
 
 size_t moe_workspace_bytes(int32_t T, int32_t H) {
   if (T < 1 || H < 1) return 0;
-  return static_cast<size_t>(T) * static_cast<size_t>(H) * sizeof(float);
+  // the fp32 accumulator plus 16 bytes for the down kernel's completion counter
+  return static_cast<size_t>(T) * static_cast<size_t>(H) * sizeof(float) + 16;
 }
 
 moe_status moe_sort_assignments(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
@@ -305,6 +357,45 @@ moe_status moe_build_expert_tiles(const int32_t *sorted_ids, int32_t A, int32_t 
   build_expert_tiles_kernel<<<1, kTileThreads, 0, stream>>>(sorted_ids, A, E, BM, offsets, tiles,
                                                             tile_count, status);
   return check_launch("moe_build_expert_tiles");
+}
+
+moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
+                                    int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
+                                    int32_t *perm, int32_t *counts, int32_t *offsets,
+                                    int32_t *tiles, int32_t *tile_count, int32_t *status,
+                                    cudaStream_t stream) {
+  clear_error();
+  if (!topk_ids || !sorted_ids || !perm || !counts || !offsets || !tiles || !tile_count ||
+      !status) {
+    set_error("moe_sort_and_build_tiles: null pointer");
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (E < 1 || E > MOE_MAX_EXPERTS) {
+    set_error("moe_sort_and_build_tiles: num_experts %d outside [1, %d]", E, MOE_MAX_EXPERTS);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (T < 1 || k < 1 || k > E) {
+    set_error("moe_sort_and_build_tiles: need T >= 1 and 1 <= k <= E (T=%d k=%d E=%d)", T, k, E);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const int64_t A = static_cast<int64_t>(T) * k;
+  if (A > (int64_t(1) << 24)) {
+    set_error("moe_sort_and_build_tiles: %lld assignments exceed 2^24", (long long)A);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (tile_m != 16 && tile_m != 32 && tile_m != 64 && tile_m != 128 && tile_m != 256) {
+    set_error("moe_sort_and_build_tiles: tile_m %d not in {16, 32, 64, 128, 256}", tile_m);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const size_t need = moe_max_tiles(static_cast<int32_t>(A), E, tile_m);
+  if (max_tiles < 0 || static_cast<size_t>(max_tiles) < need) {
+    set_error("moe_sort_and_build_tiles: max_tiles %d < required %zu", max_tiles, need);
+    return MOE_ERR_INVALID_ARG;
+  }
+  route_kernel<<<1, kSortThreads, 0, stream>>>(topk_ids, static_cast<int32_t>(A), E, tile_m,
+                                               sorted_ids, perm, counts, offsets, tiles,
+                                               tile_count, status);
+  return check_launch("moe_sort_and_build_tiles");
 }
 
 }  // extern "C"

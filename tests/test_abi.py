@@ -42,7 +42,7 @@ def test_size_helpers():
     assert mq.moe_max_tiles(32, 128, 64) == 32
     assert mq.moe_max_tiles(64, 8, 32) == 2 + 8
     assert mq.moe_max_tiles(10, 0, 32) == 0
-    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4
+    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 16
     assert mq.moe_workspace_bytes(0, 2816) == 0
 
 

@@ -117,3 +117,37 @@ def test_builder_self_check_long_input():
     sid[77777], sid[77778] = sid[77778] + 1, sid[77777]
     if sid[77777] > sid[77778]:
         assert _build_only(sid, 128, 64) == (mq.MOE_ERR_UNSORTED, 0)
+
+
+def fused_route(topk_ids: np.ndarray, E: int, tile_m: int):
+    T, k = topk_ids.shape
+    r = mq.Routing(T, k, E, tile_m)
+    ids = torch.from_numpy(np.ascontiguousarray(topk_ids, np.int32)).cuda()
+    r.tile_count.fill_(777)
+    mq.moe_sort_and_build_tiles(ids, E, tile_m, r.sorted_ids, r.perm, r.counts, r.offsets,
+                                r.tiles, r.tile_count, r.status)
+    torch.cuda.synchronize()
+    tc = int(r.tile_count.item())
+    return dict(status=int(r.status.item()), sorted_ids=r.sorted_ids.cpu().numpy(),
+                perm=r.perm.cpu().numpy(), counts=r.counts.cpu().numpy(),
+                offsets=r.offsets.cpu().numpy(), tiles=r.tiles.cpu().numpy()[:3 * tc].reshape(-1, 3),
+                tile_count=tc)
+
+
+@pytest.mark.parametrize("name", synth.CONFIG_ORDER)
+@pytest.mark.parametrize("tile_m", [32, 128])
+def test_fused_route_equals_two_calls(name, tile_m):
+    cfg = synth.CONFIGS[name]
+    ids, _ = synth.router(name, cfg["T"], cfg["E"], cfg["k"])
+    a = gpu_route(ids, cfg["E"], tile_m)
+    b = fused_route(ids, cfg["E"], tile_m)
+    assert a["status"] == 0 and b["status"] == 0
+    for key in ("sorted_ids", "perm", "counts", "offsets", "tiles", "tile_count"):
+        assert np.array_equal(np.asarray(a[key]), np.asarray(b[key])), key
+
+
+def test_fused_route_flags_out_of_range_ids():
+    ids = np.zeros((16, 2), np.int32)
+    ids[7, 0] = 8
+    g = fused_route(ids, 8, 32)
+    assert g["status"] == mq.MOE_ERR_RANGE and g["tile_count"] == 0
