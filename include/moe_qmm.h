@@ -31,6 +31,10 @@
  *     synchronises nothing; every call only enqueues kernels on `stream`
  *     (0 = the legacy default stream) and returns.
  *   - bf16 tensors are passed as `moe_bf16_t` (the raw 16-bit pattern).
+ *   - The tensor pointers of the two projection calls (activations, packed
+ *     weights, scales, biases, h, the workspace and y) must be 16-byte
+ *     aligned: the kernels move them with the copy engine.  A misaligned
+ *     pointer is refused on the host with MOE_ERR_INVALID_ARG.
  *   - Host-side validation runs before any launch and returns a status other
  *     than MOE_OK without enqueueing anything, so no output is half written.
  *     moe_last_error_string() (per host thread) then says why.
@@ -113,8 +117,8 @@ size_t moe_max_tiles(int32_t num_assignments, int32_t num_experts, int32_t tile_
 
 /*
  * Bytes of workspace that moe_gather_qmm_down_unsort needs for T tokens of
- * width H: the y accumulator ([T, H] fp32) followed by 16 bytes for a
- * completion counter.  0 for invalid sizes.
+ * width H: the y accumulator ([T, H] fp32) followed by one int32 completion
+ * counter per 16 output columns, padded to 16 bytes.  0 for invalid sizes.
  */
 size_t moe_workspace_bytes(int32_t num_tokens, int32_t hidden);
 
@@ -225,8 +229,9 @@ moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
  *   Same arguments and result as moe_gather_qmm_down_unsort, minus y_acc_ws.
  *   The fp32 accumulator is a fixed array of MOE_NOALLOC_MAX_Y_ELEMENTS floats
  *   (16 MiB) of device memory inside the library, which every GPU that loads
- *   the library holds until the process exits.  T * H + 4 above that maximum
- *   returns MOE_ERR_UNSUPPORTED before any launch.
+ *   the library holds until the process exits.  A workspace of
+ *   moe_workspace_bytes(T, H) above that maximum returns MOE_ERR_UNSUPPORTED
+ *   before any launch.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
  *   stream capture.
@@ -235,7 +240,7 @@ moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
  *   threads) race on it -- serialise them.
  * No cudaMalloc, cudaFree or allocating library routine is called.
  */
-#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304 /* floats; T * H + 4 must not exceed it */
+#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304 /* floats; moe_workspace_bytes(T, H) / 4 must not exceed it */
 moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_t *Wd,
                                               const moe_bf16_t *Sd, const moe_bf16_t *Bd,
                                               const moe_tiles_t *tiles, const float *topk_weights,

@@ -45,6 +45,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 #include "umma.cuh"
 
 namespace moeqmm {
@@ -524,38 +525,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-static bool make_map_2d(CUtensorMap *m, CUtensorMapDataType dt, size_t elem, const void *base,
-                        uint64_t dim0, uint64_t dim1, uint32_t box0, uint32_t box1,
-                        CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {dim0, dim1};
-  const cuuint64_t strides[1] = {dim0 * elem};
-  const cuuint32_t box[2] = {box0, box1};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 static int num_sms() {
   static int n = 0;
   if (!n) {
@@ -603,9 +572,9 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
                            uint16_t *h, cudaStream_t stream) {
   const char *what = "moe_gather_qmm_geglu (tensor cores)";
   CUtensorMap mw, mx;
-  if (!tc::make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wgu, H / 8,
+  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wgu, H / 8,
                        (uint64_t)t.num_experts * 2 * I, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, t.num_tokens, 64, 1,
+      !make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, t.num_tokens, 64, 1,
                        CU_TENSOR_MAP_SWIZZLE_128B)) {
     set_error("%s: tensor map encoding failed", what);
     return MOE_ERR_CUDA;
@@ -633,9 +602,9 @@ moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_
                           int32_t H, int32_t I, float *y_acc, cudaStream_t stream) {
   const char *what = "moe_gather_qmm_down_unsort (tensor cores)";
   CUtensorMap mw, mx;
-  if (!tc::make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wd, I / 8,
+  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wd, I / 8,
                        (uint64_t)t.num_experts * H, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !tc::make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hin, I, t.num_assignments, 64,
+      !make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hin, I, t.num_assignments, 64,
                        16, CU_TENSOR_MAP_SWIZZLE_128B)) {
     set_error("%s: tensor map encoding failed", what);
     return MOE_ERR_CUDA;

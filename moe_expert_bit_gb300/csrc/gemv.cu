@@ -1,7 +1,7 @@
 // Weight-streaming kernels for the two projections when expert tiles are
 // small (decode): the GEMV-style variant.  The layer is then a pure stream of
 // packed 4-bit weights from HBM, so what counts is the work per weight on
-// the CUDA cores, not matrix throughput.
+// the CUDA cores and on shared memory, not matrix throughput.
 //
 //   gate/up:  h[s, n] = gelu_tanh(sum_k Wg[e][n][k] x_s[k]) * sum_k Wu[e][n][k] x_s[k]
 //   down:     y_acc[t, n] += w_a * sum_i Wd[e][n][i] h[s, i],  a = perm[s], t = a / top_k
@@ -13,25 +13,25 @@
 //   D_g = sum_k (128 + q_k) x_k,   X_g = sum_k x_k,
 // and 128 + q is exact in bf16: OR-ing a nibble into the bf16 pattern of
 // 128.0 produces it, and one lop3 on a shifted packed word produces two of
-// them at once (nibbles j and j+4).  D_g is one warp-level bf16 MMA
-// (m16n8k16, fp32 accumulate) per 16 k: the MMA is used as the dot-product
-// engine so that the CUDA cores only unpack nibbles (under one instruction
-// per weight) and fold each group once.  The k order inside an MMA is a
-// permutation of the group's k; the activations are staged in shared memory
-// in the same permuted order, which leaves the sum unchanged.
+// them at once (nibbles j and j+4).  D_g is one warp-level bf16 MMA chain
+// (m16n8k16, fp32 accumulate, four MMAs per group): the MMA is the
+// dot-product engine, so the CUDA cores only unpack nibbles (under one
+// instruction per weight) and fold each group once.  The k order inside an
+// MMA is a permutation of the group's k; the activations are staged in
+// shared memory in the same permuted order, which leaves the sum unchanged.
 //
-// A warp owns 16 weight rows (the MMA's M) and up to 4 activation rows per
-// pass (half of the MMA's N).  Its rows are loaded whole into shared memory
-// with bulk copies, so that DRAM sees long sequential runs, and stay there
-// while the passes over the tile's activation rows run.  For gate/up the 16 rows are 8 gate rows and the 8 matching up rows, so
-// each lane ends with a gate value and its up value side by side.
+// Shared-memory traffic is the budget to watch (every weight is written
+// there once by the copy engine and read once by a warp), so the layout is
+// chosen for conflict-free reads: weight rows land at a stride of 32 mod 128
+// bytes (a 2-D TMA box wider than the row, whose tail the copy engine fills
+// with zeros), so the four rows that one quarter-warp reads fall in
+// different banks.
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 #include "umma.cuh"
 
 namespace moeqmm {
-
-constexpr int kTok = 4;  // activation rows staged per pass (MMA columns 4-7 repeat row 3)
 
 __device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
   uint32_t d;
@@ -45,278 +45,334 @@ __device__ __forceinline__ uint32_t pair128(uint32_t word, int p) {
 }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1, const float (&c)[4]) {
+                                               uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%10, %11, %12, %13};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
-        "f"(c[2]), "f"(c[3]));
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float bf16f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// In place: each 16-byte block c (activations 8c'..8c'+7 of group g, c' = c % 8) becomes the
-// MMA B fragments of lane slot t = c'/2 for m = 2(c'%2) + {0,1}: {x0,x4 | x1,x5} and
-// {x2,x6 | x3,x7}; the block's sum goes into the group sum.  Rows >= R are zeroed.
-// Run by `nthreads` threads (a multiple of 32, starting at thread 0).
-__device__ __forceinline__ void permute_rows(uint8_t *xb, float *xs, int xrb, int G, int R,
-                                             int nthreads) {
-  for (int i = threadIdx.x; i < kTok * G * 8; i += nthreads) {
-    const int j = i / (G * 8), rem = i - j * G * 8, g = rem >> 3;
-    uint4 *blk = reinterpret_cast<uint4 *>(xb + (size_t)j * xrb + rem * 16);
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    if (j < R) q = *blk;
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    auto el = [&](int e) -> uint32_t { return (e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu); };
-    float part = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) part += __uint_as_float(el(e) << 16);
-    uint4 o;
-    o.x = el(0) | (el(4) << 16);
-    o.y = el(1) | (el(5) << 16);
-    o.z = el(2) | (el(6) << 16);
-    o.w = el(3) | (el(7) << 16);
-    *blk = o;
-    // the 8 blocks of one (row, group) are 8 consecutive lanes
-    part += __shfl_xor_sync(0xffffffffu, part, 1);
-    part += __shfl_xor_sync(0xffffffffu, part, 2);
-    part += __shfl_xor_sync(0xffffffffu, part, 4);
-    if ((rem & 7) == 0) xs[j * G + g] = part;
-  }
-}
-
-// Dot products of a warp's 16 weight rows with the staged activation rows.
-//   wrows: the warp's 16 packed weight rows in shared memory (rows 0-7: MMA rows g,
-//          rows 8-15: MMA rows g + 8), row stride ws
-//   scA / scB: scale rows of MMA rows g and g+8 in shared memory (biases at +bofs)
-// acc[0], acc[1]: row g with activation rows 2t, 2t+1; acc[2], acc[3]: row g+8.
-// Two groups per iteration, each as two independent MMA chains, keep four chains in flight.
-__device__ __forceinline__ void group_mma(const uint8_t *rA, const uint8_t *rB, const uint8_t *xrow,
-                                          int g, float (&d0)[4], float (&d1)[4]) {
-  const uint2 A = *reinterpret_cast<const uint2 *>(rA + g * 32);
-  const uint2 B = *reinterpret_cast<const uint2 *>(rB + g * 32);
-  // the four B fragments of the group: two 16-byte loads
-  const uint4 f01 = *reinterpret_cast<const uint4 *>(xrow + g * 128);
-  const uint4 f23 = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
+// D_g of one group for the lane's two weight rows (A: MMA row gq, B: row gq + 8) and the
+// staged activation columns, as one chain of four MMAs.
+//   wa, wb: the lane's 8 packed bytes of the group in rows A and B (k = 16t .. 16t+15)
+//   f01, f23: the lane's two permuted 16-byte activation blocks of the group
+__device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, uint4 f01, uint4 f23,
+                                          float (&d)[4]) {
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
-    const uint32_t wA = (m >> 1) ? A.y : A.x;
-    const uint32_t wB = (m >> 1) ? B.y : B.x;
+    const uint32_t ua = (m >> 1) ? wa.y : wa.x;
+    const uint32_t ub = (m >> 1) ? wb.y : wb.x;
     const int p0 = 2 * (m & 1);
-    const uint32_t a[4] = {pair128(wA, p0), pair128(wB, p0), pair128(wA, p0 + 1),
-                           pair128(wB, p0 + 1)};
+    const uint32_t a[4] = {pair128(ua, p0), pair128(ub, p0), pair128(ua, p0 + 1),
+                           pair128(ub, p0 + 1)};
     const uint32_t b0 = m == 0 ? f01.x : m == 1 ? f01.z : m == 2 ? f23.x : f23.z;
     const uint32_t b1 = m == 0 ? f01.y : m == 1 ? f01.w : m == 2 ? f23.y : f23.w;
-    if (m < 2)
-      mma_bf16_16816(d0, a, b0, b1, d0);
-    else
-      mma_bf16_16816(d1, a, b0, b1, d1);
+    mma_bf16_16816(d, a, b0, b1);
   }
 }
 
-__device__ __forceinline__ void group_fold(const uint16_t *scA, const uint16_t *scB, int bofs,
-                                           const float *xs0, const float *xs1, int g,
-                                           const float (&d0)[4], const float (&d1)[4],
-                                           float (&acc)[4]) {
-  const float s_a = bf16f(scA[g]), s_b = bf16f(scB[g]);
-  const float c_a = fmaf(-128.f, s_a, bf16f(scA[bofs + g]));
-  const float c_b = fmaf(-128.f, s_b, bf16f(scB[bofs + g]));
-  const float x0 = xs0[g], x1 = xs1[g];
-  acc[0] = fmaf(s_a, d0[0] + d1[0], fmaf(c_a, x0, acc[0]));
-  acc[1] = fmaf(s_a, d0[1] + d1[1], fmaf(c_a, x1, acc[1]));
-  acc[2] = fmaf(s_b, d0[2] + d1[2], fmaf(c_b, x0, acc[2]));
-  acc[3] = fmaf(s_b, d0[3] + d1[3], fmaf(c_b, x1, acc[3]));
+// acc += s * D + (b - 128 s) * X for rows A (acc[0], acc[1]) and B (acc[2], acc[3]) and
+// the lane's two activation columns (x.x, x.y)
+__device__ __forceinline__ void group_fold(float sa, float ba, float sb, float bb, float2 x,
+                                           const float (&d)[4], float (&acc)[4]) {
+  const float ca = fmaf(-128.f, sa, ba), cb = fmaf(-128.f, sb, bb);
+  acc[0] = fmaf(sa, d[0], fmaf(ca, x.x, acc[0]));
+  acc[1] = fmaf(sa, d[1], fmaf(ca, x.y, acc[1]));
+  acc[2] = fmaf(sb, d[2], fmaf(cb, x.x, acc[2]));
+  acc[3] = fmaf(sb, d[3], fmaf(cb, x.y, acc[3]));
 }
 
-__device__ __forceinline__ void warp_rows_dot(const uint8_t *wrows, int ws, const uint16_t *scA,
-                                              const uint16_t *scB, int bofs, const uint8_t *xb,
-                                              int xrb, const float *xs, int G, int g_begin,
-                                              int g_end, float (&acc)[4]) {
-  const int lane = threadIdx.x & 31, gq = lane >> 2, t = lane & 3;
-  // B column gq = activation row gq; columns past the staged rows repeat the last one
-  const uint8_t *xrow = xb + (size_t)min(gq, kTok - 1) * xrb + t * 32;
-  const float *xs0 = xs + min(2 * t, kTok - 1) * G, *xs1 = xs + min(2 * t + 1, kTok - 1) * G;
-  const uint8_t *rA = wrows + gq * ws + t * 8, *rB = rA + 8 * ws;
+
+// Dot products of the warp's 16 staged weight rows with the staged activation rows over
+// groups [g_begin, g_end).
+//   rA, rB: the lane's rows (MMA rows gq and gq + 8) at byte t*8 of group 0
+//   scA, scB: scale rows of MMA rows gq and gq + 8 (bf16; biases at + bofs elements)
+//   xrow: the lane's activation row (MMA column gq) at byte t*32 of group 0
+//   xs0, xs1: group sums of the activation rows of the lane's two output columns
+// PAIR: the scales and sums of groups g, g+1 are read as pairs (needs even G and even
+// g_begin).
+template <bool PAIR>
+__device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *rB,
+                                              const uint16_t *scA, const uint16_t *scB, int bofs,
+                                              const uint8_t *xrow, const float *xs0,
+                                              const float *xs1, int g_begin, int g_end,
+                                              float (&acc)[4]) {
   int g = g_begin;
 #pragma unroll 1
   for (; g + 1 < g_end; g += 2) {
-    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-    float q0[4] = {0.f, 0.f, 0.f, 0.f}, q1[4] = {0.f, 0.f, 0.f, 0.f};
-    group_mma(rA, rB, xrow, g, p0, p1);
-    group_mma(rA, rB, xrow, g + 1, q0, q1);
-    group_fold(scA, scB, bofs, xs0, xs1, g, p0, p1, acc);
-    group_fold(scA, scB, bofs, xs0, xs1, g + 1, q0, q1, acc);
+    const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
+    const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
+    const uint2 a1 = *reinterpret_cast<const uint2 *>(rA + g * 32 + 32);
+    const uint2 b1 = *reinterpret_cast<const uint2 *>(rB + g * 32 + 32);
+    const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
+    const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
+    const uint4 f1a = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 128);
+    const uint4 f1b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 144);
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    group_mma(a0, b0, f0a, f0b, d0);
+    group_mma(a1, b1, f1a, f1b, d1);
+    float sa0, sa1, sb0, sb1, ba0, ba1, bb0, bb1;
+    float2 xg0, xg1;  // {column 2t, column 2t+1} sums of groups g and g + 1
+    if (PAIR) {
+      const uint32_t us_a = *reinterpret_cast<const uint32_t *>(scA + g);
+      const uint32_t us_b = *reinterpret_cast<const uint32_t *>(scB + g);
+      const uint32_t ub_a = *reinterpret_cast<const uint32_t *>(scA + bofs + g);
+      const uint32_t ub_b = *reinterpret_cast<const uint32_t *>(scB + bofs + g);
+      sa0 = __uint_as_float(us_a << 16);
+      sa1 = __uint_as_float(us_a & 0xFFFF0000u);
+      sb0 = __uint_as_float(us_b << 16);
+      sb1 = __uint_as_float(us_b & 0xFFFF0000u);
+      ba0 = __uint_as_float(ub_a << 16);
+      ba1 = __uint_as_float(ub_a & 0xFFFF0000u);
+      bb0 = __uint_as_float(ub_b << 16);
+      bb1 = __uint_as_float(ub_b & 0xFFFF0000u);
+      const float2 p0 = *reinterpret_cast<const float2 *>(xs0 + g);
+      const float2 p1 = *reinterpret_cast<const float2 *>(xs1 + g);
+      xg0 = make_float2(p0.x, p1.x);
+      xg1 = make_float2(p0.y, p1.y);
+    } else {
+      sa0 = bf16f(scA[g]);
+      sa1 = bf16f(scA[g + 1]);
+      sb0 = bf16f(scB[g]);
+      sb1 = bf16f(scB[g + 1]);
+      ba0 = bf16f(scA[bofs + g]);
+      ba1 = bf16f(scA[bofs + g + 1]);
+      bb0 = bf16f(scB[bofs + g]);
+      bb1 = bf16f(scB[bofs + g + 1]);
+      xg0 = make_float2(xs0[g], xs1[g]);
+      xg1 = make_float2(xs0[g + 1], xs1[g + 1]);
+    }
+    group_fold(sa0, ba0, sb0, bb0, xg0, d0, acc);
+    group_fold(sa1, ba1, sb1, bb1, xg1, d1, acc);
   }
   if (g < g_end) {
-    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-    group_mma(rA, rB, xrow, g, p0, p1);
-    group_fold(scA, scB, bofs, xs0, xs1, g, p0, p1, acc);
+    const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
+    const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
+    const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
+    const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
+    float d0[4] = {0.f, 0.f, 0.f, 0.f};
+    group_mma(a0, b0, f0a, f0b, d0);
+    group_fold(bf16f(scA[g]), bf16f(scA[bofs + g]), bf16f(scB[g]), bf16f(scB[bofs + g]),
+               make_float2(xs0[g], xs1[g]), d0, acc);
   }
 }
 
-// The persistent kernel: one CTA per SM walks a contiguous range of work
-// chunks (a chunk = 16 weight rows of one expert tile: 8 gate rows + their 8 up
-// rows, or 16 down rows).  A producer warp streams each chunk's packed rows and
-// scale/bias rows into a ring of shared-memory buffers with 1-D bulk copies
-// (every row is contiguous in global memory); up to 16 compute warps take
-// chunks in turn.  When the range moves to the next tile, the compute warps stage that
-// tile's activation rows (kTok per pass) in MMA fragment order.
-// Compute warps per CTA: 16, in 8 pairs (fewer if the ring holds fewer than 8 chunks).
-// The two warps of a pair split a chunk's K range and combine their partial sums in the
-// chunk's buffer.  Pair p takes chunks p, p + P, ... and chunk i uses buffer i % nbuf; with
-// P <= nbuf the previous use of a buffer always belongs to a chunk that landed before the
-// pair's previous chunk, so a parity wait on the buffer's barrier never runs a phase ahead.
-constexpr int kMaxComputeWarps = 16;
-
-__device__ __forceinline__ void named_sync_pair(int pair) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + pair) : "memory");
+// In place: the eight 16-byte blocks of activation row r, group g (elements 8c .. 8c+7
+// in block c) become the MMA B fragments {x0,x4 | x1,x5 | x2,x6 | x3,x7}, and the group's
+// sum goes to xs[r * G + g].  Units u = r * G + g, u = first, first + step, ...; a thread
+// visits its blocks in an order rotated by u, so neighbouring threads hit other banks.
+__device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb, int G, int nrows,
+                                              int first, int step) {
+  for (int u = first; u < nrows * G; u += step) {
+    const int r = u / G, g = u - r * G;
+    uint8_t *base = xbuf + (size_t)r * xrb + g * 128;
+    uint4 q[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(base + ((c + u) & 7) * 16);
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+      auto el = [&](int k) -> uint32_t {
+        return (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
+      };
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum += __uint_as_float(el(k) << 16);
+      uint4 o;
+      o.x = el(0) | (el(4) << 16);
+      o.y = el(1) | (el(5) << 16);
+      o.z = el(2) | (el(6) << 16);
+      o.w = el(3) | (el(7) << 16);
+      *reinterpret_cast<uint4 *>(base + ((c + u) & 7) * 16) = o;
+    }
+    xs[u] = sum;
+  }
 }
 
-// Chunks per segment: the scale and bias rows of a segment's chunks are staged with a
-// few large bulk copies at the segment start (a TMA operation costs about the same
-// whatever its size, so many small per-chunk scale copies would dominate).
-constexpr int kSegChunks = 8;
+// ---------------------------------------------------------------- the persistent kernel
+//
+// One CTA per SM walks a contiguous range of work chunks.  A chunk is 16 weight rows of
+// one expert tile (gate/up: 8 gate rows and the 8 matching up rows; down: 16 rows) with
+// their scale and bias rows.  Roles:
+//   producer warp: streams chunks into a ring of shared-memory buffers (TMA boxes for the
+//     weight rows, bulk copies for the scale and bias rows);
+//   stager warp: brings the activation rows into shared memory.  When every activation
+//     row fits ("whole" mode: decode-sized calls) it copies them all at once at the
+//     start, and every warp but the producer then permutes them into MMA fragment order;
+//     otherwise, per pass over a tile (up to `ktok` of its rows) it copies and permutes
+//     the pass's rows into one of two buffers and hands that buffer to the compute warps;
+//   compute warps, in teams: a team takes every nteams-th chunk; its warps split the
+//     chunk's groups, combine their partial sums in the consumed buffer, and the first
+//     warp writes the results.
+// Work order (shared by all roles): the range's tiles in order; per tile ceil(R / ktok)
+// passes; per pass the range's chunks of that tile.  Team p takes chunks p, p + P, ...;
+// chunk i uses ring buffer i % nbuf, and P <= nbuf keeps a team's parity wait on a
+// buffer from ever running a phase ahead.
+//
+// DOWN with a fused cast: the leader warp of each (tile, pass, chunk j) adds the pass's
+// row count to counter j (one per 16 output columns, zeroed with y_acc); the warp whose
+// addition reaches A has seen every contribution to those columns and writes them to y
+// as bf16.
+template <int MODE>
+struct GemvCfg {
+  static constexpr int kTeam = MODE == 0 ? 2 : 1;         // warps per chunk (split K)
+  static constexpr int kMaxCompute = MODE == 0 ? 16 : 24;  // compute warps per CTA
+  static constexpr int kThreads = (kMaxCompute + 2) * 32;
+  static constexpr int kBoxRows = MODE == 0 ? 8 : 16;      // weight rows per TMA box
+};
+
+// Row stride of staged weight rows: the packed row (K/2 bytes) padded to 32 mod 128.
+__host__ __device__ inline int padded_row_bytes(int K) {
+  const int ws = K / 2;
+  return ws + (((32 - ws) % 128) + 128) % 128;
+}
 
 struct PLayout {
-  int G, ws, xrb, chunk_bytes, nbuf, off_x, off_xs, off_sc, sc_part, off_bar, total;
-  __host__ __device__ PLayout(int K, int nbuf_) {
+  int G, S, xrb, w_bytes, chunk_bytes, nbuf, nxrows, ntok;
+  int off_x, off_xs, off_tok, off_bar, off_misc, total;
+  // nxrows: staged activation rows (all of them, or two passes of ktok);
+  // ntok: entries of the slot -> token table (gate/up in whole mode)
+  __host__ __device__ PLayout(int K, int nxrows_, int ntok_, int nbuf_) {
     G = K / 64;
-    ws = K / 2;                      // packed weight rows, contiguous as in global memory
-    xrb = G * 128 + 16;              // activation row stride (fragment order)
-    chunk_bytes = (16 * ws + 127) & ~127;
+    S = padded_row_bytes(K);
+    xrb = G * 128 + 16;  // staged activation row (fragment order) + 16: rows in other banks
+    w_bytes = 16 * S;
+    chunk_bytes = (w_bytes + 64 * G + 127) & ~127;  // + 16 rows x G x (scale, bias) bf16
     nbuf = nbuf_;
+    nxrows = nxrows_;
+    ntok = ntok_;
     off_x = nbuf * chunk_bytes;
-    off_xs = off_x + kTok * xrb;
-    off_sc = (off_xs + kTok * G * 4 + 15) & ~15;
-    sc_part = kSegChunks * 8 * G;    // u16 elements of one quarter of the scale region
-    off_bar = off_sc + 4 * sc_part * 2;
-    total = off_bar + (2 * nbuf + 2) * 8;
+    off_xs = off_x + ((nxrows * xrb + 127) & ~127);
+    off_tok = off_xs + ((nxrows * G * 4 + 15) & ~15);
+    off_bar = off_tok + ((ntok * 4 + 15) & ~15);
+    off_misc = off_bar + (2 * nbuf + 7) * 8;
+    total = off_misc + 16;
   }
 };
 
-__host__ __device__ inline int persist_nbuf(int K) {
-  // as many chunk buffers as fit next to the activation and scale regions, at most 16
-  for (int nb = 16; nb > 2; --nb)
-    if (PLayout(K, nb).total <= 227 * 1024) return nb;
-  return 2;
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kBarStart = 10;  // named barrier of the whole-mode start (compute + stager)
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-__device__ __forceinline__ void named_sync_compute(int nthreads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
+struct GemvArgs {
+  const uint16_t *act;  // gate/up: x [T, H]; down: h [A, I]
+  const uint16_t *Sc, *Bi;
+  const int32_t *tiles, *tile_count, *perm;
+  const float *topk_weights;
+  int32_t *status;
+  int32_t T, A, top_k, H, I, ktok, nbuf, nxrows, whole;
+  uint16_t *h;
+  float *y_acc;
+  int32_t *cnt;  // DOWN: per-16-column counters (fused cast), or null
+  uint16_t *y;
+};
 
-// The CTA counts itself done on the int just past y_acc; the last one converts y_acc to
-// bf16 y.  The threadfence before the count orders this CTA's reductions before it, and
-// the last CTA reads y_acc from L2 (where the reductions were performed).
-__device__ __forceinline__ void last_cta_cast(const float *y_acc, uint16_t *y, int64_t n,
-                                              int nthreads, bool named) {
-  __shared__ int s_last;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    int *done = const_cast<int *>(reinterpret_cast<const int *>(y_acc + n));
-    s_last = (atomicAdd(done, 1) == (int)gridDim.x - 1);
-    __threadfence();
-  }
-  if (named)
-    named_sync_compute(nthreads);
-  else
-    __syncthreads();
-  if (!s_last) return;
-  for (int64_t i = threadIdx.x; i < n / 4; i += nthreads) {
-    const float4 v = __ldcg(reinterpret_cast<const float4 *>(y_acc) + i);
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t *>(&lo);
-    o.y = *reinterpret_cast<uint32_t *>(&hi);
-    reinterpret_cast<uint2 *>(y)[i] = o;
-  }
-}
-
-template <int MODE>  // 0: gate/up + GeGLU -> h; 1: down + weighted scatter -> y_acc
-__global__ void __launch_bounds__((kMaxComputeWarps + 1) * 32, 1)
-    gemv_persist_kernel(const uint16_t *__restrict__ act, const uint32_t *__restrict__ Wq,
-                        const uint16_t *__restrict__ Sc, const uint16_t *__restrict__ Bi,
-                        const int32_t *__restrict__ tiles, const int32_t *__restrict__ tile_count,
-                        const int32_t *__restrict__ perm, const float *__restrict__ topk_weights,
-                        int32_t *__restrict__ status, int32_t top_k, int32_t H, int32_t I,
-                        int32_t nbuf, uint16_t *__restrict__ h, float *__restrict__ y_acc,
-                        uint16_t *__restrict__ y_out, int64_t n_cast) {
+template <int MODE>
+__global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
+    gemv_persist_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemvArgs p) {
   using namespace umma;
-  extern __shared__ __align__(128) uint8_t gsm[];
-  if (load_status(status) != 0) return;
-  const int K = MODE == 0 ? H : I;
-  const PLayout L(K, nbuf);
+  using Cfg = GemvCfg<MODE>;
+  constexpr int TEAM = Cfg::kTeam;
+  extern __shared__ __align__(1024) uint8_t gsm[];
+  const int K = MODE == 0 ? p.H : p.I;
+  const int nbuf = p.nbuf, ktok = p.ktok;
+  const bool whole = p.whole != 0;
+  const PLayout L(K, p.nxrows, (MODE == 0 && whole) ? p.A : 0, nbuf);
   const int G = L.G;
-  const int CPT = MODE == 0 ? I / 8 : H / 16;  // chunks per tile
-  const int rows_per_expert = MODE == 0 ? 2 * I : H;
-  const int n_tiles = *tile_count;
+  const int CPT = MODE == 0 ? p.I / 8 : p.H / 16;  // chunks per tile
+  const int rows_per_expert = MODE == 0 ? 2 * p.I : p.H;
+  const int nwc = (int)(blockDim.x >> 5) - 2;  // compute warps; then producer, stager
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *xall = gsm + L.off_x;
+  float *xsall = reinterpret_cast<float *>(gsm + L.off_xs);
+  int *tok = reinterpret_cast<int *>(gsm + L.off_tok);
+  uint64_t *full = reinterpret_cast<uint64_t *>(gsm + L.off_bar);
+  uint64_t *empty = full + nbuf;
+  uint64_t *xfull = empty + nbuf;  // [2] activation copies landed (tx)
+  uint64_t *xready = xfull + 2;    // [2] activations permuted (per-pass mode)
+  uint64_t *xempty = xready + 2;   // [2] every compute warp done with the buffer
+  uint64_t *xissued = xempty + 2;  // first activation copy issued (it goes out first)
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + L.off_misc);
+
+  if (load_status(p.status) != 0) return;
+  const int n_tiles = *p.tile_count;
   const int total = n_tiles * CPT;
   const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
-  // DOWN with n_cast > 0: the last CTA to finish converts the n_cast elements of y_acc
-  // to bf16 y (its arrival counter is the int just past y_acc, zeroed with it).
-  if (c0 >= c1) {
-    if (MODE == 1 && n_cast > 0) {
-      __syncthreads();
-      last_cta_cast(y_acc, y_out, n_cast, blockDim.x, false);
-    }
+  if (c0 >= c1) return;
+  if (smem_addr(gsm) & 127) {  // TMA destinations need 128-byte alignment
+    if (threadIdx.x == 0) raise_status(p.status, MOE_ERR_CUDA);
     return;
   }
-  uint8_t *xb = gsm + L.off_x;
-  float *xs = reinterpret_cast<float *>(gsm + L.off_xs);
-  uint64_t *full = reinterpret_cast<uint64_t *>(gsm + L.off_bar);
-  uint64_t *empty = full + nbuf;
-  uint64_t *xbar = empty + nbuf;  // activations + segment scales
-  uint16_t *scs = reinterpret_cast<uint16_t *>(gsm + L.off_sc);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwc = (int)(blockDim.x >> 5) - 1;  // compute warps; the last warp produces
   if (threadIdx.x == 0) {
     for (int i = 0; i < nbuf; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(xbar, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xfull[i], 1);
+      mbar_init(&xready[i], 1);
+      mbar_init(&xempty[i], nwc);
+    }
+    mbar_init(xissued, 1);
+    *abort_flag = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  volatile int never = 0;
 
-  // Work order (shared by producer and consumers): tiles of the range in order; per tile
-  // ceil(R / kTok) passes; per pass the range's chunks of that tile.
   if (warp == nwc) {
     // ------------------------------------------------ producer
-    // A chunk is its 16 packed weight rows: two bulk copies of 8 consecutive rows (gate
-    // rows and their up rows) or one of 16 down rows, issued by lanes 0 and 1.
+    if (lane == 0) prefetch_tensormap(&tmap_w);
+    bool ok = mbar_wait(xissued, 0, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
     uint32_t it = 0;
-    bool ok = true;
+    const uint32_t tx = (uint32_t)L.w_bytes + 64u * G;
     for (int tile = c0 / CPT; ok && tile * CPT < c1; ++tile) {
-      const int e = tiles[3 * tile], R = tiles[3 * tile + 2];
+      const int e = p.tiles[3 * tile], R = p.tiles[3 * tile + 2];
       const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
-      for (int r0 = 0; ok && r0 < R; r0 += kTok) {
+      for (int r0 = 0; ok && r0 < R; r0 += ktok) {
         for (int j = j0; j < j1; ++j, ++it) {
           const int b = it % nbuf;
-          ok = mbar_wait(&empty[b], ((it / nbuf) & 1) ^ 1, &never);
+          ok = mbar_wait(&empty[b], ((it / nbuf) & 1) ^ 1, abort_flag);
           if (!(ok = __all_sync(0xffffffffu, ok))) break;
           uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
-          const uint32_t rbytes = (uint32_t)K / 2;
-          if (lane == 0) mbar_arrive_expect_tx(&full[b], 16 * rbytes);
+          uint16_t *sc = reinterpret_cast<uint16_t *>(buf + L.w_bytes);
+          if (lane == 0) {
+            fence_proxy_async_smem();  // generic accesses of the buffer before the copies
+            mbar_arrive_expect_tx(&full[b], tx);
+          }
           __syncwarp();
-          const int64_t ra = (int64_t)e * rows_per_expert + (MODE == 0 ? 8 * j : 16 * j);
+          const int64_t rbase = (int64_t)e * rows_per_expert;
           if (MODE == 0) {
-            if (lane < 2)
-              bulk_load(buf + lane * 8 * L.ws, Wq + (ra + lane * I) * (K / 8), 8 * rbytes,
-                        &full[b]);
-          } else if (lane == 0) {
-            bulk_load(buf, Wq + ra * (K / 8), 16 * rbytes, &full[b]);
+            const int64_t rg = rbase + 8 * j, ru = rg + p.I;  // gate rows, up rows
+            if (lane < 2) {
+              tma_load_2d(buf + lane * 8 * L.S, &tmap_w, 0, (int32_t)(lane ? ru : rg), &full[b]);
+            } else if (lane < 6) {
+              const int q = lane - 2;  // gate s, up s, gate b, up b
+              const uint16_t *src = (q < 2 ? p.Sc : p.Bi) + ((q & 1) ? ru : rg) * G;
+              bulk_load(sc + q * 8 * G, src, 16u * G, &full[b]);
+            }
+          } else {
+            const int64_t r = rbase + 16 * j;
+            if (lane == 0) {
+              tma_load_2d(buf, &tmap_w, 0, (int32_t)r, &full[b]);
+            } else if (lane < 3) {
+              const int q = lane - 1;  // s, b
+              bulk_load(sc + q * 16 * G, (q ? p.Bi : p.Sc) + r * G, 32u * G, &full[b]);
+            }
           }
         }
       }
     }
-    if (!ok && lane == 0) raise_status(status, MOE_ERR_TIMEOUT);
+    if (!ok && lane == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
     // drain: copies still in flight complete before the CTA exits
     __syncwarp();
     if (lane == 0)
@@ -325,106 +381,187 @@ __global__ void __launch_bounds__((kMaxComputeWarps + 1) * 32, 1)
     return;
   }
 
+  const uint32_t xbytes = (uint32_t)K * 2;
+  bool ok = true;
+  if (whole) {
+    // ------------------------------------------------ whole mode: stage every row once
+    if (warp == nwc + 1) {
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&xfull[0], (uint32_t)L.nxrows * xbytes);
+      }
+      __syncwarp();
+      for (int r = lane; r < L.nxrows; r += 32)
+        bulk_load(xall + (size_t)r * L.xrb, p.act + (int64_t)r * K, xbytes, &xfull[0]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xissued);
+      if (MODE == 0)
+        for (int i = lane; i < L.ntok; i += 32) tok[i] = p.perm[i] / p.top_k;
+    }
+    ok = mbar_wait(&xfull[0], 0, abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    const int nt = (nwc + 1) * 32, tid = warp < nwc ? (int)threadIdx.x : (int)threadIdx.x - 32;
+    if (ok) permute_units(xall, xsall, L.xrb, G, L.nxrows, tid, nt);
+    named_sync(kBarStart, nt);
+    if (warp == nwc + 1) {
+      if (!ok && lane == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+      return;
+    }
+  } else if (warp == nwc + 1) {
+    // ------------------------------------------------ stager, per pass
+    uint32_t xit = 0;
+    bool pending = false, sent = false;
+    for (int tile = c0 / CPT; ok && tile * CPT < c1; ++tile) {
+      const int row0 = p.tiles[3 * tile + 1], R = p.tiles[3 * tile + 2];
+      for (int r0 = 0; ok && r0 < R; r0 += ktok, ++xit) {
+        const int Rp = min(ktok, R - r0), xb = xit & 1;
+        ok = mbar_wait(&xempty[xb], ((xit >> 1) & 1) ^ 1, abort_flag);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        uint8_t *xbuf = xall + (size_t)xb * ktok * L.xrb;
+        float *xs = xsall + (size_t)xb * ktok * G;
+        if (lane == 0) {
+          fence_proxy_async_smem();
+          mbar_arrive_expect_tx(&xfull[xb], Rp * xbytes);
+        }
+        __syncwarp();
+        if (lane < Rp) {
+          const int64_t src_row =
+              MODE == 0 ? p.perm[row0 + r0 + lane] / p.top_k : (int64_t)row0 + r0 + lane;
+          bulk_load(xbuf + (size_t)lane * L.xrb, p.act + src_row * K, xbytes, &xfull[xb]);
+        }
+        __syncwarp();
+        if (!sent && lane == 0) mbar_arrive(xissued);
+        sent = true;
+        pending = true;
+        ok = mbar_wait(&xfull[xb], (xit >> 1) & 1, abort_flag);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        pending = false;
+        permute_units(xbuf, xs, L.xrb, G, Rp, lane, 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xready[xb]);
+      }
+    }
+    if (!ok && lane == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+    if (!sent && lane == 0) mbar_arrive(xissued);  // never leave the producer waiting
+    if (pending && lane == 0)
+      mbar_wait(&xfull[xit & 1], (xit >> 1) & 1, nullptr, 200000000ull);
+    return;
+  }
+
   // ------------------------------------------------ compute warps
   const int gq = lane >> 2, t = lane & 3;
-  const int npairs = nwc / 2, pair = warp >> 1, half = warp & 1;
-  uint32_t it = 0, xphase = 0;
-  bool ok = true;
+  const int nteams = nwc / TEAM, team = warp / TEAM, member = warp % TEAM;
+  // this warp's groups of a chunk (even boundaries keep the paired loads aligned)
+  const int gsplit = TEAM == 1 ? G : min(G, ((G + 1) / 2 + 1) & ~1);
+  const int g_lo = member == 0 ? 0 : gsplit, g_hi = member == 0 ? gsplit : G;
+  const bool pair_loads = (G % 2) == 0;
+  uint32_t it = 0, xit = 0;
   for (int tile = c0 / CPT; tile * CPT < c1; ++tile) {
-    const int e = tiles[3 * tile], row0 = tiles[3 * tile + 1], R = tiles[3 * tile + 2];
+    const int row0 = p.tiles[3 * tile + 1], R = p.tiles[3 * tile + 2];
     const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
-    for (int r0 = 0; r0 < R; r0 += kTok) {
-      const int Rp = min(kTok, R - r0);
-      for (int s0 = j0; s0 < j1; s0 += kSegChunks, xphase ^= 1) {
-        const int s1 = min(s0 + kSegChunks, j1), nseg = s1 - s0;
-        named_sync_compute(nwc * 32);  // every warp is done with the previous staging
-        if (warp == 0) {
-          // activations of this pass (one row per lane) and the segment's scale rows
-          const uint32_t xbytes = (uint32_t)K * 2;
-          const uint32_t rows_q = MODE == 0 ? 8u * nseg : 16u * nseg;  // rows per part
-          const uint32_t sbytes = rows_q * G * 2;
-          const int nparts = MODE == 0 ? 4 : 2;
-          if (lane == 0) mbar_arrive_expect_tx(xbar, Rp * xbytes + nparts * sbytes);
-          __syncwarp();
-          if (lane < Rp) {
-            const int64_t src_row =
-                MODE == 0 ? perm[row0 + r0 + lane] / top_k : row0 + r0 + lane;
-            bulk_load(xb + (size_t)lane * L.xrb, act + src_row * K, xbytes, xbar);
-          } else if (lane >= 8 && lane < 8 + nparts) {
-            const int q = lane - 8;  // GEGLU: gate s, up s, gate b, up b; DOWN: s, b
-            const int64_t r_first = MODE == 0
-                                        ? (int64_t)e * rows_per_expert + 8 * s0 + ((q & 1) ? I : 0)
-                                        : (int64_t)e * rows_per_expert + 16 * s0;
-            const uint16_t *src = (MODE == 0 ? (q < 2 ? Sc : Bi) : (q == 0 ? Sc : Bi)) + r_first * G;
-            bulk_load(scs + (size_t)q * (MODE == 0 ? L.sc_part : 2 * L.sc_part), src, sbytes,
-                      xbar);
+    for (int r0 = 0; r0 < R; r0 += ktok, ++xit) {
+      const int Rp = min(ktok, R - r0), xb = xit & 1;
+      const uint8_t *xbuf = xall;
+      const float *xs = xsall;
+      if (!whole) {
+        if (ok) ok = mbar_wait(&xready[xb], (xit >> 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        xbuf += (size_t)xb * ktok * L.xrb;
+        xs += (size_t)xb * ktok * G;
+      }
+      // staged row of pass column c (c < Rp); columns >= Rp repeat column Rp - 1 and
+      // are discarded
+      auto row_of = [&](int c) -> int {
+        c = min(c, Rp - 1);
+        if (!whole) return c;
+        return MODE == 0 ? tok[row0 + r0 + c] : row0 + r0 + c;
+      };
+      const uint8_t *xrow = xbuf + (size_t)row_of(gq) * L.xrb + t * 32;
+      const float *xs0 = xs + (size_t)row_of(2 * t) * G, *xs1 = xs + (size_t)row_of(2 * t + 1) * G;
+      // DOWN epilogue operands of the lane's two columns, fetched once per pass
+      int a_c[2] = {0, 0};
+      float w_c[2] = {0.f, 0.f};
+      if (MODE == 1) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (2 * t + c < Rp) {
+            a_c[c] = p.perm[row0 + r0 + 2 * t + c];
+            w_c[c] = p.topk_weights[a_c[c]];
+          }
+      }
+      for (int j = j0; j < j1; ++j, ++it) {
+        if ((int)(it % nteams) != team) continue;
+        const int b = it % nbuf;
+        if (ok) ok = mbar_wait(&full[b], (it / nbuf) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
+        const uint16_t *sc = reinterpret_cast<const uint16_t *>(buf + L.w_bytes);
+        const uint8_t *rA = buf + gq * L.S + t * 8, *rB = rA + 8 * L.S;
+        const uint16_t *scA = sc + gq * G, *scB = sc + (8 + gq) * G;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok) {
+          if (pair_loads)
+            warp_rows_dot<true>(rA, rB, scA, scB, 16 * G, xrow, xs0, xs1, g_lo, g_hi, acc);
+          else
+            warp_rows_dot<false>(rA, rB, scA, scB, 16 * G, xrow, xs0, xs1, g_lo, g_hi, acc);
+        }
+        if (TEAM > 1) {
+          // combine: the other warps park their sums in the consumed buffer
+          named_sync(2 + team, TEAM * 32);
+          float4 *park = reinterpret_cast<float4 *>(buf) + lane;
+          if (member) park[32 * (member - 1)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          named_sync(2 + team, TEAM * 32);
+          if (member) continue;
+#pragma unroll
+          for (int m = 1; m < TEAM; ++m) {
+            const float4 o = park[32 * (m - 1)];
+            acc[0] += o.x;
+            acc[1] += o.y;
+            acc[2] += o.z;
+            acc[3] += o.w;
           }
         }
-        ok = mbar_wait(xbar, xphase, &never) && ok;
-        permute_rows(xb, xs, L.xrb, G, Rp, nwc * 32);
-        named_sync_compute(nwc * 32);
-        for (int j = s0; j < s1; ++j, ++it) {
-          if ((int)(it % npairs) != pair) continue;
-          const int b = it % nbuf;
-          ok = mbar_wait(&full[b], (it / nbuf) & 1, &never) && ok;
-          ok = __all_sync(0xffffffffu, ok);
-          uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
-          const int jl = j - s0;
-          const uint16_t *scA, *scB;
-          int bofs;
-          if (MODE == 0) {  // gate row jl*8 + gq in part 0, its up row in part 1
-            scA = scs + (size_t)(jl * 8 + gq) * G;
-            scB = scs + L.sc_part + (size_t)(jl * 8 + gq) * G;
-            bofs = 2 * L.sc_part;
-          } else {          // rows jl*16 + gq and + 8 in part 0 (scales), part 2 (biases)
-            scA = scs + (size_t)(jl * 16 + gq) * G;
-            scB = scs + (size_t)(jl * 16 + 8 + gq) * G;
-            bofs = 2 * L.sc_part;
-          }
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          const int gsplit = (G + 1) / 2;
-          if (ok)
-            warp_rows_dot(buf, L.ws, scA, scB, bofs, xb, L.xrb, xs, G, half ? gsplit : 0,
-                          half ? G : gsplit, acc);
-          // combine the two halves of K: the second warp parks its sums in the consumed buffer
-          named_sync_pair(pair);
-          float4 *park = reinterpret_cast<float4 *>(buf) + lane;
-          if (half) *park = make_float4(acc[0], acc[1], acc[2], acc[3]);
-          named_sync_pair(pair);
-          if (half) continue;
-          const float4 o = *park;
-          acc[0] += o.x;
-          acc[1] += o.y;
-          acc[2] += o.z;
-          acc[3] += o.w;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&empty[b]);
-          if (!ok) continue;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[b]);
+        if (!ok) continue;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const int jr = 2 * t + c;
-            if (jr >= Rp) continue;
-            if (MODE == 0) {
-              const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
-              h[(int64_t)(row0 + r0 + jr) * I + n] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
-            } else {
-              const int a = perm[row0 + r0 + jr];
-              const float w = topk_weights[a];
-              float *yrow = y_acc + (int64_t)(a / top_k) * H + 16 * j;
-              atomicAdd(yrow + gq, w * acc[c]);
-              atomicAdd(yrow + gq + 8, w * acc[2 + c]);
+        for (int c = 0; c < 2; ++c) {
+          const int jr = 2 * t + c;
+          if (jr >= Rp) continue;
+          if (MODE == 0) {
+            const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
+            p.h[(int64_t)(row0 + r0 + jr) * p.I + n] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
+          } else {
+            float *yrow = p.y_acc + (int64_t)(a_c[c] / p.top_k) * p.H + 16 * j;
+            atomicAdd(yrow + gq, w_c[c] * acc[c]);
+            atomicAdd(yrow + gq + 8, w_c[c] * acc[2 + c]);
+          }
+        }
+        if (MODE == 1 && p.cnt) {
+          // the warp barrier orders every lane's reductions before lane 0's fenced count
+          __syncwarp();
+          int last = 0;
+          if (lane == 0) {
+            __threadfence();
+            last = atomicAdd(p.cnt + j, Rp) + Rp == p.A;
+          }
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();
+            for (int i = lane; i < p.T * 16; i += 32) {
+              const int64_t o = (int64_t)(i >> 4) * p.H + 16 * j + (i & 15);
+              p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(p.y_acc + o)));
             }
           }
         }
       }
+      if (!whole) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xempty[xb]);
+      }
     }
   }
-  if (!ok) raise_status(status, MOE_ERR_TIMEOUT);
-  if (MODE == 1 && n_cast > 0) {
-    named_sync_compute(nwc * 32);  // every reduction of this CTA has been issued
-    last_cta_cast(y_acc, y_out, n_cast, nwc * 32, true);
-  }
+  if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
 }
 
 // y = bf16(y_acc), four elements per thread step
@@ -443,13 +580,7 @@ __global__ void cast_bf16_kernel(const float *__restrict__ y_acc, uint16_t *__re
   }
 }
 
-static moe_status set_smem(const void *fn, size_t smem) {
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
-}
+// ---------------------------------------------------------------- host side
 
 static int sm_count() {
   static int n = 0;
@@ -462,41 +593,118 @@ static int sm_count() {
   return n;
 }
 
+// Activation rows staged per pass in per-pass mode (the MMA has 8 columns): fewer rows
+// leave room for more ring buffers when expert tiles are small.
+static int pick_ktok(const moe_tiles_t &t) {
+  const int64_t A = t.num_assignments, used = A < t.num_experts ? A : t.num_experts;
+  if (A <= 2 * used) return 2;
+  if (A <= 4 * used) return 4;
+  return 8;
+}
+
+// Ring buffers: as many as fit beside the activation region, at most one per team.
+template <int MODE>
+static int pick_nbuf(int K, int nxrows, int ntok) {
+  using Cfg = GemvCfg<MODE>;
+  const int cap = Cfg::kMaxCompute / Cfg::kTeam;
+  for (int nb = cap; nb >= 2; --nb)
+    if (PLayout(K, nxrows, ntok, nb).total <= kSmemLimit) return nb;
+  return 0;
+}
+
+constexpr int kWholeMaxRows = 64;  // whole mode stages at most this many activation rows
+
 bool gemv_supported(int32_t H, int32_t I) {
-  return PLayout(H, 2).total <= 227 * 1024 && PLayout(I, 2).total <= 227 * 1024;
+  // one TMA box spans a padded weight row: at most 256 eight-byte elements
+  if (padded_row_bytes(H) > 2048 || padded_row_bytes(I) > 2048) return false;
+  return pick_nbuf<0>(H, 4, 0) >= 2 && pick_nbuf<1>(I, 4, 0) >= 2;
 }
 
 template <int MODE>
 static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const uint16_t *Sc,
                                  const uint16_t *Bi, const moe_tiles_t &t, const float *tw,
                                  int32_t H, int32_t I, uint16_t *h, float *y_acc, uint16_t *y,
-                                 int64_t n_cast, cudaStream_t stream, const char *what) {
+                                 bool fused_cast, cudaStream_t stream, const char *what) {
+  using Cfg = GemvCfg<MODE>;
   const int K = MODE == 0 ? H : I;
-  const int nbuf = persist_nbuf(K);
-  const size_t smem = PLayout(K, nbuf).total;
-  if (set_smem((const void *)gemv_persist_kernel<MODE>, smem) != MOE_OK) return check_launch(what);
+  const int T = t.num_tokens, A = t.num_assignments;
+  const int cap = Cfg::kMaxCompute / Cfg::kTeam;
+  // whole mode when every activation row fits beside a ring of at least 6 buffers
+  const int nx_all = MODE == 0 ? T : A, ntok_all = MODE == 0 ? A : 0;
+  const int nb_whole = nx_all <= kWholeMaxRows ? pick_nbuf<MODE>(K, nx_all, ntok_all) : 0;
+  int whole, ktok, nxrows, nbuf;
+  if (nb_whole >= (cap < 6 ? cap : 6)) {
+    whole = 1;
+    ktok = 8;
+    nxrows = nx_all;
+    nbuf = nb_whole;
+  } else {
+    whole = 0;
+    ktok = pick_ktok(t);
+    nbuf = pick_nbuf<MODE>(K, 2 * ktok, 0);
+    while (nbuf < 4 && ktok > 2) nbuf = pick_nbuf<MODE>(K, 2 * (ktok /= 2), 0);
+    nxrows = 2 * ktok;
+  }
+  if (nbuf < 2) {
+    set_error("%s: shared-memory ring does not fit (K=%d)", what, K);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const PLayout L(K, nxrows, whole ? ntok_all : 0, nbuf);
+  CUtensorMap tmap;
+  const int64_t rows = (int64_t)t.num_experts * (MODE == 0 ? 2 * I : H);
+  if (!make_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, Wq, (uint64_t)K / 16,
+                   (uint64_t)rows, (uint32_t)(L.S / 8), (uint32_t)Cfg::kBoxRows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    set_error("%s: cuTensorMapEncodeTiled failed for the weight tensor", what);
+    return MOE_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute((const void *)gemv_persist_kernel<MODE>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
+    return check_launch(what);
   const int64_t max_chunks = (int64_t)t.max_tiles * (MODE == 0 ? I / 8 : H / 16);
   int grid = sm_count();
-  if (max_chunks < grid) grid = (int)max_chunks;
-  const int nwc = 2 * nbuf < kMaxComputeWarps ? 2 * nbuf : kMaxComputeWarps;
-  gemv_persist_kernel<MODE><<<grid, (nwc + 1) * 32, smem, stream>>>(
-      act, Wq, Sc, Bi, t.tiles, t.tile_count, t.perm, tw, t.status, t.top_k, H, I, nbuf, h,
-      y_acc, y, n_cast);
+  if (max_chunks < grid) grid = (int)(max_chunks > 0 ? max_chunks : 1);
+  int nwc = nbuf * Cfg::kTeam;
+  if (nwc > Cfg::kMaxCompute) nwc = Cfg::kMaxCompute;
+  GemvArgs a;
+  a.act = act;
+  a.Sc = Sc;
+  a.Bi = Bi;
+  a.tiles = t.tiles;
+  a.tile_count = t.tile_count;
+  a.perm = t.perm;
+  a.topk_weights = tw;
+  a.status = t.status;
+  a.T = T;
+  a.A = A;
+  a.top_k = t.top_k;
+  a.H = H;
+  a.I = I;
+  a.ktok = ktok;
+  a.nbuf = nbuf;
+  a.nxrows = nxrows;
+  a.whole = whole;
+  a.h = h;
+  a.y_acc = y_acc;
+  // the column-block counters follow the T x H accumulator in the workspace
+  a.cnt = (MODE == 1 && fused_cast) ? reinterpret_cast<int32_t *>(y_acc + (int64_t)T * H) : nullptr;
+  a.y = y;
+  gemv_persist_kernel<MODE><<<grid, (nwc + 2) * 32, L.total, stream>>>(tmap, a);
   return check_launch(what);
 }
 
 moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
                              uint16_t *h, cudaStream_t stream) {
-  return launch_persist<0>(x, Wgu, Sgu, Bgu, t, nullptr, H, I, h, nullptr, nullptr, 0, stream,
-                           "moe_gather_qmm_geglu (gemv)");
+  return launch_persist<0>(x, Wgu, Sgu, Bgu, t, nullptr, H, I, h, nullptr, nullptr, false,
+                           stream, "moe_gather_qmm_geglu (gemv)");
 }
 
 moe_status launch_down_gemv(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
-                            int32_t H, int32_t I, float *y_acc, uint16_t *y, int64_t n_cast,
+                            int32_t H, int32_t I, float *y_acc, uint16_t *y, bool fused_cast,
                             cudaStream_t stream) {
-  return launch_persist<1>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y, n_cast,
+  return launch_persist<1>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y, fused_cast,
                            stream, "moe_gather_qmm_down_unsort (gemv)");
 }
 

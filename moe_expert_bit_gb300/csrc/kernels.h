@@ -10,11 +10,12 @@ namespace moeqmm {
 moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
                              uint16_t *h, cudaStream_t stream);
-// n_cast > 0: the kernel also writes y = bf16(y_acc[0 .. n_cast)) (last CTA to finish);
-// y_acc then needs an int of zeroed space just past its n_cast floats.
+// fused_cast: the kernel also writes y = bf16(y_acc), each 16-column block as soon as
+// its last contribution lands; y_acc [T, H] is then followed by H/16 zeroed int counters
+// (the workspace layout of moe_workspace_bytes).
 moe_status launch_down_gemv(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
-                            int32_t H, int32_t I, float *y_acc, uint16_t *y, int64_t n_cast,
+                            int32_t H, int32_t I, float *y_acc, uint16_t *y, bool fused_cast,
                             cudaStream_t stream);
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m);
 bool gemv_supported(int32_t H, int32_t I);

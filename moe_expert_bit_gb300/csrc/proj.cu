@@ -3,6 +3,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <initializer_list>
+
 namespace moeqmm {
 
 static moe_status validate_tiles(const char *fn, const moe_tiles_t *t) {
@@ -35,6 +37,16 @@ static moe_status validate_tiles(const char *fn, const moe_tiles_t *t) {
               t->num_assignments, t->num_experts, bm);
     return MOE_ERR_INVALID_ARG;
   }
+  return MOE_OK;
+}
+
+// every tensor pointer of the projections is moved by the copy engine: 16-byte aligned
+static moe_status validate_aligned(const char *fn, std::initializer_list<const void *> ptrs) {
+  for (const void *q : ptrs)
+    if (reinterpret_cast<uintptr_t>(q) % 16) {
+      set_error("%s: tensor pointer %p is not 16-byte aligned", fn, q);
+      return MOE_ERR_INVALID_ARG;
+    }
   return MOE_OK;
 }
 
@@ -102,6 +114,7 @@ extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *
     set_error("%s: null pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
+  if ((st = validate_aligned(fn, {x, Wgu, Sgu, Bgu, h})) != MOE_OK) return st;
   if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
   if (variant == MOE_VARIANT_TC) return launch_geglu_tc(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
   return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
@@ -122,6 +135,7 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
     set_error("%s: null pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
+  if ((st = validate_aligned(fn, {h, Wd, Sd, Bd, y_acc_ws, y})) != MOE_OK) return st;
   if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
   // zero the accumulator and the completion counter that follows it
   const int64_t n = (int64_t)tiles->num_tokens * H;
@@ -136,8 +150,8 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
   }
   // small outputs: the last CTA of the down kernel does the cast (one launch fewer)
   const bool fuse_cast = n <= (int64_t(1) << 20);
-  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, y,
-                        fuse_cast ? n : 0, stream);
+  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, y, fuse_cast,
+                        stream);
   if (st != MOE_OK || fuse_cast) return st;
   return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
 }

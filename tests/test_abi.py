@@ -42,7 +42,10 @@ def test_size_helpers():
     assert mq.moe_max_tiles(32, 128, 64) == 32
     assert mq.moe_max_tiles(64, 8, 32) == 2 + 8
     assert mq.moe_max_tiles(10, 0, 32) == 0
-    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 16
+    # accumulator + one int per 16 columns, padded to 16 bytes
+    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 704
+    assert mq.moe_workspace_bytes(4, 64) == 4 * 64 * 4 + 16
+    assert mq.moe_workspace_bytes(1, 192) == 192 * 4 + 48
     assert mq.moe_workspace_bytes(0, 2816) == 0
 
 

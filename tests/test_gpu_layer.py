@@ -82,6 +82,8 @@ def test_decode_layer_full(variant):
     (1, 128, 64, 1, 1),        # one assignment
     (3, 256, 192, 300, 2),     # tiles with many rows, ragged tail
     (16, 512, 320, 129, 4),
+    (8, 256, 128, 64, 1),      # 64 tokens / 64 assignments: every activation row staged once
+    (4, 128, 64, 16, 4),       # staged once, tiles of ~16 rows: several passes per tile
 ])
 def test_custom_shapes_full(variant, E, H, I, T, k):
     _variant_or_skip(variant)
