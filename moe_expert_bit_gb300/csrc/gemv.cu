@@ -53,6 +53,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// d = A B (no accumulator input: the first MMA of a chain)
+__device__ __forceinline__ void mma_bf16_16816_first(float (&d)[4], const uint32_t (&a)[4],
+                                                     uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
 __device__ __forceinline__ float bf16f(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
@@ -72,7 +82,10 @@ __device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, uint4 f01, uint4 f
                            pair128(ub, p0 + 1)};
     const uint32_t b0 = m == 0 ? f01.x : m == 1 ? f01.z : m == 2 ? f23.x : f23.z;
     const uint32_t b1 = m == 0 ? f01.y : m == 1 ? f01.w : m == 2 ? f23.y : f23.w;
-    mma_bf16_16816(d, a, b0, b1);
+    if (m == 0)
+      mma_bf16_16816_first(d, a, b0, b1);
+    else
+      mma_bf16_16816(d, a, b0, b1);
   }
 }
 
@@ -94,8 +107,14 @@ __device__ __forceinline__ void group_fold(float sa, float ba, float sb, float b
 //   scA, scB: scale rows of MMA rows gq and gq + 8 (bf16; biases at + bofs elements)
 //   xrow: the lane's activation row (MMA column gq) at byte t*32 of group 0
 //   xs0, xs1: group sums of the activation rows of the lane's two output columns
-// PAIR: the scales and sums of groups g, g+1 are read as pairs (needs even G and even
-// g_begin).
+// PAIR: the scales and sums of groups g, g+1 are read as pairs from an even g (needs
+// even G: rows start 4-byte aligned); an odd first group is done on its own.
+template <bool PAIR>
+__device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
+                                          const uint16_t *scA, const uint16_t *scB, int bofs,
+                                          const uint8_t *xrow, const float *xs0,
+                                          const float *xs1, int g, float (&acc)[4]);
+
 template <bool PAIR>
 __device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *rB,
                                               const uint16_t *scA, const uint16_t *scB, int bofs,
@@ -103,6 +122,10 @@ __device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *
                                               const float *xs1, int g_begin, int g_end,
                                               float (&acc)[4]) {
   int g = g_begin;
+  if (PAIR && (g & 1) && g < g_end) {
+    one_group<PAIR>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g, acc);
+    ++g;
+  }
 #pragma unroll 1
   for (; g + 1 < g_end; g += 2) {
     const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
@@ -113,7 +136,7 @@ __device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *
     const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
     const uint4 f1a = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 128);
     const uint4 f1b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 144);
-    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    float d0[4], d1[4];
     group_mma(a0, b0, f0a, f0b, d0);
     group_mma(a1, b1, f1a, f1b, d1);
     float sa0, sa1, sb0, sb1, ba0, ba1, bb0, bb1;
@@ -150,16 +173,22 @@ __device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *
     group_fold(sa0, ba0, sb0, bb0, xg0, d0, acc);
     group_fold(sa1, ba1, sb1, bb1, xg1, d1, acc);
   }
-  if (g < g_end) {
-    const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
-    const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
-    const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
-    const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
-    float d0[4] = {0.f, 0.f, 0.f, 0.f};
-    group_mma(a0, b0, f0a, f0b, d0);
-    group_fold(bf16f(scA[g]), bf16f(scA[bofs + g]), bf16f(scB[g]), bf16f(scB[bofs + g]),
-               make_float2(xs0[g], xs1[g]), d0, acc);
-  }
+  if (g < g_end) one_group<PAIR>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g, acc);
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
+                                          const uint16_t *scA, const uint16_t *scB, int bofs,
+                                          const uint8_t *xrow, const float *xs0,
+                                          const float *xs1, int g, float (&acc)[4]) {
+  const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
+  const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
+  const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
+  const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
+  float d0[4];
+  group_mma(a0, b0, f0a, f0b, d0);
+  group_fold(bf16f(scA[g]), bf16f(scA[bofs + g]), bf16f(scB[g]), bf16f(scB[bofs + g]),
+             make_float2(xs0[g], xs1[g]), d0, acc);
 }
 
 // In place: the eight 16-byte blocks of activation row r, group g (elements 8c .. 8c+7
@@ -196,9 +225,10 @@ __device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb,
 
 // ---------------------------------------------------------------- the persistent kernel
 //
-// One CTA per SM walks a contiguous range of work chunks.  A chunk is 16 weight rows of
-// one expert tile (gate/up: 8 gate rows and the 8 matching up rows; down: 16 rows) with
-// their scale and bias rows.  Roles:
+// One CTA per SM walks a contiguous range of work chunks.  A chunk is a block of weight
+// rows of one expert tile with their scale and bias rows: gate/up, 8 gate rows and the 8
+// matching up rows (one MMA tile of 16 rows, its K split over the warps of a team);
+// down, 64 rows (16 per warp of a team, each warp over the whole K).  Roles:
 //   producer warp: streams chunks into a ring of shared-memory buffers (TMA boxes for the
 //     weight rows, bulk copies for the scale and bias rows);
 //   stager warp: brings the activation rows into shared memory.  When every activation
@@ -206,24 +236,29 @@ __device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb,
 //     start, and every warp but the producer then permutes them into MMA fragment order;
 //     otherwise, per pass over a tile (up to `ktok` of its rows) it copies and permutes
 //     the pass's rows into one of two buffers and hands that buffer to the compute warps;
-//   compute warps, in teams: a team takes every nteams-th chunk; its warps split the
-//     chunk's groups, combine their partial sums in the consumed buffer, and the first
-//     warp writes the results.
+//   compute warps, in teams: a team takes every nteams-th chunk.  Gate/up: its warps
+//     split the chunk's groups, combine their partial sums in the consumed buffer, and
+//     the first warp writes the results.  Down: each warp owns 16 of the rows.
 // Work order (shared by all roles): the range's tiles in order; per tile ceil(R / ktok)
 // passes; per pass the range's chunks of that tile.  Team p takes chunks p, p + P, ...;
-// chunk i uses ring buffer i % nbuf, and P <= nbuf keeps a team's parity wait on a
-// buffer from ever running a phase ahead.
+// chunk i uses ring buffer i % nbuf.  nbuf >= 2P: every team has a second buffer in
+// flight while it computes on one (and P <= nbuf keeps a team's parity wait on a buffer
+// from ever running a phase ahead).
 //
 // DOWN with a fused cast: the leader warp of each (tile, pass, chunk j) adds the pass's
 // row count to counter j (one per 16 output columns, zeroed with y_acc); the warp whose
 // addition reaches A has seen every contribution to those columns and writes them to y
 // as bf16.
+constexpr int kSplitKTeam = 4;  // gate/up: warps sharing one 16-row chunk
+
 template <int MODE>
 struct GemvCfg {
-  static constexpr int kTeam = MODE == 0 ? 2 : 1;         // warps per chunk (split K)
-  static constexpr int kMaxCompute = MODE == 0 ? 16 : 24;  // compute warps per CTA
+  static constexpr int kTeam = MODE == 0 ? kSplitKTeam : 4;  // warps per chunk
+  static constexpr bool kSplitK = MODE == 0;                // else: split rows
+  static constexpr int kRows = MODE == 0 ? 16 : 16 * kTeam;  // weight rows per chunk
+  static constexpr int kBoxRows = MODE == 0 ? 8 : kRows;     // weight rows per TMA box
+  static constexpr int kMaxCompute = 16;                     // compute warps per CTA
   static constexpr int kThreads = (kMaxCompute + 2) * 32;
-  static constexpr int kBoxRows = MODE == 0 ? 8 : 16;      // weight rows per TMA box
 };
 
 // Row stride of staged weight rows: the packed row (K/2 bytes) padded to 32 mod 128.
@@ -233,16 +268,19 @@ __host__ __device__ inline int padded_row_bytes(int K) {
 }
 
 struct PLayout {
-  int G, S, xrb, w_bytes, chunk_bytes, nbuf, nxrows, ntok;
+  int G, S, xrb, rows, w_bytes, chunk_bytes, nbuf, nxrows, ntok;
   int off_x, off_xs, off_tok, off_bar, off_misc, total;
-  // nxrows: staged activation rows (all of them, or two passes of ktok);
-  // ntok: entries of the slot -> token table (gate/up in whole mode)
-  __host__ __device__ PLayout(int K, int nxrows_, int ntok_, int nbuf_) {
+  // rows: weight rows per chunk; nxrows: staged activation rows (all of them, or two
+  // passes of ktok); ntok: entries of the slot -> token table (gate/up in whole mode)
+  __host__ __device__ PLayout(int K, int rows_, int nxrows_, int ntok_, int nbuf_) {
     G = K / 64;
     S = padded_row_bytes(K);
     xrb = G * 128 + 16;  // staged activation row (fragment order) + 16: rows in other banks
-    w_bytes = 16 * S;
-    chunk_bytes = (w_bytes + 64 * G + 127) & ~127;  // + 16 rows x G x (scale, bias) bf16
+    rows = rows_;
+    w_bytes = rows * S;
+    chunk_bytes = (w_bytes + 4 * rows * G + 127) & ~127;  // + rows x G x (scale, bias) bf16
+    // a split-K team parks the partial sums of all but its first warp in the buffer
+    if (rows == 16 && chunk_bytes < (kSplitKTeam - 1) * 512) chunk_bytes = (kSplitKTeam - 1) * 512;
     nbuf = nbuf_;
     nxrows = nxrows_;
     ntok = ntok_;
@@ -256,11 +294,21 @@ struct PLayout {
 };
 
 constexpr int kSmemLimit = 227 * 1024;
-constexpr int kBarStart = 10;  // named barrier of the whole-mode start (compute + stager)
+// named barriers: 0 the CTA, 1 every compute warp, 2 + 2p and 3 + 2p team p's combine
+// (split K), 15 the whole-mode start (compute warps + stager)
+constexpr int kBarStart = 15;
+constexpr int kMaxTeams = 13;
 
 __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+struct GemvArgs;
+__device__ void cast_block(const GemvArgs &p, int blk, int lane);
 
 struct GemvArgs {
   const uint16_t *act;  // gate/up: x [T, H]; down: h [A, I]
@@ -275,6 +323,16 @@ struct GemvArgs {
   uint16_t *y;
 };
 
+// y[:, 16 blk .. 16 blk + 15] = bf16(y_acc[...]) by one warp, after the count of block blk
+// reached A (every contribution performed; the fence orders the reads after the count)
+__device__ void cast_block(const GemvArgs &p, int blk, int lane) {
+  __threadfence();
+  for (int i = lane; i < p.T * 16; i += 32) {
+    const int64_t o = (int64_t)(i >> 4) * p.H + 16 * blk + (i & 15);
+    p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(p.y_acc + o)));
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
     gemv_persist_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemvArgs p) {
@@ -285,9 +343,9 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   const int K = MODE == 0 ? p.H : p.I;
   const int nbuf = p.nbuf, ktok = p.ktok;
   const bool whole = p.whole != 0;
-  const PLayout L(K, p.nxrows, (MODE == 0 && whole) ? p.A : 0, nbuf);
+  const PLayout L(K, Cfg::kRows, p.nxrows, (MODE == 0 && whole) ? p.A : 0, nbuf);
   const int G = L.G;
-  const int CPT = MODE == 0 ? p.I / 8 : p.H / 16;  // chunks per tile
+  const int CPT = MODE == 0 ? p.I / 8 : p.H / Cfg::kRows;  // chunks per tile
   const int rows_per_expert = MODE == 0 ? 2 * p.I : p.H;
   const int nwc = (int)(blockDim.x >> 5) - 2;  // compute warps; then producer, stager
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -315,7 +373,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < nbuf; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], Cfg::kSplitK ? 1 : TEAM);  // the leader, or every warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&xfull[i], 1);
@@ -334,7 +392,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
     bool ok = mbar_wait(xissued, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     uint32_t it = 0;
-    const uint32_t tx = (uint32_t)L.w_bytes + 64u * G;
+    const uint32_t tx = (uint32_t)L.w_bytes + 4u * Cfg::kRows * G;
     for (int tile = c0 / CPT; ok && tile * CPT < c1; ++tile) {
       const int e = p.tiles[3 * tile], R = p.tiles[3 * tile + 2];
       const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
@@ -351,22 +409,25 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
           }
           __syncwarp();
           const int64_t rbase = (int64_t)e * rows_per_expert;
+          // the issuing lanes rotate over four groups of 8: a lane's copies go out one
+          // chunk in four (a thread's successive copies are issued one after another)
+          const int q = lane - 8 * (int)(it & 3);
           if (MODE == 0) {
             const int64_t rg = rbase + 8 * j, ru = rg + p.I;  // gate rows, up rows
-            if (lane < 2) {
-              tma_load_2d(buf + lane * 8 * L.S, &tmap_w, 0, (int32_t)(lane ? ru : rg), &full[b]);
-            } else if (lane < 6) {
-              const int q = lane - 2;  // gate s, up s, gate b, up b
-              const uint16_t *src = (q < 2 ? p.Sc : p.Bi) + ((q & 1) ? ru : rg) * G;
-              bulk_load(sc + q * 8 * G, src, 16u * G, &full[b]);
+            if (q == 0 || q == 1) {
+              tma_load_2d(buf + q * 8 * L.S, &tmap_w, 0, (int32_t)(q ? ru : rg), &full[b]);
+            } else if (q >= 2 && q < 6) {
+              const int k = q - 2;  // gate s, up s, gate b, up b
+              const uint16_t *src = (k < 2 ? p.Sc : p.Bi) + ((k & 1) ? ru : rg) * G;
+              bulk_load(sc + k * 8 * G, src, 16u * G, &full[b]);
             }
           } else {
-            const int64_t r = rbase + 16 * j;
-            if (lane == 0) {
+            const int64_t r = rbase + (int64_t)Cfg::kRows * j;
+            if (q == 0) {
               tma_load_2d(buf, &tmap_w, 0, (int32_t)r, &full[b]);
-            } else if (lane < 3) {
-              const int q = lane - 1;  // s, b
-              bulk_load(sc + q * 16 * G, (q ? p.Bi : p.Sc) + r * G, 32u * G, &full[b]);
+            } else if (q == 1 || q == 2) {  // scales, biases
+              bulk_load(sc + (q - 1) * Cfg::kRows * G, (q == 2 ? p.Bi : p.Sc) + r * G,
+                        2u * Cfg::kRows * G, &full[b]);
             }
           }
         }
@@ -451,10 +512,23 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   // ------------------------------------------------ compute warps
   const int gq = lane >> 2, t = lane & 3;
   const int nteams = nwc / TEAM, team = warp / TEAM, member = warp % TEAM;
-  // this warp's groups of a chunk (even boundaries keep the paired loads aligned)
-  const int gsplit = TEAM == 1 ? G : min(G, ((G + 1) / 2 + 1) & ~1);
-  const int g_lo = member == 0 ? 0 : gsplit, g_hi = member == 0 ? gsplit : G;
+  // split K: this warp's groups [m G / TEAM, (m+1) G / TEAM); split rows: all groups of
+  // rows 16 m .. 16 m + 15
+  int g_lo = 0, g_hi = G, row_lo = 0;
+  if (Cfg::kSplitK) {
+    g_lo = member * G / TEAM;
+    g_hi = (member + 1) * G / TEAM;
+  } else {
+    row_lo = 16 * member;
+  }
   const bool pair_loads = (G % 2) == 0;
+  // DOWN fused cast, pipelined one chunk deep so that no warp waits on a fence or on the
+  // counter's round trip: a chunk's reductions are counted after the next chunk's dot
+  // (when they have long been performed), and the count's result is looked at one chunk
+  // later still.
+  int pend_blk = -1, pend_rows = 0;  // reductions issued, not yet counted
+  int flt_blk = -1, flt_rows = 0;    // counted; lane 0 holds the counter's old value
+  int flt_old = 0;
   uint32_t it = 0, xit = 0;
   for (int tile = c0 / CPT; tile * CPT < c1; ++tile) {
     const int row0 = p.tiles[3 * tile + 1], R = p.tiles[3 * tile + 2];
@@ -496,22 +570,29 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
         const uint16_t *sc = reinterpret_cast<const uint16_t *>(buf + L.w_bytes);
-        const uint8_t *rA = buf + gq * L.S + t * 8, *rB = rA + 8 * L.S;
-        const uint16_t *scA = sc + gq * G, *scB = sc + (8 + gq) * G;
+        const uint8_t *rA = buf + (row_lo + gq) * L.S + t * 8, *rB = rA + 8 * L.S;
+        const uint16_t *scA = sc + (row_lo + gq) * G, *scB = scA + 8 * G;
+        const int bofs = Cfg::kRows * G;  // biases follow the chunk's scales
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (ok) {
           if (pair_loads)
-            warp_rows_dot<true>(rA, rB, scA, scB, 16 * G, xrow, xs0, xs1, g_lo, g_hi, acc);
+            warp_rows_dot<true>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g_lo, g_hi, acc);
           else
-            warp_rows_dot<false>(rA, rB, scA, scB, 16 * G, xrow, xs0, xs1, g_lo, g_hi, acc);
+            warp_rows_dot<false>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g_lo, g_hi, acc);
         }
-        if (TEAM > 1) {
-          // combine: the other warps park their sums in the consumed buffer
-          named_sync(2 + team, TEAM * 32);
+        if (Cfg::kSplitK) {
+          // combine: once every warp of the team is done reading the buffer, the other
+          // warps park their sums in it and go on; only the first warp waits for them.
+          // (No warp passes the team's next first barrier before the first warp is there,
+          // so the arrivals of two chunks never meet on one barrier.)
+          named_sync(2 + 2 * team, TEAM * 32);
           float4 *park = reinterpret_cast<float4 *>(buf) + lane;
-          if (member) park[32 * (member - 1)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-          named_sync(2 + team, TEAM * 32);
-          if (member) continue;
+          if (member) {
+            park[32 * (member - 1)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            named_arrive(3 + 2 * team, TEAM * 32);
+            continue;
+          }
+          named_sync(3 + 2 * team, TEAM * 32);
 #pragma unroll
           for (int m = 1; m < TEAM; ++m) {
             const float4 o = park[32 * (m - 1)];
@@ -524,6 +605,23 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[b]);
         if (!ok) continue;
+        if (MODE == 1 && p.cnt) {
+          if (flt_blk >= 0) {  // the count issued one chunk ago
+            const int old = __shfl_sync(0xffffffffu, flt_old, 0);
+            if (old + flt_rows == p.A) cast_block(p, flt_blk, lane);
+            flt_blk = -1;
+          }
+          if (pend_blk >= 0) {  // count the previous chunk's reductions
+            __syncwarp();
+            if (lane == 0) {
+              __threadfence();
+              flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
+            }
+            flt_blk = pend_blk;
+            flt_rows = pend_rows;
+            pend_blk = -1;
+          }
+        }
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int jr = 2 * t + c;
@@ -533,32 +631,35 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
             p.h[(int64_t)(row0 + r0 + jr) * p.I + n] =
                 __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
           } else {
-            float *yrow = p.y_acc + (int64_t)(a_c[c] / p.top_k) * p.H + 16 * j;
+            float *yrow = p.y_acc + (int64_t)(a_c[c] / p.top_k) * p.H + Cfg::kRows * j + row_lo;
             atomicAdd(yrow + gq, w_c[c] * acc[c]);
             atomicAdd(yrow + gq + 8, w_c[c] * acc[2 + c]);
           }
         }
         if (MODE == 1 && p.cnt) {
-          // the warp barrier orders every lane's reductions before lane 0's fenced count
-          __syncwarp();
-          int last = 0;
-          if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(p.cnt + j, Rp) + Rp == p.A;
-          }
-          if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
-            for (int i = lane; i < p.T * 16; i += 32) {
-              const int64_t o = (int64_t)(i >> 4) * p.H + 16 * j + (i & 15);
-              p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(p.y_acc + o)));
-            }
-          }
+          pend_blk = (Cfg::kRows * j + row_lo) / 16;  // this warp's 16 columns
+          pend_rows = Rp;
         }
       }
       if (!whole) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&xempty[xb]);
       }
+    }
+  }
+  if (MODE == 1 && p.cnt && ok) {  // drain the count pipeline
+    if (flt_blk >= 0) {
+      const int old = __shfl_sync(0xffffffffu, flt_old, 0);
+      if (old + flt_rows == p.A) cast_block(p, flt_blk, lane);
+    }
+    if (pend_blk >= 0) {
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
+      }
+      const int old = __shfl_sync(0xffffffffu, flt_old, 0);
+      if (old + pend_rows == p.A) cast_block(p, pend_blk, lane);
     }
   }
   if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
@@ -602,13 +703,12 @@ static int pick_ktok(const moe_tiles_t &t) {
   return 8;
 }
 
-// Ring buffers: as many as fit beside the activation region, at most one per team.
+// Ring buffers: as many as fit beside the activation region, at most two per team.
 template <int MODE>
 static int pick_nbuf(int K, int nxrows, int ntok) {
   using Cfg = GemvCfg<MODE>;
-  const int cap = Cfg::kMaxCompute / Cfg::kTeam;
-  for (int nb = cap; nb >= 2; --nb)
-    if (PLayout(K, nxrows, ntok, nb).total <= kSmemLimit) return nb;
+  for (int nb = 16; nb >= 2; --nb)
+    if (PLayout(K, Cfg::kRows, nxrows, ntok, nb).total <= kSmemLimit) return nb;
   return 0;
 }
 
@@ -628,12 +728,12 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   using Cfg = GemvCfg<MODE>;
   const int K = MODE == 0 ? H : I;
   const int T = t.num_tokens, A = t.num_assignments;
-  const int cap = Cfg::kMaxCompute / Cfg::kTeam;
-  // whole mode when every activation row fits beside a ring of at least 6 buffers
-  const int nx_all = MODE == 0 ? T : A, ntok_all = MODE == 0 ? A : 0;
-  const int nb_whole = nx_all <= kWholeMaxRows ? pick_nbuf<MODE>(K, nx_all, ntok_all) : 0;
+  // whole mode (gate/up) when every token row fits beside a ring of at least 6 buffers
+  const int nx_all = T, ntok_all = A;
+  const int nb_whole =
+      (MODE == 0 && nx_all <= kWholeMaxRows) ? pick_nbuf<MODE>(K, nx_all, ntok_all) : 0;
   int whole, ktok, nxrows, nbuf;
-  if (nb_whole >= (cap < 6 ? cap : 6)) {
+  if (nb_whole >= 6) {
     whole = 1;
     ktok = 8;
     nxrows = nx_all;
@@ -649,9 +749,21 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
     set_error("%s: shared-memory ring does not fit (K=%d)", what, K);
     return MOE_ERR_UNSUPPORTED;
   }
-  const PLayout L(K, nxrows, whole ? ntok_all : 0, nbuf);
+  // teams: half the buffers (each team double-buffered), at least one
+  int nteams = nbuf / 2 > 0 ? nbuf / 2 : 1;
+  if (nteams > Cfg::kMaxCompute / Cfg::kTeam) nteams = Cfg::kMaxCompute / Cfg::kTeam;
+  if (nteams > kMaxTeams) nteams = kMaxTeams;
+  const int nwc = nteams * Cfg::kTeam;
+  // split K: exactly two buffers per team (the combine's barrier parity relies on it)
+  if (Cfg::kSplitK) nbuf = 2 * nteams;
+  const PLayout L(K, Cfg::kRows, nxrows, whole ? ntok_all : 0, nbuf);
   CUtensorMap tmap;
   const int64_t rows = (int64_t)t.num_experts * (MODE == 0 ? 2 * I : H);
+  if ((MODE == 0 ? I % 8 : H % Cfg::kRows) != 0) {
+    set_error("%s: %s must be a multiple of %d", what, MODE == 0 ? "inter" : "hidden",
+              MODE == 0 ? 8 : Cfg::kRows);
+    return MOE_ERR_UNSUPPORTED;
+  }
   if (!make_map_2d(&tmap, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, Wq, (uint64_t)K / 16,
                    (uint64_t)rows, (uint32_t)(L.S / 8), (uint32_t)Cfg::kBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_NONE)) {
@@ -661,11 +773,9 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   if (cudaFuncSetAttribute((const void *)gemv_persist_kernel<MODE>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
     return check_launch(what);
-  const int64_t max_chunks = (int64_t)t.max_tiles * (MODE == 0 ? I / 8 : H / 16);
+  const int64_t max_chunks = (int64_t)t.max_tiles * (MODE == 0 ? I / 8 : H / Cfg::kRows);
   int grid = sm_count();
   if (max_chunks < grid) grid = (int)(max_chunks > 0 ? max_chunks : 1);
-  int nwc = nbuf * Cfg::kTeam;
-  if (nwc > Cfg::kMaxCompute) nwc = Cfg::kMaxCompute;
   GemvArgs a;
   a.act = act;
   a.Sc = Sc;
