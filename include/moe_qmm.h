@@ -206,7 +206,10 @@ moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu, const 
  *   Sd, Bd [E, H, I/64] bf16
  *   topk_weights [T, k] fp32 router weights
  *   y_acc_ws [T, H]  fp32   caller-owned workspace of moe_workspace_bytes(T, H)
- *                           bytes; overwritten
+ *                           bytes, all zero on entry: clear it once after
+ *                           allocating.  A call that completes leaves it all
+ *                           zero again (no memset per call); after a call that
+ *                           set the status word, clear it before reusing it.
  *   y   [T, H]       bf16   out: y[t] = sum_j topk_weights[t, j] * (Wd[e] . h[s]),
  *                           s the slot of a = t*k + j, e = sorted_ids[s]
  * The k terms of a token are added with fp32 atomics, so the order of the

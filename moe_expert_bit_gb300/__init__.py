@@ -231,7 +231,8 @@ class MoeLayerBuffers:
     def __init__(self, T, k, E, H, I, tile_m, device="cuda"):
         self.routing = Routing(T, k, E, tile_m, device)
         self.h = torch.empty(T * k, I, dtype=torch.bfloat16, device=device)
-        self.y_acc = torch.empty((moe_workspace_bytes(T, H) + 3) // 4, dtype=torch.float32,
+        # the down call needs a zeroed workspace and leaves it zeroed
+        self.y_acc = torch.zeros((moe_workspace_bytes(T, H) + 3) // 4, dtype=torch.float32,
                                  device=device)
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.H, self.I = H, I

@@ -24,6 +24,33 @@ __device__ __forceinline__ int32_t load_status(const int32_t *status) {
   return *reinterpret_cast<const volatile int32_t *>(status);
 }
 
+// ---- programmatic dependent launch ----
+// A kernel launched with launch_pdl may start while the previous kernel on the stream is
+// still running: it does its prologue (shared memory, barriers), then griddep_wait()
+// before it reads anything an earlier kernel wrote or writes anything an earlier kernel
+// reads; griddep_launch() lets the next kernel start its own prologue.  Without the
+// launch attribute both are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- numerics ----
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);

@@ -324,13 +324,17 @@ struct GemvArgs {
 };
 
 // y[:, 16 blk .. 16 blk + 15] = bf16(y_acc[...]) by one warp, after the count of block blk
-// reached A (every contribution performed; the fence orders the reads after the count)
+// reached A (every contribution performed; the fence orders the reads after the count).
+// The warp then clears those accumulator entries and the counter: the workspace is left
+// zeroed for the next call.
 __device__ void cast_block(const GemvArgs &p, int blk, int lane) {
   __threadfence();
   for (int i = lane; i < p.T * 16; i += 32) {
     const int64_t o = (int64_t)(i >> 4) * p.H + 16 * blk + (i & 15);
     p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(p.y_acc + o)));
+    __stcg(p.y_acc + o, 0.f);
   }
+  if (lane == 0) p.cnt[blk] = 0;
 }
 
 template <int MODE>
@@ -360,6 +364,10 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   uint64_t *xissued = xempty + 2;  // first activation copy issued (it goes out first)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + L.off_misc);
 
+  // prologue (may overlap the previous kernel): nothing in global memory is touched
+  if (warp == nwc && lane == 0) prefetch_tensormap(&tmap_w);
+  griddep_wait();
+  griddep_launch();
   if (load_status(p.status) != 0) return;
   const int n_tiles = *p.tile_count;
   const int total = n_tiles * CPT;
@@ -388,7 +396,6 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
 
   if (warp == nwc) {
     // ------------------------------------------------ producer
-    if (lane == 0) prefetch_tensormap(&tmap_w);
     bool ok = mbar_wait(xissued, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     uint32_t it = 0;
@@ -665,13 +672,15 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
 }
 
-// y = bf16(y_acc), four elements per thread step
-__global__ void cast_bf16_kernel(const float *__restrict__ y_acc, uint16_t *__restrict__ y,
-                                 int64_t n4, const int32_t *__restrict__ status) {
+// y = bf16(y_acc), four elements per thread step; y_acc is cleared behind the reads (the
+// workspace is left zeroed for the next call)
+__global__ void cast_bf16_kernel(float *__restrict__ y_acc, uint16_t *__restrict__ y, int64_t n4,
+                                 const int32_t *__restrict__ status) {
   if (load_status(status) != 0) return;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 v = reinterpret_cast<const float4 *>(y_acc)[i];
+    reinterpret_cast<float4 *>(y_acc)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
     __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
     uint2 o;
@@ -799,7 +808,7 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   // the column-block counters follow the T x H accumulator in the workspace
   a.cnt = (MODE == 1 && fused_cast) ? reinterpret_cast<int32_t *>(y_acc + (int64_t)T * H) : nullptr;
   a.y = y;
-  gemv_persist_kernel<MODE><<<grid, (nwc + 2) * 32, L.total, stream>>>(tmap, a);
+  launch_pdl(gemv_persist_kernel<MODE>, dim3(grid), dim3((nwc + 2) * 32), L.total, stream, tmap, a);
   return check_launch(what);
 }
 
@@ -818,7 +827,7 @@ moe_status launch_down_gemv(const uint16_t *hin, const uint32_t *Wd, const uint1
                            stream, "moe_gather_qmm_down_unsort (gemv)");
 }
 
-moe_status launch_cast_bf16(const float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
+moe_status launch_cast_bf16(float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
                             cudaStream_t stream) {
   const int64_t n4 = n / 4;  // n = T * H with H % 64 == 0
   int blocks = (int)((n4 + 255) / 256);

@@ -11,12 +11,19 @@ moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint1
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
                              uint16_t *h, cudaStream_t stream);
 // fused_cast: the kernel also writes y = bf16(y_acc), each 16-column block as soon as
-// its last contribution lands; y_acc [T, H] is then followed by H/16 zeroed int counters
-// (the workspace layout of moe_workspace_bytes).
+// its last contribution lands, and clears the block; y_acc [T, H] is then followed by
+// H/16 int counters (the workspace layout of moe_workspace_bytes), zero on entry and
+// on exit.
 moe_status launch_down_gemv(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                             int32_t H, int32_t I, float *y_acc, uint16_t *y, bool fused_cast,
                             cudaStream_t stream);
+// moe_gather_qmm_down_unsort behind the C ABI (fn names the entry point in errors);
+// clear_ws: zero the workspace first (after validation)
+moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,
+                       const moe_bf16_t *Sd, const moe_bf16_t *Bd, const moe_tiles_t *tiles,
+                       const float *topk_weights, int32_t H, int32_t I, int32_t variant,
+                       float *y_acc_ws, moe_bf16_t *y, bool clear_ws, cudaStream_t stream);
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m);
 bool gemv_supported(int32_t H, int32_t I);
 moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
@@ -25,7 +32,8 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
 moe_status launch_down_tc(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                           const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                           int32_t H, int32_t I, float *y_acc, cudaStream_t stream);
-moe_status launch_cast_bf16(const float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
+// y = bf16(y_acc[0 .. n)); clears y_acc behind the reads
+moe_status launch_cast_bf16(float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
                             cudaStream_t stream);
 
 }  // namespace moeqmm

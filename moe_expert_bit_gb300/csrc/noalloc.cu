@@ -76,16 +76,9 @@ extern "C" moe_status moe_gather_qmm_down_unsort_noalloc(
   float *scratch = nullptr;
   moe_status st = noalloc_scratch(&scratch);
   if (st != MOE_OK) return st;
-  // The full validation and launch sequence of the workspace entry point,
-  // pointed at the built-in accumulator.
-  st = moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, tiles, topk_weights, H, I, variant, scratch, y,
-                                  stream);
-  if (st != MOE_OK) {
-    // keep the error text pointing at this entry point
-    const char *msg = moe_last_error_string();
-    char copy[512];
-    snprintf(copy, sizeof copy, "%s", msg);
-    set_error("%s: %s", fn, copy);
-  }
-  return st;
+  // The full validation and launch sequence of the workspace entry point, pointed at
+  // the built-in accumulator, which is cleared first (after validation): a call that
+  // stopped on a device error cannot leave it dirty for the next one.
+  return down_unsort(fn, h, Wd, Sd, Bd, tiles, topk_weights, H, I, variant, scratch, y, true,
+                     stream);
 }

@@ -120,14 +120,12 @@ extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *
   return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
 }
 
-extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
-                                                 const moe_bf16_t *Sd, const moe_bf16_t *Bd,
-                                                 const moe_tiles_t *tiles,
-                                                 const float *topk_weights, int32_t H, int32_t I,
-                                                 int32_t variant, float *y_acc_ws, moe_bf16_t *y,
-                                                 cudaStream_t stream) {
-  const char *fn = "moe_gather_qmm_down_unsort";
-  clear_error();
+namespace moeqmm {
+
+moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,
+                       const moe_bf16_t *Sd, const moe_bf16_t *Bd, const moe_tiles_t *tiles,
+                       const float *topk_weights, int32_t H, int32_t I, int32_t variant,
+                       float *y_acc_ws, moe_bf16_t *y, bool clear_ws, cudaStream_t stream) {
   moe_status st = validate_tiles(fn, tiles);
   if (st != MOE_OK) return st;
   if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
@@ -137,21 +135,36 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
   }
   if ((st = validate_aligned(fn, {h, Wd, Sd, Bd, y_acc_ws, y})) != MOE_OK) return st;
   if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
-  // zero the accumulator and the completion counter that follows it
+  // The workspace arrives zeroed and is left zeroed: whoever converts a part of the
+  // accumulator to y also clears it (and its completion counter), so a call needs no
+  // memset in front of its kernels (clear_ws: clear it anyway, after validation).
   const int64_t n = (int64_t)tiles->num_tokens * H;
-  if (cudaMemsetAsync(y_acc_ws, 0, moe_workspace_bytes(tiles->num_tokens, H), stream) !=
-      cudaSuccess) {
+  if (clear_ws &&
+      cudaMemsetAsync(y_acc_ws, 0, moe_workspace_bytes(tiles->num_tokens, H), stream) !=
+          cudaSuccess)
     return check_launch(fn);
-  }
   if (variant == MOE_VARIANT_TC) {
     st = launch_down_tc(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
     if (st != MOE_OK) return st;
     return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
   }
-  // small outputs: the last CTA of the down kernel does the cast (one launch fewer)
+  // small outputs: the down kernel itself casts each column block when it completes
   const bool fuse_cast = n <= (int64_t(1) << 20);
   st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, y, fuse_cast,
                         stream);
   if (st != MOE_OK || fuse_cast) return st;
   return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
+}
+
+}  // namespace moeqmm
+
+extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
+                                                 const moe_bf16_t *Sd, const moe_bf16_t *Bd,
+                                                 const moe_tiles_t *tiles,
+                                                 const float *topk_weights, int32_t H, int32_t I,
+                                                 int32_t variant, float *y_acc_ws, moe_bf16_t *y,
+                                                 cudaStream_t stream) {
+  clear_error();
+  return down_unsort("moe_gather_qmm_down_unsort", h, Wd, Sd, Bd, tiles, topk_weights, H, I,
+                     variant, y_acc_ws, y, false, stream);
 }

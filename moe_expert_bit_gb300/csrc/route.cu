@@ -51,6 +51,7 @@ constexpr int kSortWarps = kSortThreads / 32;
 struct SortSmem {
   int32_t hist[MOE_MAX_EXPERTS];
   int32_t cursor[MOE_MAX_EXPERTS];
+  int32_t off[MOE_MAX_EXPERTS + 1];  // first slot of each expert (+ A)
   int32_t warp[kSortWarps][MOE_MAX_EXPERTS];
   int32_t bad;
 };
@@ -104,10 +105,12 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
       int e = lane * 8 + i;
       if (e < E) {
         s_cursor[e] = run;
+        sm.off[e] = run;
         counts[e] = local[i];
       }
       run += local[i];
     }
+    if (lane == 31) sm.off[E] = run;
   }
   __syncthreads();
 
@@ -149,6 +152,8 @@ __global__ void __launch_bounds__(kSortThreads)
                             int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
                             int32_t *__restrict__ counts, int32_t *__restrict__ status) {
   __shared__ SortSmem sm;
+  griddep_wait();
+  griddep_launch();
   if (load_status(status) != 0) return;
   sort_body(sm, ids, A, E, sorted_ids, perm, counts, status);
 }
@@ -173,11 +178,12 @@ __device__ __forceinline__ int32_t lower_bound_dev(const int32_t *v, int32_t n, 
 }
 
 // Offsets, tile counts, exclusive scan and strided descriptor emission, one CTA.
-// Block of any multiple of 32 threads (>= 32).
+// Block of any multiple of 32 threads (>= 32).  known_off: each expert's first slot when
+// the caller already has it (the fused kernel's sort), else found by binary search.
 __device__ void build_body(TileSmem &sm, const int32_t *__restrict__ sorted_ids, int32_t A,
                            int32_t E, int32_t BM, int32_t *__restrict__ offsets,
                            int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
-                           int32_t *__restrict__ status) {
+                           int32_t *__restrict__ status, const int32_t *known_off = nullptr) {
   int32_t *s_off = sm.off, *s_tstart = sm.tstart;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x;
@@ -197,8 +203,9 @@ __device__ void build_body(TileSmem &sm, const int32_t *__restrict__ sorted_ids,
     }
     return;
   }
-  // per-expert sorted range by binary search
-  for (int e = tid; e <= E; e += nthr) s_off[e] = (e == E) ? A : lower_bound_dev(sorted_ids, A, e);
+  // per-expert sorted range (on a sorted array the binary search and the sort's scan agree)
+  for (int e = tid; e <= E; e += nthr)
+    s_off[e] = known_off ? known_off[e] : (e == E) ? A : lower_bound_dev(sorted_ids, A, e);
   __syncthreads();
   // tiles per expert, exclusive scan by warp 0 (8 experts per lane)
   if (warp == 0) {
@@ -255,6 +262,8 @@ __global__ void __launch_bounds__(kTileThreads)
                               int32_t *__restrict__ tiles, int32_t *__restrict__ tile_count,
                               int32_t *__restrict__ status) {
   __shared__ TileSmem sm;
+  griddep_wait();
+  griddep_launch();
   if (load_status(status) != 0) {
     if (threadIdx.x == 0) *tile_count = 0;
     return;
@@ -272,6 +281,8 @@ __global__ void __launch_bounds__(kSortThreads)
                  int32_t *__restrict__ status) {
   __shared__ SortSmem ssm;
   __shared__ TileSmem tsm;
+  griddep_wait();
+  griddep_launch();
   if (load_status(status) != 0) {
     if (threadIdx.x == 0) *tile_count = 0;
     return;
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(kSortThreads)
     return;
   }
   __syncthreads();
-  build_body(tsm, sorted_ids, A, E, BM, offsets, tiles, tile_count, status);
+  build_body(tsm, sorted_ids, A, E, BM, offsets, tiles, tile_count, status, ssm.off);
 }
 
 }  // namespace moeqmm
@@ -325,8 +336,8 @@ moe_status moe_sort_assignments(const int32_t *topk_ids, int32_t T, int32_t k, i
     set_error("moe_sort_assignments: %lld assignments exceed 2^24", (long long)A);
     return MOE_ERR_UNSUPPORTED;
   }
-  sort_assignments_kernel<<<1, kSortThreads, 0, stream>>>(topk_ids, static_cast<int32_t>(A), E,
-                                                          sorted_ids, perm, counts, status);
+  launch_pdl(sort_assignments_kernel, dim3(1), dim3(kSortThreads), 0, stream, topk_ids,
+             static_cast<int32_t>(A), E, sorted_ids, perm, counts, status);
   return check_launch("moe_sort_assignments");
 }
 
@@ -355,8 +366,8 @@ moe_status moe_build_expert_tiles(const int32_t *sorted_ids, int32_t A, int32_t 
     set_error("moe_build_expert_tiles: max_tiles %d < required %zu", max_tiles, need);
     return MOE_ERR_INVALID_ARG;
   }
-  build_expert_tiles_kernel<<<1, kTileThreads, 0, stream>>>(sorted_ids, A, E, BM, offsets, tiles,
-                                                            tile_count, status);
+  launch_pdl(build_expert_tiles_kernel, dim3(1), dim3(kTileThreads), 0, stream, sorted_ids, A, E,
+             BM, offsets, tiles, tile_count, status);
   return check_launch("moe_build_expert_tiles");
 }
 
@@ -393,9 +404,9 @@ moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t T, int32_t 
     set_error("moe_sort_and_build_tiles: max_tiles %d < required %zu", max_tiles, need);
     return MOE_ERR_INVALID_ARG;
   }
-  route_kernel<<<1, kSortThreads, 0, stream>>>(topk_ids, static_cast<int32_t>(A), E, tile_m,
-                                               sorted_ids, perm, counts, offsets, tiles,
-                                               tile_count, status);
+  launch_pdl(route_kernel, dim3(1), dim3(kSortThreads), 0, stream, topk_ids,
+             static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets, tiles,
+             tile_count, status);
   return check_launch("moe_sort_and_build_tiles");
 }
 
