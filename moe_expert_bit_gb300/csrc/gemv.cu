@@ -257,7 +257,7 @@ struct GemvCfg {
   static constexpr bool kSplitK = MODE == 0;                // else: split rows
   static constexpr int kRows = MODE == 0 ? 16 : 16 * kTeam;  // weight rows per chunk
   static constexpr int kBoxRows = MODE == 0 ? 8 : kRows;     // weight rows per TMA box
-  static constexpr int kMaxCompute = 16;                     // compute warps per CTA
+  static constexpr int kMaxCompute = MODE == 0 ? 16 : 24;    // compute warps per CTA
   static constexpr int kThreads = (kMaxCompute + 2) * 32;
 };
 
@@ -368,8 +368,9 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   if (warp == nwc && lane == 0) prefetch_tensormap(&tmap_w);
   griddep_wait();
   griddep_launch();
-  if (load_status(p.status) != 0) return;
+  const int32_t st = load_status(p.status);  // both loads in flight together
   const int n_tiles = *p.tile_count;
+  if (st != 0) return;
   const int total = n_tiles * CPT;
   const int c0 = (int)((int64_t)total * blockIdx.x / gridDim.x);
   const int c1 = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
@@ -398,15 +399,15 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
     // ------------------------------------------------ producer
     bool ok = mbar_wait(xissued, 0, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
-    uint32_t it = 0;
+    uint32_t it = 0, ph = 0;
+    int b = 0;  // it % nbuf, ph = (it / nbuf) & 1
     const uint32_t tx = (uint32_t)L.w_bytes + 4u * Cfg::kRows * G;
     for (int tile = c0 / CPT; ok && tile * CPT < c1; ++tile) {
       const int e = p.tiles[3 * tile], R = p.tiles[3 * tile + 2];
       const int j0 = max(c0 - tile * CPT, 0), j1 = min(c1 - tile * CPT, CPT);
       for (int r0 = 0; ok && r0 < R; r0 += ktok) {
-        for (int j = j0; j < j1; ++j, ++it) {
-          const int b = it % nbuf;
-          ok = mbar_wait(&empty[b], ((it / nbuf) & 1) ^ 1, abort_flag);
+        for (int j = j0; j < j1; ++j) {
+          ok = mbar_wait(&empty[b], ph ^ 1, abort_flag);
           if (!(ok = __all_sync(0xffffffffu, ok))) break;
           uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
           uint16_t *sc = reinterpret_cast<uint16_t *>(buf + L.w_bytes);
@@ -436,6 +437,11 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
               bulk_load(sc + (q - 1) * Cfg::kRows * G, (q == 2 ? p.Bi : p.Sc) + r * G,
                         2u * Cfg::kRows * G, &full[b]);
             }
+          }
+          ++it;
+          if (++b == nbuf) {
+            b = 0;
+            ph ^= 1u;
           }
         }
       }
@@ -570,10 +576,22 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
             w_c[c] = p.topk_weights[a_c[c]];
           }
       }
-      for (int j = j0; j < j1; ++j, ++it) {
-        if ((int)(it % nteams) != team) continue;
-        const int b = it % nbuf;
-        if (ok) ok = mbar_wait(&full[b], (it / nbuf) & 1, abort_flag);
+      // the team's chunks of this pass: global chunk numbers it + jj with jj = the first
+      // one that is the team's, then every nteams-th; buffer and phase advance by nteams
+      const int len = j1 - j0;
+      const int jfirst = (team - (int)(it % (uint32_t)nteams) + nteams) % nteams;
+      int bn = (int)((it + jfirst) % (uint32_t)nbuf);
+      uint32_t phn = ((it + jfirst) / (uint32_t)nbuf) & 1u;
+      it += len;
+      for (int jj = jfirst; jj < len; jj += nteams) {
+        const int j = j0 + jj, b = bn;
+        const uint32_t ph = phn;
+        bn += nteams;
+        if (bn >= nbuf) {
+          bn -= nbuf;
+          phn ^= 1u;
+        }
+        if (ok) ok = mbar_wait(&full[b], ph, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
         const uint16_t *sc = reinterpret_cast<const uint16_t *>(buf + L.w_bytes);
@@ -758,8 +776,10 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
     set_error("%s: shared-memory ring does not fit (K=%d)", what, K);
     return MOE_ERR_UNSUPPORTED;
   }
-  // teams: half the buffers (each team double-buffered), at least one
-  int nteams = nbuf / 2 > 0 ? nbuf / 2 : 1;
+  // teams: split K, half the buffers (each team double-buffered); split rows, all but one
+  // buffer (the ring then holds nearly a whole range of a decode call at once)
+  int nteams = Cfg::kSplitK ? nbuf / 2 : nbuf - 1;
+  if (nteams < 1) nteams = 1;
   if (nteams > Cfg::kMaxCompute / Cfg::kTeam) nteams = Cfg::kMaxCompute / Cfg::kTeam;
   if (nteams > kMaxTeams) nteams = kMaxTeams;
   const int nwc = nteams * Cfg::kTeam;

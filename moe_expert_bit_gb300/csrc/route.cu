@@ -37,26 +37,36 @@ moe_status check_launch(const char *what) {
   return MOE_OK;
 }
 
-constexpr int kSortThreads = 1024;
+constexpr int kSortThreads = 1024;  // the most threads of a sort block
 constexpr int kSortWarps = kSortThreads / 32;
+constexpr int kSmemSorted = 2048;   // up to this many sorted ids are also kept on-chip
+
+// Threads of a sort block: one per assignment (rounded to whole warps), at most 1024;
+// small calls (decode) then pay for no idle warps at the block barriers.
+static int sort_threads(int64_t A) {
+  const int64_t t = (A + 31) / 32 * 32;
+  return t < 64 ? 64 : t > kSortThreads ? kSortThreads : (int)t;
+}
 
 // Stable counting sort, one CTA.
 //  pass 1: histogram of expert ids in shared memory (+ range check);
 //  scan:   exclusive prefix over experts -> first slot of each expert;
-//  pass 2: rounds of 1024 consecutive assignments.  Inside a warp,
+//  pass 2: rounds of blockDim consecutive assignments.  Inside a warp,
 //          __match_any_sync groups equal experts and a popcount of the lower
 //          lanes gives each element's rank; per-warp counts are scanned across
-//          the 32 warps per expert and added to a running cursor, so slots
+//          the block's warps per expert and added to a running cursor, so slots
 //          follow ascending a within every expert.
 struct SortSmem {
   int32_t hist[MOE_MAX_EXPERTS];
   int32_t cursor[MOE_MAX_EXPERTS];
   int32_t off[MOE_MAX_EXPERTS + 1];  // first slot of each expert (+ A)
   int32_t warp[kSortWarps][MOE_MAX_EXPERTS];
+  int32_t sorted[kSmemSorted];  // copy of sorted_ids when A <= kSmemSorted
   int32_t bad;
 };
 
-// Returns false (status raised) if an id is out of range.  Block of kSortThreads threads.
+// Returns false (status raised) if an id is out of range.  Block of 64 .. kSortThreads
+// threads, a multiple of 32.
 __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t A, int32_t E,
                           int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
                           int32_t *__restrict__ counts, int32_t *__restrict__ status) {
@@ -64,13 +74,14 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
   int32_t(*s_warp)[MOE_MAX_EXPERTS] = sm.warp;
   int32_t &s_bad = sm.bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthr = blockDim.x, nw = nthr >> 5;
 
-  for (int e = tid; e < E; e += kSortThreads) s_hist[e] = 0;
-  for (int i = tid; i < kSortWarps * MOE_MAX_EXPERTS; i += kSortThreads) (&s_warp[0][0])[i] = 0;
+  for (int e = tid; e < E; e += nthr) s_hist[e] = 0;
+  for (int i = tid; i < nw * MOE_MAX_EXPERTS; i += nthr) (&s_warp[0][0])[i] = 0;
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
-  for (int a = tid; a < A; a += kSortThreads) {
+  for (int a = tid; a < A; a += nthr) {
     int32_t e = ids[a];
     if (e < 0 || e >= E)
       s_bad = 1;
@@ -115,7 +126,7 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
   __syncthreads();
 
   const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < A; base += kSortThreads) {
+  for (int base = 0; base < A; base += nthr) {
     const int a = base + tid;
     const bool valid = a < A;
     const int32_t e = valid ? ids[a] : -1;
@@ -123,10 +134,9 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
     const int32_t rank = __popc(same & lt_mask);
     if (valid && rank == 0) s_warp[warp][e] = __popc(same);
     __syncthreads();
-    for (int ex = tid; ex < E; ex += kSortThreads) {  // per-expert scan over the warps
+    for (int ex = tid; ex < E; ex += nthr) {  // per-expert scan over the warps
       int32_t run = s_cursor[ex];
-#pragma unroll 8
-      for (int w = 0; w < kSortWarps; ++w) {
+      for (int w = 0; w < nw; ++w) {
         int32_t c = s_warp[w][ex];
         s_warp[w][ex] = run;
         run += c;
@@ -138,11 +148,14 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
       const int32_t slot = s_warp[warp][e] + rank;
       sorted_ids[slot] = e;
       perm[slot] = a;
+      if (A <= kSmemSorted) sm.sorted[slot] = e;
     }
     __syncthreads();
-    for (int ex = tid; ex < E; ex += kSortThreads)
-      for (int w = 0; w < kSortWarps; ++w) s_warp[w][ex] = 0;
-    __syncthreads();
+    if (base + nthr < A) {
+      for (int ex = tid; ex < E; ex += nthr)
+        for (int w = 0; w < nw; ++w) s_warp[w][ex] = 0;
+      __syncthreads();
+    }
   }
   return true;
 }
@@ -292,7 +305,9 @@ __global__ void __launch_bounds__(kSortThreads)
     return;
   }
   __syncthreads();
-  build_body(tsm, sorted_ids, A, E, BM, offsets, tiles, tile_count, status, ssm.off);
+  // the builder checks the sort's output: its on-chip copy when there is one
+  build_body(tsm, A <= kSmemSorted ? ssm.sorted : sorted_ids, A, E, BM, offsets, tiles,
+             tile_count, status, ssm.off);
 }
 
 }  // namespace moeqmm
@@ -336,7 +351,7 @@ moe_status moe_sort_assignments(const int32_t *topk_ids, int32_t T, int32_t k, i
     set_error("moe_sort_assignments: %lld assignments exceed 2^24", (long long)A);
     return MOE_ERR_UNSUPPORTED;
   }
-  launch_pdl(sort_assignments_kernel, dim3(1), dim3(kSortThreads), 0, stream, topk_ids,
+  launch_pdl(sort_assignments_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, topk_ids,
              static_cast<int32_t>(A), E, sorted_ids, perm, counts, status);
   return check_launch("moe_sort_assignments");
 }
@@ -404,7 +419,7 @@ moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t T, int32_t 
     set_error("moe_sort_and_build_tiles: max_tiles %d < required %zu", max_tiles, need);
     return MOE_ERR_INVALID_ARG;
   }
-  launch_pdl(route_kernel, dim3(1), dim3(kSortThreads), 0, stream, topk_ids,
+  launch_pdl(route_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, topk_ids,
              static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets, tiles,
              tile_count, status);
   return check_launch("moe_sort_and_build_tiles");
