@@ -235,7 +235,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode", choices=synth.CONFIG_ORDER)
-    ap.add_argument("--variant", default="auto", choices=["auto", "gemv", "tc"])
+    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "gemv", "tc"],
+                    help="auto: the four calls with the library's own variant choice; "
+                         "fused: the one-launch layer (decode-sized calls)")
     ap.add_argument("--tile-m", type=int, default=128)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -256,7 +258,8 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    variant = {"auto": mq.VARIANT_AUTO, "gemv": mq.VARIANT_GEMV, "tc": mq.VARIANT_TC}[args.variant]
+    variant = {"auto": mq.VARIANT_AUTO, "fused": mq.VARIANT_AUTO, "gemv": mq.VARIANT_GEMV,
+               "tc": mq.VARIANT_TC}[args.variant]
 
     cfg = synth.CONFIGS[args.config]
     d = synth.make(args.config)
@@ -282,7 +285,19 @@ def main():
     r = buf.routing
     r.status.zero_()
 
+    # the one-launch layer when asked for (it measures no faster than the four calls yet)
+    use_fused = args.variant == "fused" and mq.fused_layer_fits(T, k, E, H, I, args.tile_m)
+    if args.variant == "fused" and not use_fused:
+        raise SystemExit("the fused layer does not take this workload")
+    path = "moe_layer_fused" if use_fused else f"four calls, variant {args.variant}"
+
     def step(ev=None):
+        if use_fused:
+            mq.moe_layer_fused(x, ids, tw, W, E, buf, stream)
+            if ev is not None:
+                for e in ev:
+                    e.record(stream)
+            return
         # the four library calls; events (if given) bracket the gate/up launch
         mq.moe_sort_and_build_tiles(ids, E, args.tile_m, r.sorted_ids, r.perm, r.counts,
                                     r.offsets, r.tiles, r.tile_count, r.status, stream)
@@ -373,11 +388,15 @@ def main():
     t_roof_ms = max(w_bytes / (hbm * 1e9), flops / (tf_burst * 1e12)) * 1e3
     geglu_avg = sum(geglu_ms) / len(geglu_ms)
     geglu_bytes = touched * gu_b + T * H * 2 + A * I * 2
+    if use_fused:
+        # the one kernel: every weight byte, x, h written and read back, y
+        geglu_avg = sum(route_ms) / len(route_ms)
+        geglu_bytes = w_bytes + T * H * 2 + 2 * A * I * 2 + T * H * 2
     achieved = geglu_bytes / (geglu_avg * 1e-3) / 1e9
     # route (1) + gate/up (1) + down (1) + cast (1 unless fused into the down kernel)
     fused_cast = variant != mq.VARIANT_TC and T * H <= (1 << 20) and not (
         variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
-    launches_per_step = 3 if fused_cast else 4
+    launches_per_step = 1 if use_fused else 3 if fused_cast else 4
     line = {
         "metric": "MoE layer assignments/s", "value": world * A / (ms * 1e-3),
         "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -385,6 +404,7 @@ def main():
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name(args.config, cfg), "assignments": A,
                    "experts_touched": touched, "tile_m": args.tile_m, "variant": args.variant,
+                   "path": path,
                    "l2": "flushed between steps outside the timed events: 512 MB write, "
                          "then 256 MB read (the flush's dirty lines written back)",
                    "parallelism": f"{world} independent replica(s), no collective"},
@@ -394,14 +414,18 @@ def main():
                            "weight_bytes": w_bytes, "flops": flops,
                            "bound": "hbm" if w_bytes / (hbm * 1e9) >= flops / (tf_burst * 1e12)
                            else "tensor", "peaks": peak_src},
-        "kernels_us": {"route (sort + tiles, one launch)": 1e3 * statistics.median(route_ms),
+        "kernels_us": {"moe_layer_fused (every step, one launch)": 1e3 * statistics.median(route_ms)}
+        if use_fused else
+        {"route (sort + tiles, one launch)": 1e3 * statistics.median(route_ms),
                        "gather_qmm_geglu": 1e3 * statistics.median(geglu_ms),
                        "gather_qmm_down_unsort (+cast)": 1e3 * statistics.median(down_ms),
                        "note": "separate pass with events between the calls (serialised)"},
-        "roofline": {"kernel": "gather_qmm_geglu", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "fused_layer_kernel" if use_fused else "gather_qmm_geglu",
+                     "bound": "hbm", "achieved": achieved,
                      "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "peak_source": f"{peak_src} (copy bandwidth)",
-                     "traffic": kernel_traffic("gather_qmm_geglu_" + args.config),
+                     "traffic": kernel_traffic(("layer_fused_" if use_fused else
+                                                "gather_qmm_geglu_") + args.config),
                      "algorithmic_bytes": geglu_bytes},
         "e2e": {"value": world * A / (e2e_total_ms / args.steps * 1e-3), "unit": "assignments/s",
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + ids_h.numel() * 4 + tw_h.numel() * 4),

@@ -207,9 +207,12 @@ moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu, const 
  *   topk_weights [T, k] fp32 router weights
  *   y_acc_ws [T, H]  fp32   caller-owned workspace of moe_workspace_bytes(T, H)
  *                           bytes, all zero on entry: clear it once after
- *                           allocating.  A call that completes leaves it all
- *                           zero again (no memset per call); after a call that
- *                           set the status word, clear it before reusing it.
+ *                           allocating.  A call that completes leaves its
+ *                           accumulator and counters zero again (no memset per
+ *                           call; moe_layer_fused also keeps a grid-barrier
+ *                           generation word after them, any value of which is
+ *                           valid); after a call that set the status word, clear
+ *                           it before reusing it.
  *   y   [T, H]       bf16   out: y[t] = sum_j topk_weights[t, j] * (Wd[e] . h[s]),
  *                           s the slot of a = t*k + j, e = sorted_ids[s]
  * The k terms of a token are added with fp32 atomics, so the order of the
@@ -249,6 +252,44 @@ moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_
                                               const moe_tiles_t *tiles, const float *topk_weights,
                                               int32_t hidden, int32_t inter, int32_t variant,
                                               moe_bf16_t *y, cudaStream_t stream);
+
+/*
+ * The whole layer of a decode-sized call in ONE launch (steps a1-a8 with the GEMV-style
+ * variant of step a9; the pages' hot path end to end: sorted gathered 4-bit QMM with the
+ * parallel descriptor builder and its self-check, Layr-Labs/mlx PR #4, "What" and the final
+ * review wave; the fused GeGLU product, SharpAI/SwiftLM issue #236, "Still missing"; the
+ * direct weighted un-sort, PR #4, "Measured standing").  Same results as the four calls
+ * (moe_sort_and_build_tiles, then moe_gather_qmm_geglu and moe_gather_qmm_down_unsort with
+ * MOE_VARIANT_GEMV): the routing state bit for bit, h and y as the GEMV variant computes them.
+ *   topk_ids [T, k] int32, topk_weights [T, k] fp32, x [T, H] bf16, the packed weights,
+ *   scales and biases as for the two projections;
+ *   routing state out, as moe_sort_and_build_tiles writes it (sorted_ids [A], perm [A],
+ *   counts [E], offsets [E+1], tiles [max_tiles*3], tile_count [1]), tile_m and max_tiles
+ *   as there; status: the device status word;
+ *   h [A, I] bf16 out (sorted-slot order); y_acc_ws: a workspace of
+ *   moe_workspace_bytes(T, H) bytes, zero on entry and left zero; y [T, H] bf16 out.
+ * Limits: A = T*k <= 256, T <= 64, H and I multiples of 64 whose padded packed rows fit one
+ * copy (K/2 + padding <= 2048 bytes); other calls return MOE_ERR_UNSUPPORTED before any
+ * launch (use the four calls).  The launch is cooperative (one CTA per SM, all resident at
+ * once): it starts when every SM can take its CTA.  Every wait, the grid barrier included,
+ * is bounded (MOE_ERR_TIMEOUT).
+ */
+moe_status moe_layer_fused(const int32_t *topk_ids, const float *topk_weights, int32_t num_tokens,
+                           int32_t top_k, int32_t num_experts, const moe_bf16_t *x,
+                           const uint32_t *Wgu, const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
+                           const uint32_t *Wd, const moe_bf16_t *Sd, const moe_bf16_t *Bd,
+                           int32_t hidden, int32_t inter, int32_t tile_m, int32_t max_tiles,
+                           int32_t *sorted_ids, int32_t *perm, int32_t *counts, int32_t *offsets,
+                           int32_t *tiles, int32_t *tile_count, int32_t *status, moe_bf16_t *h,
+                           float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream);
+
+/*
+ * MOE_OK if moe_layer_fused takes a call of this shape (T tokens, top-k, E experts, hidden,
+ * inter, tile_m), else MOE_ERR_UNSUPPORTED (or MOE_ERR_INVALID_ARG for sizes no call takes).
+ * Host-side only: no device work.
+ */
+moe_status moe_layer_fused_supported(int32_t num_tokens, int32_t top_k, int32_t num_experts,
+                                     int32_t hidden, int32_t inter, int32_t tile_m);
 
 /* Why the last call on this host thread did not return MOE_OK ("" if it did). */
 const char *moe_last_error_string(void);

@@ -35,7 +35,7 @@ MAX_EXPERTS = 256
 ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
                "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc",
-               "moe_sort_and_build_tiles")
+               "moe_sort_and_build_tiles", "moe_layer_fused", "moe_layer_fused_supported")
 NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
@@ -86,8 +86,12 @@ def load(build_if_needed: bool = True):
                                                    i32, i32, p, p, p]
         lib.moe_gather_qmm_down_unsort_noalloc.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles),
                                                            p, i32, i32, i32, p, p]
+        lib.moe_layer_fused.argtypes = [p, p, i32, i32, i32, p, p, p, p, p, p, p, i32, i32, i32,
+                                        i32, p, p, p, p, p, p, p, p, p, p, p]
+        lib.moe_layer_fused_supported.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.moe_layer_fused_supported.restype = ctypes.c_int
         for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_sort_and_build_tiles",
-                   "moe_gather_qmm_geglu",
+                   "moe_gather_qmm_geglu", "moe_layer_fused",
                    "moe_gather_qmm_down_unsort", "moe_gather_qmm_down_unsort_noalloc"):
             getattr(lib, fn).restype = ctypes.c_int
         lib.moe_last_error_string.argtypes = []
@@ -238,16 +242,49 @@ class MoeLayerBuffers:
         self.H, self.I = H, I
 
 
+def fused_layer_fits(num_tokens, top_k, num_experts, hidden, inter, tile_m=128) -> bool:
+    """Whether moe_layer_fused takes a call of this shape (the library's own host check)."""
+    return load().moe_layer_fused_supported(num_tokens, top_k, num_experts, hidden, inter,
+                                            tile_m) == MOE_OK
+
+
+def moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, buffers, stream=None):
+    """The whole layer of a decode-sized call in one launch (writes the same buffers as the
+    four calls).  Raises MoeError(MOE_ERR_UNSUPPORTED) for calls beyond its limits."""
+    T, k = topk_ids.shape
+    H = x.shape[1]
+    I = weights["Wd"].shape[2] * 8
+    A = T * k
+    r, E = buffers.routing, num_experts
+    _check(load().moe_layer_fused(
+        _ptr(topk_ids, torch.int32, "topk_ids", A), _ptr(topk_weights, torch.float32,
+                                                         "topk_weights", A),
+        T, k, E, _bf16(x, "x"), _ptr(weights["Wgu"], torch.int32, "Wgu"),
+        _bf16(weights["Sgu"], "Sgu"), _bf16(weights["Bgu"], "Bgu"),
+        _ptr(weights["Wd"], torch.int32, "Wd"), _bf16(weights["Sd"], "Sd"),
+        _bf16(weights["Bd"], "Bd"), H, I, r.tile_m, r.max_tiles,
+        _ptr(r.sorted_ids, torch.int32, "sorted_ids", A), _ptr(r.perm, torch.int32, "perm", A),
+        _ptr(r.counts, torch.int32, "counts", E), _ptr(r.offsets, torch.int32, "offsets", E + 1),
+        _ptr(r.tiles, torch.int32, "tiles", 3 * r.max_tiles),
+        _ptr(r.tile_count, torch.int32, "tile_count", 1), _ptr(r.status, torch.int32, "status", 1),
+        _bf16(buffers.h, "h"), _ptr(buffers.y_acc, torch.float32, "y_acc_ws"),
+        _bf16(buffers.y, "y"), _stream(stream)))
+
+
 def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, variant=VARIANT_AUTO,
-              buffers=None, stream=None, fused_route=False):
-    """Run the four calls on one stream.  ``weights``: dict of Wgu, Sgu, Bgu, Wd, Sd, Bd
-    device tensors (uint32 data as int32, bf16 scales/biases).  Returns the buffers."""
+              buffers=None, stream=None, fused_route=False, fused=False):
+    """Run the four calls on one stream (fused: the one-launch layer).  ``weights``: dict of
+    Wgu, Sgu, Bgu, Wd, Sd, Bd device tensors (uint32 data as int32, bf16 scales/biases).
+    Returns the buffers."""
     T, k = topk_ids.shape
     H = x.shape[1]
     I = weights["Wd"].shape[2] * 8
     b = buffers or MoeLayerBuffers(T, k, num_experts, H, I, tile_m, device=x.device)
     r = b.routing
     r.status.zero_()
+    if fused:
+        moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, b, stream)
+        return b
     if fused_route:
         moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, r.sorted_ids, r.perm, r.counts,
                                  r.offsets, r.tiles, r.tile_count, r.status, stream)

@@ -1,0 +1,732 @@
+// The whole expert layer of a decode-sized call in one launch: routing (steps a1, a2),
+// gate/up + GeGLU (a3-a6) and down + weighted un-sort (a7, a8), the GEMV-style variant (a9).
+//
+// Per-call kernels pay, at each of their boundaries, for the grid to drain, the next one to
+// start, and a start-up chain of dependent loads (status, tile count, tiles, first copy).
+// At decode sizes that costs as much as the weight stream itself.  Here one persistent CTA
+// per SM does everything:
+//   1. every CTA sorts the (few) assignments itself in shared memory and builds the tile
+//      descriptors, so the weight stream starts as soon as the ids are read (CTA 0 also
+//      writes the routing state out for the caller);
+//   2. gate/up + GeGLU exactly as the per-call GEMV (split-K teams, h to global memory);
+//   3. a grid barrier (the launch is cooperative, so every CTA is resident): h is complete;
+//   4. down + un-sort, reading h from L2, with the per-column-block cast.
+// The producer warp is not held by the barrier: the ring is one stream of gate/up chunks
+// followed by down chunks, so the down weights flow into the buffers the last gate/up
+// chunks release while the grid waits for its slowest CTA.
+#include "common.cuh"
+#include "gemv_core.cuh"
+#include "kernels.h"
+#include "tmap.h"
+#include "umma.cuh"
+
+namespace moeqmm {
+
+constexpr int kFTeam = 4;                        // warps per team (both phases)
+constexpr int kFTeams = 4;                       // teams
+constexpr int kFCompute = kFTeam * kFTeams;      // compute warps
+constexpr int kFThreads = (kFCompute + 2) * 32;  // + producer, stager
+constexpr int kFDownRows = 16 * kFTeam;          // down chunk: 16 rows per warp
+constexpr int kFPassG = 8;                       // gate/up columns per pass (all rows staged)
+constexpr int kFPassD = 4;                       // down rows staged per pass (two buffers)
+constexpr int kFMaxA = 256;                      // assignments the fused kernel takes
+constexpr int kFMaxT = 64;                       // token rows it stages
+// named barriers: 1 compute + stager (grid barrier), 2 + 2p / 3 + 2p team p's combine,
+// 15 the start (compute + stager)
+constexpr int kFBarGrid = 1, kFBarStart = 15;
+
+struct FLayout {
+  int Gh, Gi, Sh, Si, xrbh, xrbi, slot, nbuf, T, A, E, max_tiles;
+  int off_x, off_xs, off_tiles, off_perm, off_tok, off_w, off_bar, off_misc, total;
+  __host__ __device__ FLayout(int H, int I, int T_, int A_, int E_, int max_tiles_, int nbuf_) {
+    Gh = H / 64;
+    Gi = I / 64;
+    Sh = padded_row_bytes(H);
+    Si = padded_row_bytes(I);
+    xrbh = Gh * 128 + 16;
+    xrbi = Gi * 128 + 16;
+    T = T_;
+    A = A_;
+    E = E_;
+    max_tiles = max_tiles_;
+    nbuf = nbuf_;
+    const int gu = 16 * Sh + 64 * Gh;                 // 16 rows + scales and biases
+    const int dn = kFDownRows * Si + 4 * kFDownRows * Gi;
+    int sl = gu > dn ? gu : dn;
+    if (sl < (kFTeam - 1) * 512) sl = (kFTeam - 1) * 512;  // the split-K park area
+    slot = (sl + 127) & ~127;
+    const int xg = T * xrbh, xd = 2 * kFPassD * xrbi;
+    const int xsg = T * Gh, xsd = 2 * kFPassD * Gi;
+    off_x = nbuf * slot;
+    off_xs = off_x + (((xg > xd ? xg : xd) + 127) & ~127);
+    off_tiles = off_xs + (((xsg > xsd ? xsg : xsd) * 4 + 15) & ~15);
+    off_perm = off_tiles + ((max_tiles * 12 + 15) & ~15);
+    off_tok = off_perm + ((A * 4 + 15) & ~15);
+    off_w = off_tok + ((A * 4 + 15) & ~15);
+    off_bar = off_w + ((A * 4 + 15) & ~15);
+    off_misc = off_bar + (2 * nbuf + 6) * 8;
+    total = off_misc + 32;
+  }
+  // transient routing scratch, inside the last ring slot (no copy lands there before the
+  // routing is done): ids, weights by flat index, sorted ids, histogram, offsets, tile starts
+  __host__ __device__ int scratch_bytes() const { return (3 * A + 3 * (E + 1)) * 4; }
+};
+
+struct FArgs {
+  const int32_t *topk_ids;
+  const float *topk_weights;
+  const uint16_t *x, *Sgu, *Bgu, *Sd, *Bd;
+  int32_t T, k, A, E, H, I, BM, max_tiles, nbuf;
+  int32_t *sorted_ids, *perm, *counts, *offsets, *tiles, *tile_count, *status;
+  uint16_t *h;
+  float *y_acc;
+  int32_t *cnt;   // H/16 column-block counters, after y_acc
+  int32_t *gbar;  // grid barrier: arrivals, generation
+  uint16_t *y;
+};
+
+// The grid barrier (thread 0 of each CTA; the launch is cooperative), sense-reversing:
+// gbar[0] counts arrivals, gbar[1] is a generation word read before arriving.  The last
+// CTA to arrive clears the count (so it is zero again on exit) and advances the
+// generation, which releases the others.  The arrival carries release semantics for this
+// CTA's earlier stores (ordered before it by the block barrier); the acquire load that
+// sees the new generation makes every CTA's stores visible.
+__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool grid_barrier(int32_t *gbar, int32_t gen,
+                                             volatile int *abort_flag) {
+  int32_t old;
+  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(gbar) : "memory");
+  if (old == (int)gridDim.x - 1) {
+    gbar[0] = 0;
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(gbar + 1), "r"(gen + 1) : "memory");
+    return true;
+  }
+  const uint64_t t0 = umma::globaltimer_ns();
+  for (uint32_t i = 1; ld_acquire(gbar + 1) == gen; ++i) {
+    if ((i & 63u) == 0 && (*abort_flag || umma::globaltimer_ns() - t0 > 2000000000ull))
+      return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kFThreads, 1)
+    fused_layer_kernel(const __grid_constant__ CUtensorMap tmap_gu,
+                       const __grid_constant__ CUtensorMap tmap_d, const FArgs p) {
+  using namespace umma;
+  extern __shared__ __align__(1024) uint8_t gsm[];
+  const FLayout L(p.H, p.I, p.T, p.A, p.E, p.max_tiles, p.nbuf);
+  const int nbuf = p.nbuf, Gh = L.Gh, Gi = L.Gi;
+  const int nwc = kFCompute;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  uint8_t *xall = gsm + L.off_x;
+  float *xsall = reinterpret_cast<float *>(gsm + L.off_xs);
+  int32_t *s_tiles = reinterpret_cast<int32_t *>(gsm + L.off_tiles);
+  int32_t *s_perm = reinterpret_cast<int32_t *>(gsm + L.off_perm);
+  int32_t *s_tok = reinterpret_cast<int32_t *>(gsm + L.off_tok);
+  float *s_w = reinterpret_cast<float *>(gsm + L.off_w);
+  uint64_t *full = reinterpret_cast<uint64_t *>(gsm + L.off_bar);
+  uint64_t *empty = full + nbuf;
+  uint64_t *xfull = empty + nbuf;  // the token rows landed (tx)
+  uint64_t *xready = xfull + 2;    // [2] down-phase h rows staged
+  uint64_t *xempty = xready + 2;   // [2] every compute warp done with them
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + L.off_misc);
+  int *s_flags = reinterpret_cast<int *>(gsm + L.off_misc + 4);  // [0] range, [1] order
+  int *s_ntiles = reinterpret_cast<int *>(gsm + L.off_misc + 12);
+  uint32_t *issued = reinterpret_cast<uint32_t *>(gsm + L.off_misc + 16);  // chunks issued
+  int32_t *s_gen = reinterpret_cast<int32_t *>(gsm + L.off_misc + 20);     // barrier generation
+  int32_t *sc_ids = reinterpret_cast<int32_t *>(gsm + (size_t)(nbuf - 1) * L.slot);
+  float *sc_wa = reinterpret_cast<float *>(sc_ids + p.A);
+  int32_t *sc_sorted = sc_ids + 2 * p.A;
+  int32_t *sc_hist = sc_ids + 3 * p.A;
+  int32_t *sc_off = sc_hist + (p.E + 1);
+  int32_t *sc_tstart = sc_off + (p.E + 1);
+
+  if (load_status(p.status) != 0) return;
+  if (smem_addr(gsm) & 127) {
+    if (tid == 0) raise_status(p.status, MOE_ERR_CUDA);
+    return;
+  }
+  const uint32_t xbytes_g = (uint32_t)p.H * 2;
+  if (tid == 0) {
+    for (int i = 0; i < nbuf; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kFTeam);  // every warp of the team that used the buffer
+    }
+    mbar_init(&xfull[0], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&xready[i], 1);
+      mbar_init(&xempty[i], nwc);
+    }
+    *abort_flag = 0;
+    *issued = 0;
+    // the grid barrier's generation, read before any CTA can arrive (arrivals follow the
+    // gate/up phase of every CTA)
+    *s_gen = *reinterpret_cast<volatile int32_t *>(p.gbar + 1);
+    s_flags[0] = s_flags[1] = 0;
+    fence_mbar_init();
+    // the token rows go out first: they depend on nothing
+    mbar_arrive_expect_tx(&xfull[0], (uint32_t)p.T * xbytes_g);
+  }
+  __syncthreads();
+  if (warp == nwc + 1)
+    for (int r = lane; r < p.T; r += 32)
+      bulk_load(xall + (size_t)r * L.xrbh, p.x + (int64_t)r * p.H, xbytes_g, &xfull[0]);
+  if (warp == nwc && lane == 0) {
+    prefetch_tensormap(&tmap_gu);
+    prefetch_tensormap(&tmap_d);
+  }
+
+  // ------------------------------------------------ routing, every CTA (steps a1, a2)
+  // stable counting sort of the flat assignments by expert, ties by ascending index
+  for (int e = tid; e <= p.E; e += nthr) sc_hist[e] = 0;
+  for (int a = tid; a < p.A; a += nthr) {
+    const int32_t e = p.topk_ids[a];
+    sc_ids[a] = e;
+    sc_wa[a] = p.topk_weights[a];
+    if (e < 0 || e >= p.E) s_flags[0] = 1;
+  }
+  __syncthreads();
+  const bool range_bad = s_flags[0] != 0;
+  if (!range_bad)
+    for (int a = tid; a < p.A; a += nthr) atomicAdd(&sc_hist[sc_ids[a]], 1);
+  __syncthreads();
+  if (range_bad) {
+    if (blockIdx.x == 0 && tid == 0) {
+      *p.tile_count = 0;
+      raise_status(p.status, MOE_ERR_RANGE);
+    }
+    if (tid == 0) mbar_wait(&xfull[0], 0, nullptr, 200000000ull);  // the token rows in flight
+    return;
+  }
+  if (warp == 0) {  // exclusive scan over <= 256 experts, 8 per lane
+    int32_t loc[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      loc[i] = e < p.E ? sc_hist[e] : 0;
+      sum += loc[i];
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int32_t run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < p.E) sc_off[e] = run;
+      run += loc[i];
+    }
+    if (lane == 31) sc_off[p.E] = incl;
+  }
+  __syncthreads();
+  // slot of assignment a: its expert's first slot + the earlier assignments of that expert
+  for (int a = tid; a < p.A; a += nthr) {
+    const int32_t e = sc_ids[a];
+    int r = 0;
+    for (int b2 = 0; b2 < a; ++b2) r += sc_ids[b2] == e;
+    const int s = sc_off[e] + r;
+    sc_sorted[s] = e;
+    s_perm[s] = a;
+    s_tok[s] = a / p.k;
+    s_w[s] = sc_wa[a];
+  }
+  __syncthreads();
+  // the builder's self-check on the sorted ids (range was checked above)
+  int order_bad = 0;
+  for (int s = tid; s + 1 < p.A; s += nthr) order_bad |= sc_sorted[s] > sc_sorted[s + 1];
+  order_bad = __syncthreads_or(order_bad);
+  if (order_bad) {
+    if (blockIdx.x == 0 && tid == 0) {
+      *p.tile_count = 0;
+      raise_status(p.status, MOE_ERR_UNSORTED);
+    }
+    if (tid == 0) mbar_wait(&xfull[0], 0, nullptr, 200000000ull);  // the token rows in flight
+    return;
+  }
+  if (warp == 0) {  // tiles per expert and their exclusive scan
+    int32_t loc[8], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      const int c = e < p.E ? sc_off[e + 1] - sc_off[e] : 0;
+      loc[i] = (c + p.BM - 1) / p.BM;
+      sum += loc[i];
+    }
+    int32_t incl = sum;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int32_t run = incl - sum;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane * 8 + i;
+      if (e < p.E) sc_tstart[e] = run;
+      run += loc[i];
+    }
+    if (lane == 31) {
+      sc_tstart[p.E] = incl;
+      *s_ntiles = incl;
+    }
+  }
+  __syncthreads();
+  const int n_tiles = *s_ntiles;
+  for (int i = tid; i < n_tiles; i += nthr) {  // tile i belongs to the last e with start <= i
+    int lo = 0, hi = p.E;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sc_tstart[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int r = i - sc_tstart[lo], c = sc_off[lo + 1] - sc_off[lo];
+    s_tiles[3 * i] = lo;
+    s_tiles[3 * i + 1] = sc_off[lo] + r * p.BM;
+    s_tiles[3 * i + 2] = min(p.BM, c - r * p.BM);
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {  // the routing state for the caller
+    for (int s = tid; s < p.A; s += nthr) {
+      p.sorted_ids[s] = sc_sorted[s];
+      p.perm[s] = s_perm[s];
+    }
+    for (int e = tid; e <= p.E; e += nthr) {
+      p.offsets[e] = sc_off[e];
+      if (e < p.E) p.counts[e] = sc_off[e + 1] - sc_off[e];
+    }
+    for (int i = tid; i < 3 * n_tiles; i += nthr) p.tiles[i] = s_tiles[i];
+    if (tid == 0) *p.tile_count = n_tiles;
+  }
+  __syncthreads();  // the scratch slot is free from here on
+
+  // work ranges of the two phases (contiguous chunk ranges per CTA)
+  const int cpt_g = p.I / 8, cpt_d = p.H / kFDownRows;
+  const int tot_g = n_tiles * cpt_g, tot_d = n_tiles * cpt_d;
+  const int g0 = (int)((int64_t)tot_g * blockIdx.x / gridDim.x);
+  const int g1 = (int)((int64_t)tot_g * (blockIdx.x + 1) / gridDim.x);
+  const int d0 = (int)((int64_t)tot_d * blockIdx.x / gridDim.x);
+  const int d1 = (int)((int64_t)tot_d * (blockIdx.x + 1) / gridDim.x);
+
+  if (warp == nwc) {
+    // ------------------------------------------------ producer: gate/up chunks, then down
+    bool ok = true;
+    uint32_t it = 0, ph = 0;
+    int b = 0;
+    const uint32_t tx_g = 16u * L.Sh + 64u * Gh;
+    const uint32_t tx_d = (uint32_t)kFDownRows * L.Si + 4u * kFDownRows * Gi;
+    for (int phase = 0; phase < 2 && ok; ++phase) {
+      const int c0 = phase ? d0 : g0, c1 = phase ? d1 : g1, cpt = phase ? cpt_d : cpt_g;
+      const int pass = phase ? kFPassD : kFPassG;
+      for (int tile = c0 / cpt; ok && tile * cpt < c1; ++tile) {
+        const int e = s_tiles[3 * tile], R = s_tiles[3 * tile + 2];
+        const int j0 = max(c0 - tile * cpt, 0), j1 = min(c1 - tile * cpt, cpt);
+        for (int r0 = 0; ok && r0 < R; r0 += pass) {
+          for (int j = j0; j < j1; ++j) {
+            ok = mbar_wait(&empty[b], ph ^ 1, abort_flag);
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
+            uint8_t *buf = gsm + (size_t)b * L.slot;
+            if (lane == 0) {
+              fence_proxy_async_smem();  // generic accesses of the buffer before the copies
+              mbar_arrive_expect_tx(&full[b], phase ? tx_d : tx_g);
+            }
+            __syncwarp();
+            const int q = lane - 8 * (int)(it & 3);  // issuing lanes rotate over four groups
+            if (phase == 0) {
+              uint16_t *sc = reinterpret_cast<uint16_t *>(buf + 16 * L.Sh);
+              const int64_t rg = (int64_t)e * 2 * p.I + 8 * j, ru = rg + p.I;
+              if (q == 0 || q == 1) {
+                tma_load_2d(buf + q * 8 * L.Sh, &tmap_gu, 0, (int32_t)(q ? ru : rg), &full[b]);
+              } else if (q >= 2 && q < 6) {
+                const int kk = q - 2;  // gate s, up s, gate b, up b
+                const uint16_t *src = (kk < 2 ? p.Sgu : p.Bgu) + ((kk & 1) ? ru : rg) * Gh;
+                bulk_load(sc + kk * 8 * Gh, src, 16u * Gh, &full[b]);
+              }
+            } else {
+              uint16_t *sc = reinterpret_cast<uint16_t *>(buf + kFDownRows * L.Si);
+              const int64_t r = (int64_t)e * p.H + (int64_t)kFDownRows * j;
+              if (q == 0) {
+                tma_load_2d(buf, &tmap_d, 0, (int32_t)r, &full[b]);
+              } else if (q == 1 || q == 2) {
+                bulk_load(sc + (q - 1) * kFDownRows * Gi, (q == 2 ? p.Bd : p.Sd) + r * Gi,
+                          2u * kFDownRows * Gi, &full[b]);
+              }
+            }
+            ++it;
+            __syncwarp();
+            if (lane == 0) publish_issued(issued, it);
+            if (++b == nbuf) {
+              b = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+    __syncwarp();
+    if (lane == 0)
+      for (uint32_t i = (it > (uint32_t)nbuf ? it - nbuf : 0); i < it; ++i)
+        mbar_wait(&full[i % nbuf], (i / nbuf) & 1, nullptr, 200000000ull);
+    return;
+  }
+
+  // ------------------------------------------------ compute warps and stager
+  // the token rows: every non-producer warp permutes them into MMA fragment order
+  const int nt = (nwc + 1) * 32, ctid = warp < nwc ? tid : tid - 32;
+  bool ok = mbar_wait(&xfull[0], 0, abort_flag);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok) permute_units(xall, xsall, L.xrbh, Gh, p.T, ctid, nt);
+  named_sync(kFBarStart, nt);
+
+  const int gq = lane >> 2, t = lane & 3;
+  const int team = warp / kFTeam, member = warp % kFTeam;
+  uint32_t it = 0;  // chunk number in the CTA's stream (both phases)
+
+  if (warp < nwc) {
+    // ------------------------------------------------ gate/up + GeGLU (split K)
+    const int g_lo = member * Gh / kFTeam, g_hi = (member + 1) * Gh / kFTeam;
+    const bool pair_loads = (Gh % 2) == 0;
+    for (int tile = g0 / cpt_g; tile * cpt_g < g1; ++tile) {
+      const int row0 = s_tiles[3 * tile + 1], R = s_tiles[3 * tile + 2];
+      const int j0 = max(g0 - tile * cpt_g, 0), j1 = min(g1 - tile * cpt_g, cpt_g);
+      for (int r0 = 0; r0 < R; r0 += kFPassG) {
+        const int Rp = min(kFPassG, R - r0);
+        auto row_of = [&](int c) -> int { return s_tok[row0 + r0 + min(c, Rp - 1)]; };
+        const uint8_t *xrow = xall + (size_t)row_of(gq) * L.xrbh + t * 32;
+        const float *xs0 = xsall + (size_t)row_of(2 * t) * Gh;
+        const float *xs1 = xsall + (size_t)row_of(2 * t + 1) * Gh;
+        const int len = j1 - j0;
+        const int jfirst = (team - (int)(it % kFTeams) + kFTeams) % kFTeams;
+        int bn = (int)((it + jfirst) % (uint32_t)nbuf);
+        uint32_t phn = ((it + jfirst) / (uint32_t)nbuf) & 1u;
+        const uint32_t it_pass = it;
+        it += len;
+        for (int jj = jfirst; jj < len; jj += kFTeams) {
+          const int j = j0 + jj, b = bn;
+          const uint32_t phb = phn;
+          bn += kFTeams;
+          if (bn >= nbuf) {
+            bn -= nbuf;
+            phn ^= 1u;
+          }
+          if (ok) ok = wait_issued(issued, it_pass + jj + 1, abort_flag);
+          if (ok) ok = mbar_wait(&full[b], phb, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          uint8_t *buf = gsm + (size_t)b * L.slot;
+          const uint16_t *sc = reinterpret_cast<const uint16_t *>(buf + 16 * L.Sh);
+          const uint8_t *rA = buf + gq * L.Sh + t * 8, *rB = rA + 8 * L.Sh;
+          const uint16_t *scA = sc + gq * Gh, *scB = scA + 8 * Gh;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          if (ok) {
+            if (pair_loads)
+              warp_rows_dot<true>(rA, rB, scA, scB, 16 * Gh, xrow, xs0, xs1, g_lo, g_hi, acc);
+            else
+              warp_rows_dot<false>(rA, rB, scA, scB, 16 * Gh, xrow, xs0, xs1, g_lo, g_hi, acc);
+          }
+          // combine as in the per-call kernel: one team barrier (every warp done reading),
+          // the other warps park their sums, release the buffer and go on
+          named_sync(2 + 2 * team, kFTeam * 32);
+          float4 *park = reinterpret_cast<float4 *>(buf) + lane;
+          if (member) {
+            park[32 * (member - 1)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            named_arrive(3 + 2 * team, kFTeam * 32);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[b]);
+            continue;
+          }
+          named_sync(3 + 2 * team, kFTeam * 32);
+#pragma unroll
+          for (int m = 1; m < kFTeam; ++m) {
+            const float4 o = park[32 * (m - 1)];
+            acc[0] += o.x;
+            acc[1] += o.y;
+            acc[2] += o.z;
+            acc[3] += o.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[b]);
+          if (!ok) continue;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int jr = 2 * t + c;
+            if (jr >= Rp) continue;
+            const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
+            p.h[(int64_t)(row0 + r0 + jr) * p.I + n] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------ grid barrier: h is complete
+  named_sync(kFBarGrid, nt);
+  if (tid == 0) s_flags[1] = grid_barrier(p.gbar, *s_gen, abort_flag) ? 0 : 1;
+  named_sync(kFBarGrid, nt);
+  if (s_flags[1]) {
+    ok = false;
+    if (tid == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+  }
+
+  if (warp == nwc + 1) {
+    // ------------------------------------------------ stager: h rows of each down pass
+    uint32_t xit = 0;
+    for (int tile = d0 / cpt_d; ok && tile * cpt_d < d1; ++tile) {
+      const int row0 = s_tiles[3 * tile + 1], R = s_tiles[3 * tile + 2];
+      for (int r0 = 0; ok && r0 < R; r0 += kFPassD, ++xit) {
+        const int Rp = min(kFPassD, R - r0), xb = xit & 1;
+        ok = mbar_wait(&xempty[xb], ((xit >> 1) & 1) ^ 1, abort_flag);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        uint8_t *xbuf = xall + (size_t)xb * kFPassD * L.xrbi;
+        float *xs = xsall + (size_t)xb * kFPassD * Gi;
+        // plain loads from L2 (h was written by other CTAs before the barrier), permuted
+        // in registers; the 8 blocks of a group are 8 consecutive lanes
+        const int nblk = Rp * Gi * 8;
+        for (int base = 0; base < nblk; base += 32) {
+          const int i = base + lane;
+          const bool act = i < nblk;
+          const int jrow = i / (Gi * 8), rem = i - jrow * Gi * 8, g = rem >> 3;
+          float part = 0.f;
+          if (act) {
+            const uint4 q = __ldcg(reinterpret_cast<const uint4 *>(
+                                       p.h + (int64_t)(row0 + r0 + jrow) * p.I) + rem);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+            auto el = [&](int kk) -> uint32_t {
+              return (kk & 1) ? (w[kk >> 1] >> 16) : (w[kk >> 1] & 0xFFFFu);
+            };
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) part += __uint_as_float(el(kk) << 16);
+            uint4 o;
+            o.x = el(0) | (el(4) << 16);
+            o.y = el(1) | (el(5) << 16);
+            o.z = el(2) | (el(6) << 16);
+            o.w = el(3) | (el(7) << 16);
+            *reinterpret_cast<uint4 *>(xbuf + (size_t)jrow * L.xrbi + rem * 16) = o;
+          }
+          part += __shfl_xor_sync(0xffffffffu, part, 1);
+          part += __shfl_xor_sync(0xffffffffu, part, 2);
+          part += __shfl_xor_sync(0xffffffffu, part, 4);
+          if (act && (rem & 7) == 0) xs[jrow * Gi + g] = part;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xready[xb]);
+      }
+    }
+    if (!ok && lane == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+    return;
+  }
+
+  // ------------------------------------------------ down + weighted un-sort (split rows)
+  {
+    const int row_lo = 16 * member;
+    const bool pair_loads = (Gi % 2) == 0;
+    int pend_blk = -1, pend_rows = 0, flt_blk = -1, flt_rows = 0, flt_old = 0;
+    uint32_t xit = 0;
+    for (int tile = d0 / cpt_d; tile * cpt_d < d1; ++tile) {
+      const int row0 = s_tiles[3 * tile + 1], R = s_tiles[3 * tile + 2];
+      const int j0 = max(d0 - tile * cpt_d, 0), j1 = min(d1 - tile * cpt_d, cpt_d);
+      for (int r0 = 0; r0 < R; r0 += kFPassD, ++xit) {
+        const int Rp = min(kFPassD, R - r0), xb = xit & 1;
+        if (ok) ok = mbar_wait(&xready[xb], (xit >> 1) & 1, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        const uint8_t *xbuf = xall + (size_t)xb * kFPassD * L.xrbi;
+        const float *xs = xsall + (size_t)xb * kFPassD * Gi;
+        const uint8_t *xrow = xbuf + (size_t)min(gq, Rp - 1) * L.xrbi + t * 32;
+        const float *xs0 = xs + (size_t)min(2 * t, Rp - 1) * Gi;
+        const float *xs1 = xs + (size_t)min(2 * t + 1, Rp - 1) * Gi;
+        int a_c[2] = {0, 0};
+        float w_c[2] = {0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          if (2 * t + c < Rp) {
+            a_c[c] = s_perm[row0 + r0 + 2 * t + c];
+            w_c[c] = s_w[row0 + r0 + 2 * t + c];
+          }
+        const int len = j1 - j0;
+        const int jfirst = (team - (int)(it % kFTeams) + kFTeams) % kFTeams;
+        int bn = (int)((it + jfirst) % (uint32_t)nbuf);
+        uint32_t phn = ((it + jfirst) / (uint32_t)nbuf) & 1u;
+        const uint32_t it_pass = it;
+        it += len;
+        for (int jj = jfirst; jj < len; jj += kFTeams) {
+          const int j = j0 + jj, b = bn;
+          const uint32_t phb = phn;
+          bn += kFTeams;
+          if (bn >= nbuf) {
+            bn -= nbuf;
+            phn ^= 1u;
+          }
+          if (ok) ok = wait_issued(issued, it_pass + jj + 1, abort_flag);
+          if (ok) ok = mbar_wait(&full[b], phb, abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          uint8_t *buf = gsm + (size_t)b * L.slot;
+          const uint16_t *sc = reinterpret_cast<const uint16_t *>(buf + kFDownRows * L.Si);
+          const uint8_t *rA = buf + (row_lo + gq) * L.Si + t * 8, *rB = rA + 8 * L.Si;
+          const uint16_t *scA = sc + (row_lo + gq) * Gi, *scB = scA + 8 * Gi;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          if (ok) {
+            if (pair_loads)
+              warp_rows_dot<true>(rA, rB, scA, scB, kFDownRows * Gi, xrow, xs0, xs1, 0, Gi,
+                                  acc);
+            else
+              warp_rows_dot<false>(rA, rB, scA, scB, kFDownRows * Gi, xrow, xs0, xs1, 0, Gi,
+                                   acc);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[b]);
+          if (!ok) continue;
+          if (flt_blk >= 0) {  // the count issued one chunk ago
+            const int old = __shfl_sync(0xffffffffu, flt_old, 0);
+            if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
+            flt_blk = -1;
+          }
+          if (pend_blk >= 0) {  // count the previous chunk's reductions
+            __syncwarp();
+            if (lane == 0) {
+              __threadfence();
+              flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
+            }
+            flt_blk = pend_blk;
+            flt_rows = pend_rows;
+            pend_blk = -1;
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            if (2 * t + c >= Rp) continue;
+            float *yrow = p.y_acc + (int64_t)(a_c[c] / p.k) * p.H + kFDownRows * j + row_lo;
+            atomicAdd(yrow + gq, w_c[c] * acc[c]);
+            atomicAdd(yrow + gq + 8, w_c[c] * acc[2 + c]);
+          }
+          pend_blk = (kFDownRows * j + row_lo) / 16;
+          pend_rows = Rp;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xempty[xb]);
+      }
+    }
+    if (ok) {  // drain the count pipeline
+      if (flt_blk >= 0) {
+        const int old = __shfl_sync(0xffffffffu, flt_old, 0);
+        if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
+      }
+      if (pend_blk >= 0) {
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence();
+          flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
+        }
+        const int old = __shfl_sync(0xffffffffu, flt_old, 0);
+        if (old + pend_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, pend_blk, lane);
+      }
+    }
+    if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+static int fused_sm_count() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+static int fused_nbuf(int H, int I, int T, int A, int E, int max_tiles) {
+  for (int nb = 16; nb >= 4; --nb) {
+    const FLayout L(H, I, T, A, E, max_tiles, nb);
+    if (L.total <= 227 * 1024 && L.scratch_bytes() <= L.slot) return nb;
+  }
+  return 0;
+}
+
+moe_status fused_layer_check(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                             int32_t tile_m, int32_t max_tiles) {
+  const int64_t A = (int64_t)T * k;
+  if (A > kFMaxA || T > kFMaxT) return MOE_ERR_UNSUPPORTED;
+  if (!gemv_supported(H, I) || H % kFDownRows || I % 8) return MOE_ERR_UNSUPPORTED;
+  if (fused_nbuf(H, I, T, (int)A, E, max_tiles) < 4) return MOE_ERR_UNSUPPORTED;
+  (void)tile_m;
+  return MOE_OK;
+}
+
+moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights, int32_t T,
+                              int32_t k, int32_t E, const uint16_t *x, const uint32_t *Wgu,
+                              const uint16_t *Sgu, const uint16_t *Bgu, const uint32_t *Wd,
+                              const uint16_t *Sd, const uint16_t *Bd, int32_t H, int32_t I,
+                              int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
+                              int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
+                              int32_t *tile_count, int32_t *status, uint16_t *h, float *y_acc,
+                              uint16_t *y, cudaStream_t stream) {
+  const char *what = "moe_layer_fused";
+  const int A = T * k;
+  const int nbuf = fused_nbuf(H, I, T, A, E, max_tiles);
+  const FLayout L(H, I, T, A, E, max_tiles, nbuf);
+  CUtensorMap mgu, md;
+  if (!make_map_2d(&mgu, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, Wgu, (uint64_t)H / 16,
+                   (uint64_t)E * 2 * I, (uint32_t)(L.Sh / 8), 8u, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&md, CU_TENSOR_MAP_DATA_TYPE_UINT64, 8, Wd, (uint64_t)I / 16, (uint64_t)E * H,
+                   (uint32_t)(L.Si / 8), (uint32_t)kFDownRows, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+    set_error("%s: cuTensorMapEncodeTiled failed for a weight tensor", what);
+    return MOE_ERR_CUDA;
+  }
+  if (cudaFuncSetAttribute((const void *)fused_layer_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
+    return check_launch(what);
+  FArgs a;
+  a.topk_ids = topk_ids;
+  a.topk_weights = topk_weights;
+  a.x = x;
+  a.Sgu = Sgu;
+  a.Bgu = Bgu;
+  a.Sd = Sd;
+  a.Bd = Bd;
+  a.T = T;
+  a.k = k;
+  a.A = A;
+  a.E = E;
+  a.H = H;
+  a.I = I;
+  a.BM = tile_m;
+  a.max_tiles = max_tiles;
+  a.nbuf = nbuf;
+  a.sorted_ids = sorted_ids;
+  a.perm = perm;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.tiles = tiles;
+  a.tile_count = tile_count;
+  a.status = status;
+  a.h = h;
+  a.y_acc = y_acc;
+  a.cnt = reinterpret_cast<int32_t *>(y_acc + (int64_t)T * H);
+  a.gbar = a.cnt + H / 16;
+  a.y = y;
+  // cooperative: every CTA resident at once (the grid barrier waits for all of them)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(fused_sm_count());
+  cfg.blockDim = dim3(kFThreads);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, fused_layer_kernel, mgu, md, a);
+  return check_launch(what);
+}
+
+}  // namespace moeqmm

@@ -27,201 +27,12 @@
 // with zeros), so the four rows that one quarter-warp reads fall in
 // different banks.
 #include "common.cuh"
+#include "gemv_core.cuh"
 #include "kernels.h"
 #include "tmap.h"
 #include "umma.cuh"
 
 namespace moeqmm {
-
-__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
-  return d;
-}
-
-// bf16x2 {128 + q_p (low half), 128 + q_{p+4} (high half)} of one packed word
-__device__ __forceinline__ uint32_t pair128(uint32_t word, int p) {
-  return lop_and_or(word >> (4 * p), 0x000F000Fu, 0x43004300u);
-}
-
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                               uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// d = A B (no accumulator input: the first MMA of a chain)
-__device__ __forceinline__ void mma_bf16_16816_first(float (&d)[4], const uint32_t (&a)[4],
-                                                     uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-      "{%8, %9}, {%10, %10, %10, %10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
-}
-
-__device__ __forceinline__ float bf16f(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
-
-// D_g of one group for the lane's two weight rows (A: MMA row gq, B: row gq + 8) and the
-// staged activation columns, as one chain of four MMAs.
-//   wa, wb: the lane's 8 packed bytes of the group in rows A and B (k = 16t .. 16t+15)
-//   f01, f23: the lane's two permuted 16-byte activation blocks of the group
-__device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, uint4 f01, uint4 f23,
-                                          float (&d)[4]) {
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const uint32_t ua = (m >> 1) ? wa.y : wa.x;
-    const uint32_t ub = (m >> 1) ? wb.y : wb.x;
-    const int p0 = 2 * (m & 1);
-    const uint32_t a[4] = {pair128(ua, p0), pair128(ub, p0), pair128(ua, p0 + 1),
-                           pair128(ub, p0 + 1)};
-    const uint32_t b0 = m == 0 ? f01.x : m == 1 ? f01.z : m == 2 ? f23.x : f23.z;
-    const uint32_t b1 = m == 0 ? f01.y : m == 1 ? f01.w : m == 2 ? f23.y : f23.w;
-    if (m == 0)
-      mma_bf16_16816_first(d, a, b0, b1);
-    else
-      mma_bf16_16816(d, a, b0, b1);
-  }
-}
-
-// acc += s * D + (b - 128 s) * X for rows A (acc[0], acc[1]) and B (acc[2], acc[3]) and
-// the lane's two activation columns (x.x, x.y)
-__device__ __forceinline__ void group_fold(float sa, float ba, float sb, float bb, float2 x,
-                                           const float (&d)[4], float (&acc)[4]) {
-  const float ca = fmaf(-128.f, sa, ba), cb = fmaf(-128.f, sb, bb);
-  acc[0] = fmaf(sa, d[0], fmaf(ca, x.x, acc[0]));
-  acc[1] = fmaf(sa, d[1], fmaf(ca, x.y, acc[1]));
-  acc[2] = fmaf(sb, d[2], fmaf(cb, x.x, acc[2]));
-  acc[3] = fmaf(sb, d[3], fmaf(cb, x.y, acc[3]));
-}
-
-
-// Dot products of the warp's 16 staged weight rows with the staged activation rows over
-// groups [g_begin, g_end).
-//   rA, rB: the lane's rows (MMA rows gq and gq + 8) at byte t*8 of group 0
-//   scA, scB: scale rows of MMA rows gq and gq + 8 (bf16; biases at + bofs elements)
-//   xrow: the lane's activation row (MMA column gq) at byte t*32 of group 0
-//   xs0, xs1: group sums of the activation rows of the lane's two output columns
-// PAIR: the scales and sums of groups g, g+1 are read as pairs from an even g (needs
-// even G: rows start 4-byte aligned); an odd first group is done on its own.
-template <bool PAIR>
-__device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
-                                          const uint16_t *scA, const uint16_t *scB, int bofs,
-                                          const uint8_t *xrow, const float *xs0,
-                                          const float *xs1, int g, float (&acc)[4]);
-
-template <bool PAIR>
-__device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *rB,
-                                              const uint16_t *scA, const uint16_t *scB, int bofs,
-                                              const uint8_t *xrow, const float *xs0,
-                                              const float *xs1, int g_begin, int g_end,
-                                              float (&acc)[4]) {
-  int g = g_begin;
-  if (PAIR && (g & 1) && g < g_end) {
-    one_group<PAIR>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g, acc);
-    ++g;
-  }
-#pragma unroll 1
-  for (; g + 1 < g_end; g += 2) {
-    const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
-    const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
-    const uint2 a1 = *reinterpret_cast<const uint2 *>(rA + g * 32 + 32);
-    const uint2 b1 = *reinterpret_cast<const uint2 *>(rB + g * 32 + 32);
-    const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
-    const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
-    const uint4 f1a = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 128);
-    const uint4 f1b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 144);
-    float d0[4], d1[4];
-    group_mma(a0, b0, f0a, f0b, d0);
-    group_mma(a1, b1, f1a, f1b, d1);
-    float sa0, sa1, sb0, sb1, ba0, ba1, bb0, bb1;
-    float2 xg0, xg1;  // {column 2t, column 2t+1} sums of groups g and g + 1
-    if (PAIR) {
-      const uint32_t us_a = *reinterpret_cast<const uint32_t *>(scA + g);
-      const uint32_t us_b = *reinterpret_cast<const uint32_t *>(scB + g);
-      const uint32_t ub_a = *reinterpret_cast<const uint32_t *>(scA + bofs + g);
-      const uint32_t ub_b = *reinterpret_cast<const uint32_t *>(scB + bofs + g);
-      sa0 = __uint_as_float(us_a << 16);
-      sa1 = __uint_as_float(us_a & 0xFFFF0000u);
-      sb0 = __uint_as_float(us_b << 16);
-      sb1 = __uint_as_float(us_b & 0xFFFF0000u);
-      ba0 = __uint_as_float(ub_a << 16);
-      ba1 = __uint_as_float(ub_a & 0xFFFF0000u);
-      bb0 = __uint_as_float(ub_b << 16);
-      bb1 = __uint_as_float(ub_b & 0xFFFF0000u);
-      const float2 p0 = *reinterpret_cast<const float2 *>(xs0 + g);
-      const float2 p1 = *reinterpret_cast<const float2 *>(xs1 + g);
-      xg0 = make_float2(p0.x, p1.x);
-      xg1 = make_float2(p0.y, p1.y);
-    } else {
-      sa0 = bf16f(scA[g]);
-      sa1 = bf16f(scA[g + 1]);
-      sb0 = bf16f(scB[g]);
-      sb1 = bf16f(scB[g + 1]);
-      ba0 = bf16f(scA[bofs + g]);
-      ba1 = bf16f(scA[bofs + g + 1]);
-      bb0 = bf16f(scB[bofs + g]);
-      bb1 = bf16f(scB[bofs + g + 1]);
-      xg0 = make_float2(xs0[g], xs1[g]);
-      xg1 = make_float2(xs0[g + 1], xs1[g + 1]);
-    }
-    group_fold(sa0, ba0, sb0, bb0, xg0, d0, acc);
-    group_fold(sa1, ba1, sb1, bb1, xg1, d1, acc);
-  }
-  if (g < g_end) one_group<PAIR>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g, acc);
-}
-
-template <bool PAIR>
-__device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
-                                          const uint16_t *scA, const uint16_t *scB, int bofs,
-                                          const uint8_t *xrow, const float *xs0,
-                                          const float *xs1, int g, float (&acc)[4]) {
-  const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
-  const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
-  const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
-  const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
-  float d0[4];
-  group_mma(a0, b0, f0a, f0b, d0);
-  group_fold(bf16f(scA[g]), bf16f(scA[bofs + g]), bf16f(scB[g]), bf16f(scB[bofs + g]),
-             make_float2(xs0[g], xs1[g]), d0, acc);
-}
-
-// In place: the eight 16-byte blocks of activation row r, group g (elements 8c .. 8c+7
-// in block c) become the MMA B fragments {x0,x4 | x1,x5 | x2,x6 | x3,x7}, and the group's
-// sum goes to xs[r * G + g].  Units u = r * G + g, u = first, first + step, ...; a thread
-// visits its blocks in an order rotated by u, so neighbouring threads hit other banks.
-__device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb, int G, int nrows,
-                                              int first, int step) {
-  for (int u = first; u < nrows * G; u += step) {
-    const int r = u / G, g = u - r * G;
-    uint8_t *base = xbuf + (size_t)r * xrb + g * 128;
-    uint4 q[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(base + ((c + u) & 7) * 16);
-    float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
-      auto el = [&](int k) -> uint32_t {
-        return (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
-      };
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sum += __uint_as_float(el(k) << 16);
-      uint4 o;
-      o.x = el(0) | (el(4) << 16);
-      o.y = el(1) | (el(5) << 16);
-      o.z = el(2) | (el(6) << 16);
-      o.w = el(3) | (el(7) << 16);
-      *reinterpret_cast<uint4 *>(base + ((c + u) & 7) * 16) = o;
-    }
-    xs[u] = sum;
-  }
-}
 
 // ---------------------------------------------------------------- the persistent kernel
 //
@@ -261,12 +72,6 @@ struct GemvCfg {
   static constexpr int kThreads = (kMaxCompute + 2) * 32;
 };
 
-// Row stride of staged weight rows: the packed row (K/2 bytes) padded to 32 mod 128.
-__host__ __device__ inline int padded_row_bytes(int K) {
-  const int ws = K / 2;
-  return ws + (((32 - ws) % 128) + 128) % 128;
-}
-
 struct PLayout {
   int G, S, xrb, rows, w_bytes, chunk_bytes, nbuf, nxrows, ntok;
   int off_x, off_xs, off_tok, off_bar, off_misc, total;
@@ -299,17 +104,6 @@ constexpr int kSmemLimit = 227 * 1024;
 constexpr int kBarStart = 15;
 constexpr int kMaxTeams = 13;
 
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ void named_arrive(int id, int nthreads) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-struct GemvArgs;
-__device__ void cast_block(const GemvArgs &p, int blk, int lane);
-
 struct GemvArgs {
   const uint16_t *act;  // gate/up: x [T, H]; down: h [A, I]
   const uint16_t *Sc, *Bi;
@@ -322,20 +116,6 @@ struct GemvArgs {
   int32_t *cnt;  // DOWN: per-16-column counters (fused cast), or null
   uint16_t *y;
 };
-
-// y[:, 16 blk .. 16 blk + 15] = bf16(y_acc[...]) by one warp, after the count of block blk
-// reached A (every contribution performed; the fence orders the reads after the count).
-// The warp then clears those accumulator entries and the counter: the workspace is left
-// zeroed for the next call.
-__device__ void cast_block(const GemvArgs &p, int blk, int lane) {
-  __threadfence();
-  for (int i = lane; i < p.T * 16; i += 32) {
-    const int64_t o = (int64_t)(i >> 4) * p.H + 16 * blk + (i & 15);
-    p.y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(p.y_acc + o)));
-    __stcg(p.y_acc + o, 0.f);
-  }
-  if (lane == 0) p.cnt[blk] = 0;
-}
 
 template <int MODE>
 __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
@@ -363,6 +143,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   uint64_t *xempty = xready + 2;   // [2] every compute warp done with the buffer
   uint64_t *xissued = xempty + 2;  // first activation copy issued (it goes out first)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + L.off_misc);
+  uint32_t *issued = reinterpret_cast<uint32_t *>(gsm + L.off_misc + 8);  // chunks issued
 
   // prologue (may overlap the previous kernel): nothing in global memory is touched
   if (warp == nwc && lane == 0) prefetch_tensormap(&tmap_w);
@@ -391,6 +172,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
     }
     mbar_init(xissued, 1);
     *abort_flag = 0;
+    *issued = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -439,6 +221,8 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
             }
           }
           ++it;
+          __syncwarp();
+          if (lane == 0) publish_issued(issued, it);
           if (++b == nbuf) {
             b = 0;
             ph ^= 1u;
@@ -582,6 +366,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
       const int jfirst = (team - (int)(it % (uint32_t)nteams) + nteams) % nteams;
       int bn = (int)((it + jfirst) % (uint32_t)nbuf);
       uint32_t phn = ((it + jfirst) / (uint32_t)nbuf) & 1u;
+      const uint32_t it_pass = it;
       it += len;
       for (int jj = jfirst; jj < len; jj += nteams) {
         const int j = j0 + jj, b = bn;
@@ -591,6 +376,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
           bn -= nbuf;
           phn ^= 1u;
         }
+        if (ok) ok = wait_issued(issued, it_pass + jj + 1, abort_flag);
         if (ok) ok = mbar_wait(&full[b], ph, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         uint8_t *buf = gsm + (size_t)b * L.chunk_bytes;
@@ -633,7 +419,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
         if (MODE == 1 && p.cnt) {
           if (flt_blk >= 0) {  // the count issued one chunk ago
             const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-            if (old + flt_rows == p.A) cast_block(p, flt_blk, lane);
+            if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
             flt_blk = -1;
           }
           if (pend_blk >= 0) {  // count the previous chunk's reductions
@@ -675,7 +461,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   if (MODE == 1 && p.cnt && ok) {  // drain the count pipeline
     if (flt_blk >= 0) {
       const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-      if (old + flt_rows == p.A) cast_block(p, flt_blk, lane);
+      if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
     }
     if (pend_blk >= 0) {
       __syncwarp();
@@ -684,7 +470,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
         flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
       }
       const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-      if (old + pend_rows == p.A) cast_block(p, pend_blk, lane);
+      if (old + pend_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, pend_blk, lane);
     }
   }
   if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
@@ -783,8 +569,6 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   if (nteams > Cfg::kMaxCompute / Cfg::kTeam) nteams = Cfg::kMaxCompute / Cfg::kTeam;
   if (nteams > kMaxTeams) nteams = kMaxTeams;
   const int nwc = nteams * Cfg::kTeam;
-  // split K: exactly two buffers per team (the combine's barrier parity relies on it)
-  if (Cfg::kSplitK) nbuf = 2 * nteams;
   const PLayout L(K, Cfg::kRows, nxrows, whole ? ntok_all : 0, nbuf);
   CUtensorMap tmap;
   const int64_t rows = (int64_t)t.num_experts * (MODE == 0 ? 2 * I : H);

@@ -1,0 +1,266 @@
+// Device building blocks of the weight-streaming kernels (the per-call GEMV in gemv.cu and the
+// fused decode layer in fused.cu): nibble unpack into bf16 MMA operands, the per-group dot
+// product and affine fold, the activation permutation, barriers.  Not part of the C ABI.
+//
+// Per 64-wide group g of one weight row the dot product splits as
+//   sum_k w_k x_k = s_g * D_g + (b_g - 128 s_g) * X_g,
+//   D_g = sum_k (128 + q_k) x_k,   X_g = sum_k x_k,
+// with w = scale * q + bias per 64-group (Layr-Labs/mlx PR #4, "What").
+#pragma once
+
+#include "common.cuh"
+#include "umma.cuh"
+
+namespace moeqmm {
+
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t bits) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(mask), "r"(bits));
+  return d;
+}
+
+// bf16x2 {128 + q_p (low half), 128 + q_{p+4} (high half)} of one packed word
+__device__ __forceinline__ uint32_t pair128(uint32_t word, int p) {
+  return lop_and_or(word >> (4 * p), 0x000F000Fu, 0x43004300u);
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// d = A B (no accumulator input: the first MMA of a chain)
+__device__ __forceinline__ void mma_bf16_16816_first(float (&d)[4], const uint32_t (&a)[4],
+                                                     uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.f));
+}
+
+__device__ __forceinline__ float bf16f(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// D_g of one group for the lane's two weight rows (A: MMA row gq, B: row gq + 8) and the
+// staged activation columns, as one chain of four MMAs.
+//   wa, wb: the lane's 8 packed bytes of the group in rows A and B (k = 16t .. 16t+15)
+//   f01, f23: the lane's two permuted 16-byte activation blocks of the group
+__device__ __forceinline__ void group_mma(uint2 wa, uint2 wb, uint4 f01, uint4 f23,
+                                          float (&d)[4]) {
+#pragma unroll
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t ua = (m >> 1) ? wa.y : wa.x;
+    const uint32_t ub = (m >> 1) ? wb.y : wb.x;
+    const int p0 = 2 * (m & 1);
+    const uint32_t a[4] = {pair128(ua, p0), pair128(ub, p0), pair128(ua, p0 + 1),
+                           pair128(ub, p0 + 1)};
+    const uint32_t b0 = m == 0 ? f01.x : m == 1 ? f01.z : m == 2 ? f23.x : f23.z;
+    const uint32_t b1 = m == 0 ? f01.y : m == 1 ? f01.w : m == 2 ? f23.y : f23.w;
+    if (m == 0)
+      mma_bf16_16816_first(d, a, b0, b1);
+    else
+      mma_bf16_16816(d, a, b0, b1);
+  }
+}
+
+// acc += s * D + (b - 128 s) * X for rows A (acc[0], acc[1]) and B (acc[2], acc[3]) and
+// the lane's two activation columns (x.x, x.y)
+__device__ __forceinline__ void group_fold(float sa, float ba, float sb, float bb, float2 x,
+                                           const float (&d)[4], float (&acc)[4]) {
+  const float ca = fmaf(-128.f, sa, ba), cb = fmaf(-128.f, sb, bb);
+  acc[0] = fmaf(sa, d[0], fmaf(ca, x.x, acc[0]));
+  acc[1] = fmaf(sa, d[1], fmaf(ca, x.y, acc[1]));
+  acc[2] = fmaf(sb, d[2], fmaf(cb, x.x, acc[2]));
+  acc[3] = fmaf(sb, d[3], fmaf(cb, x.y, acc[3]));
+}
+
+
+// Dot products of the warp's 16 staged weight rows with the staged activation rows over
+// groups [g_begin, g_end).
+//   rA, rB: the lane's rows (MMA rows gq and gq + 8) at byte t*8 of group 0
+//   scA, scB: scale rows of MMA rows gq and gq + 8 (bf16; biases at + bofs elements)
+//   xrow: the lane's activation row (MMA column gq) at byte t*32 of group 0
+//   xs0, xs1: group sums of the activation rows of the lane's two output columns
+// PAIR: the scales and sums of groups g, g+1 are read as pairs from an even g (needs
+// even G: rows start 4-byte aligned); an odd first group is done on its own.
+template <bool PAIR>
+__device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
+                                          const uint16_t *scA, const uint16_t *scB, int bofs,
+                                          const uint8_t *xrow, const float *xs0,
+                                          const float *xs1, int g, float (&acc)[4]);
+
+template <bool PAIR>
+__device__ __forceinline__ void warp_rows_dot(const uint8_t *rA, const uint8_t *rB,
+                                              const uint16_t *scA, const uint16_t *scB, int bofs,
+                                              const uint8_t *xrow, const float *xs0,
+                                              const float *xs1, int g_begin, int g_end,
+                                              float (&acc)[4]) {
+  int g = g_begin;
+  if (PAIR && (g & 1) && g < g_end) {
+    one_group<PAIR>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g, acc);
+    ++g;
+  }
+#pragma unroll 1
+  for (; g + 1 < g_end; g += 2) {
+    const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
+    const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
+    const uint2 a1 = *reinterpret_cast<const uint2 *>(rA + g * 32 + 32);
+    const uint2 b1 = *reinterpret_cast<const uint2 *>(rB + g * 32 + 32);
+    const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
+    const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
+    const uint4 f1a = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 128);
+    const uint4 f1b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 144);
+    float d0[4], d1[4];
+    group_mma(a0, b0, f0a, f0b, d0);
+    group_mma(a1, b1, f1a, f1b, d1);
+    float sa0, sa1, sb0, sb1, ba0, ba1, bb0, bb1;
+    float2 xg0, xg1;  // {column 2t, column 2t+1} sums of groups g and g + 1
+    if (PAIR) {
+      const uint32_t us_a = *reinterpret_cast<const uint32_t *>(scA + g);
+      const uint32_t us_b = *reinterpret_cast<const uint32_t *>(scB + g);
+      const uint32_t ub_a = *reinterpret_cast<const uint32_t *>(scA + bofs + g);
+      const uint32_t ub_b = *reinterpret_cast<const uint32_t *>(scB + bofs + g);
+      sa0 = __uint_as_float(us_a << 16);
+      sa1 = __uint_as_float(us_a & 0xFFFF0000u);
+      sb0 = __uint_as_float(us_b << 16);
+      sb1 = __uint_as_float(us_b & 0xFFFF0000u);
+      ba0 = __uint_as_float(ub_a << 16);
+      ba1 = __uint_as_float(ub_a & 0xFFFF0000u);
+      bb0 = __uint_as_float(ub_b << 16);
+      bb1 = __uint_as_float(ub_b & 0xFFFF0000u);
+      const float2 p0 = *reinterpret_cast<const float2 *>(xs0 + g);
+      const float2 p1 = *reinterpret_cast<const float2 *>(xs1 + g);
+      xg0 = make_float2(p0.x, p1.x);
+      xg1 = make_float2(p0.y, p1.y);
+    } else {
+      sa0 = bf16f(scA[g]);
+      sa1 = bf16f(scA[g + 1]);
+      sb0 = bf16f(scB[g]);
+      sb1 = bf16f(scB[g + 1]);
+      ba0 = bf16f(scA[bofs + g]);
+      ba1 = bf16f(scA[bofs + g + 1]);
+      bb0 = bf16f(scB[bofs + g]);
+      bb1 = bf16f(scB[bofs + g + 1]);
+      xg0 = make_float2(xs0[g], xs1[g]);
+      xg1 = make_float2(xs0[g + 1], xs1[g + 1]);
+    }
+    group_fold(sa0, ba0, sb0, bb0, xg0, d0, acc);
+    group_fold(sa1, ba1, sb1, bb1, xg1, d1, acc);
+  }
+  if (g < g_end) one_group<PAIR>(rA, rB, scA, scB, bofs, xrow, xs0, xs1, g, acc);
+}
+
+template <bool PAIR>
+__device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
+                                          const uint16_t *scA, const uint16_t *scB, int bofs,
+                                          const uint8_t *xrow, const float *xs0,
+                                          const float *xs1, int g, float (&acc)[4]) {
+  const uint2 a0 = *reinterpret_cast<const uint2 *>(rA + g * 32);
+  const uint2 b0 = *reinterpret_cast<const uint2 *>(rB + g * 32);
+  const uint4 f0a = *reinterpret_cast<const uint4 *>(xrow + g * 128);
+  const uint4 f0b = *reinterpret_cast<const uint4 *>(xrow + g * 128 + 16);
+  float d0[4];
+  group_mma(a0, b0, f0a, f0b, d0);
+  group_fold(bf16f(scA[g]), bf16f(scA[bofs + g]), bf16f(scB[g]), bf16f(scB[bofs + g]),
+             make_float2(xs0[g], xs1[g]), d0, acc);
+}
+
+// In place: the eight 16-byte blocks of activation row r, group g (elements 8c .. 8c+7
+// in block c) become the MMA B fragments {x0,x4 | x1,x5 | x2,x6 | x3,x7}, and the group's
+// sum goes to xs[r * G + g].  Units u = r * G + g, u = first, first + step, ...; a thread
+// visits its blocks in an order rotated by u, so neighbouring threads hit other banks.
+__device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb, int G, int nrows,
+                                              int first, int step) {
+  for (int u = first; u < nrows * G; u += step) {
+    const int r = u / G, g = u - r * G;
+    uint8_t *base = xbuf + (size_t)r * xrb + g * 128;
+    uint4 q[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(base + ((c + u) & 7) * 16);
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
+      auto el = [&](int k) -> uint32_t {
+        return (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
+      };
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum += __uint_as_float(el(k) << 16);
+      uint4 o;
+      o.x = el(0) | (el(4) << 16);
+      o.y = el(1) | (el(5) << 16);
+      o.z = el(2) | (el(6) << 16);
+      o.w = el(3) | (el(7) << 16);
+      *reinterpret_cast<uint4 *>(base + ((c + u) & 7) * 16) = o;
+    }
+    xs[u] = sum;
+  }
+}
+
+// Row stride of staged weight rows: the packed row (K/2 bytes) padded to 32 mod 128.
+__host__ __device__ inline int padded_row_bytes(int K) {
+  const int ws = K / 2;
+  return ws + (((32 - ws) % 128) + 128) % 128;
+}
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void named_arrive(int id, int nthreads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+
+// y[:, 16 blk .. 16 blk + 15] = bf16(y_acc[...]) by one warp, once the count of block blk
+// reached the number of assignments (every contribution performed; the fence orders the
+// reads after the count).  The warp then clears those accumulator entries and the counter:
+// the workspace is left zeroed for the next call.
+__device__ __forceinline__ void cast_block(float *y_acc, uint16_t *y, int32_t *cnt, int T, int H,
+                                           int blk, int lane) {
+  __threadfence();
+  for (int i = lane; i < T * 16; i += 32) {
+    const int64_t o = (int64_t)(i >> 4) * H + 16 * blk + (i & 15);
+    y[o] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(y_acc + o)));
+    __stcg(y_acc + o, 0.f);
+  }
+  if (lane == 0) cnt[blk] = 0;
+}
+
+// A ring whose buffers are shared by several consumer teams: chunk i uses buffer i % nbuf,
+// and its consumer waits on the buffer's barrier with the parity of its use.  That parity
+// also matches two uses back, so the consumer first waits until the producer has issued
+// chunk i (the producer publishes the number of chunks issued): by then the buffer's
+// previous chunk has been consumed, hence has landed, and the parity wait sees exactly the
+// phase of chunk i.  Bounded like every wait (sets the abort flag when it gives up).
+__device__ __forceinline__ bool wait_issued(const uint32_t *issued, uint32_t need,
+                                            volatile int *abort_flag) {
+  const volatile uint32_t *v = issued;
+  if (*v < need) {
+    const uint64_t t0 = umma::globaltimer_ns();
+    while (*v < need) {
+      __nanosleep(32);
+      if (*abort_flag) return false;
+      if (umma::globaltimer_ns() - t0 > 2000000000ull) {
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  __threadfence_block();
+  return true;
+}
+
+// the producer's side: after issuing chunk n - 1
+__device__ __forceinline__ void publish_issued(uint32_t *issued, uint32_t n) {
+  __threadfence_block();
+  *reinterpret_cast<volatile uint32_t *>(issued) = n;
+}
+
+}  // namespace moeqmm

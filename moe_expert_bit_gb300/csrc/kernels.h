@@ -24,6 +24,17 @@ moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,
                        const moe_bf16_t *Sd, const moe_bf16_t *Bd, const moe_tiles_t *tiles,
                        const float *topk_weights, int32_t H, int32_t I, int32_t variant,
                        float *y_acc_ws, moe_bf16_t *y, bool clear_ws, cudaStream_t stream);
+// The fused decode layer (fused.cu): MOE_OK if a call of this shape fits it.
+moe_status fused_layer_check(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
+                             int32_t tile_m, int32_t max_tiles);
+moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights, int32_t T,
+                              int32_t k, int32_t E, const uint16_t *x, const uint32_t *Wgu,
+                              const uint16_t *Sgu, const uint16_t *Bgu, const uint32_t *Wd,
+                              const uint16_t *Sd, const uint16_t *Bd, int32_t H, int32_t I,
+                              int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
+                              int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
+                              int32_t *tile_count, int32_t *status, uint16_t *h, float *y_acc,
+                              uint16_t *y, cudaStream_t stream);
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m);
 bool gemv_supported(int32_t H, int32_t I);
 moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,

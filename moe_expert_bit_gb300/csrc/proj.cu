@@ -168,3 +168,64 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
   return down_unsort("moe_gather_qmm_down_unsort", h, Wd, Sd, Bd, tiles, topk_weights, H, I,
                      variant, y_acc_ws, y, false, stream);
 }
+
+extern "C" moe_status moe_layer_fused(
+    const int32_t *topk_ids, const float *topk_weights, int32_t T, int32_t k, int32_t E,
+    const moe_bf16_t *x, const uint32_t *Wgu, const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
+    const uint32_t *Wd, const moe_bf16_t *Sd, const moe_bf16_t *Bd, int32_t H, int32_t I,
+    int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids, int32_t *perm, int32_t *counts,
+    int32_t *offsets, int32_t *tiles, int32_t *tile_count, int32_t *status, moe_bf16_t *h,
+    float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream) {
+  const char *fn = "moe_layer_fused";
+  clear_error();
+  if (!topk_ids || !topk_weights || !x || !Wgu || !Sgu || !Bgu || !Wd || !Sd || !Bd ||
+      !sorted_ids || !perm || !counts || !offsets || !tiles || !tile_count || !status || !h ||
+      !y_acc_ws || !y) {
+    set_error("%s: null pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (E < 1 || E > MOE_MAX_EXPERTS) {
+    set_error("%s: num_experts %d outside [1, %d]", fn, E, MOE_MAX_EXPERTS);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (T < 1 || k < 1 || k > E) {
+    set_error("%s: need T >= 1 and 1 <= k <= E (T=%d k=%d E=%d)", fn, T, k, E);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (tile_m != 16 && tile_m != 32 && tile_m != 64 && tile_m != 128 && tile_m != 256) {
+    set_error("%s: tile_m %d not in {16, 32, 64, 128, 256}", fn, tile_m);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t A = (int64_t)T * k;
+  if (A > (1 << 24) || max_tiles < 0 ||
+      (size_t)max_tiles < moe_max_tiles((int32_t)A, E, tile_m)) {
+    set_error("%s: max_tiles %d below the bound for A=%lld E=%d tile_m=%d", fn, max_tiles,
+              (long long)A, E, tile_m);
+    return MOE_ERR_INVALID_ARG;
+  }
+  moe_status st = validate_dims(fn, H, I, MOE_VARIANT_GEMV);
+  if (st != MOE_OK) return st;
+  if ((st = validate_aligned(fn, {x, Wgu, Sgu, Bgu, Wd, Sd, Bd, h, y_acc_ws, y})) != MOE_OK)
+    return st;
+  if (fused_layer_check(T, k, E, H, I, tile_m, max_tiles) != MOE_OK) {
+    set_error("%s: T=%d k=%d H=%d I=%d is beyond the fused kernel (A <= 256, T <= 64, "
+              "padded rows within one copy); use the four calls", fn, T, k, H, I);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return launch_fused_layer(topk_ids, topk_weights, T, k, E, x, Wgu, Sgu, Bgu, Wd, Sd, Bd, H, I,
+                            tile_m, max_tiles, sorted_ids, perm, counts, offsets, tiles,
+                            tile_count, status, h, y_acc_ws, y, stream);
+}
+
+extern "C" moe_status moe_layer_fused_supported(int32_t T, int32_t k, int32_t E, int32_t H,
+                                                int32_t I, int32_t tile_m) {
+  clear_error();
+  if (T < 1 || k < 1 || E < 1 || k > E || H < 64 || I < 64) return MOE_ERR_INVALID_ARG;
+  if (E > MOE_MAX_EXPERTS || H % 64 || I % 64) return MOE_ERR_UNSUPPORTED;
+  if (tile_m != 16 && tile_m != 32 && tile_m != 64 && tile_m != 128 && tile_m != 256)
+    return MOE_ERR_UNSUPPORTED;
+  const int64_t A = (int64_t)T * k;
+  if (A > (1 << 24)) return MOE_ERR_UNSUPPORTED;
+  return fused_layer_check(T, k, E, H, I, tile_m,
+                           (int32_t)moe_max_tiles((int32_t)A, E, tile_m));
+}

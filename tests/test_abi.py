@@ -42,10 +42,10 @@ def test_size_helpers():
     assert mq.moe_max_tiles(32, 128, 64) == 32
     assert mq.moe_max_tiles(64, 8, 32) == 2 + 8
     assert mq.moe_max_tiles(10, 0, 32) == 0
-    # accumulator + one int per 16 columns, padded to 16 bytes
-    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 704
-    assert mq.moe_workspace_bytes(4, 64) == 4 * 64 * 4 + 16
-    assert mq.moe_workspace_bytes(1, 192) == 192 * 4 + 48
+    # accumulator + one int per 16 columns + 4 ints (grid barrier), padded to 16 bytes
+    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 720
+    assert mq.moe_workspace_bytes(4, 64) == 4 * 64 * 4 + 32
+    assert mq.moe_workspace_bytes(1, 192) == 192 * 4 + 64
     assert mq.moe_workspace_bytes(0, 2816) == 0
 
 
@@ -109,3 +109,42 @@ def test_projection_host_validation(tkw, H, I, variant, code):
     assert st == code
     assert _raw().moe_gather_qmm_geglu(NULL, 1, 1, 1, ctypes.byref(_tiles()), 128, 64, 0, 1,
                                        NULL) == mq.MOE_ERR_INVALID_ARG
+
+
+def _fused_args(**kw):
+    a = dict(ids=1, w=1, T=4, k=8, E=128, x=16, Wgu=16, Sgu=16, Bgu=16, Wd=16, Sd=16, Bd=16,
+             H=2816, I=704, tile_m=128, max_tiles=32, sorted=1, perm=1, counts=1, offsets=1,
+             tiles=1, tile_count=1, status=1, h=16, y_acc=16, y=16, stream=NULL)
+    a.update(kw)
+    return tuple(a.values())
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ids=NULL), mq.MOE_ERR_INVALID_ARG),
+    (dict(y=NULL), mq.MOE_ERR_INVALID_ARG),
+    (dict(E=300), mq.MOE_ERR_UNSUPPORTED),
+    (dict(k=200, E=128), mq.MOE_ERR_INVALID_ARG),          # k > E
+    (dict(tile_m=48), mq.MOE_ERR_UNSUPPORTED),
+    (dict(max_tiles=31), mq.MOE_ERR_INVALID_ARG),           # below floor(A/BM) + min(E, A)
+    (dict(H=96), mq.MOE_ERR_UNSUPPORTED),                   # H % 64
+    (dict(x=24), mq.MOE_ERR_INVALID_ARG),                   # misaligned tensor
+    (dict(T=65, k=1, max_tiles=65), mq.MOE_ERR_UNSUPPORTED),  # more token rows than it stages
+    (dict(T=64, k=8, max_tiles=512), mq.MOE_ERR_UNSUPPORTED),  # A = 512 > 256
+    (dict(H=8192, max_tiles=32), mq.MOE_ERR_UNSUPPORTED),   # padded row beyond one copy
+])
+def test_fused_layer_host_validation(kw, code):
+    assert _raw().moe_layer_fused(*_fused_args(**kw)) == code
+    assert _raw().moe_last_error_string()
+
+
+@pytest.mark.parametrize("shape,ok", [
+    ((4, 8, 128, 2816, 704, 128), True),     # decode
+    ((32, 2, 8, 128, 64, 128), True),        # tiny
+    ((32, 8, 16, 512, 320, 32), True),       # A = 256
+    ((33, 8, 16, 512, 320, 32), False),      # A = 264
+    ((64, 4, 128, 2816, 704, 128), False),   # 64 token rows of 2816 do not fit beside the ring
+    ((4, 8, 128, 8192, 704, 128), False),    # a padded row beyond one copy
+])
+def test_fused_layer_supported(shape, ok):
+    assert mq.fused_layer_fits(*shape) is ok
+    assert (_raw().moe_layer_fused_supported(*shape) == mq.MOE_OK) is ok
