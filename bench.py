@@ -289,6 +289,9 @@ def main():
     use_fused = args.variant == "fused" and mq.fused_layer_fits(T, k, E, H, I, args.tile_m)
     if args.variant == "fused" and not use_fused:
         raise SystemExit("the fused layer does not take this workload")
+    # the library's AUTO rule: the weight-streaming GEMV for small tiles, else tensor cores
+    tc_path = variant == mq.VARIANT_TC or (variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
+    use_ws = tc_path and not use_fused
     path = "moe_layer_fused" if use_fused else f"four calls, variant {args.variant}"
 
     def step(ev=None):
@@ -303,7 +306,12 @@ def main():
                                     r.offsets, r.tiles, r.tile_count, r.status, stream)
         if ev is not None:
             ev[0].record(stream)
-        mq.moe_gather_qmm_geglu(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.h, variant, stream)
+        if use_ws:  # the tensor-core variant loads tile rows from the sorted copy of x
+            mq.moe_gather_qmm_geglu_ws(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.x_sorted,
+                                       buf.h, variant, stream)
+        else:
+            mq.moe_gather_qmm_geglu(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.h, variant,
+                                    stream)
         if ev is not None:
             ev[1].record(stream)
         mq.moe_gather_qmm_down_unsort(buf.h, W["Wd"], W["Sd"], W["Bd"], r, tw, H, I, buf.y_acc,
@@ -396,7 +404,7 @@ def main():
     # route (1) + gate/up (1) + down (1) + cast (1 unless fused into the down kernel)
     fused_cast = variant != mq.VARIANT_TC and T * H <= (1 << 20) and not (
         variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
-    launches_per_step = 1 if use_fused else 3 if fused_cast else 4
+    launches_per_step = 1 if use_fused else (3 if fused_cast else 4) + (1 if use_ws else 0)
     line = {
         "metric": "MoE layer assignments/s", "value": world * A / (ms * 1e-3),
         "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

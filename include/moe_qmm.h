@@ -197,6 +197,20 @@ moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu, const 
                                 cudaStream_t stream);
 
 /*
+ * moe_gather_qmm_geglu with a caller workspace: the same arguments and result, plus
+ *   x_sorted_ws [A, H] bf16  caller-owned workspace (A * hidden * 2 bytes; contents
+ *                            on entry irrelevant, overwritten)
+ * The tensor-core variant first gathers the activation rows into sorted-slot order
+ * (x_sorted_ws[s] = x[perm[s] / top_k]), so that the GEMM loads each tile's rows as
+ * contiguous boxes instead of gathering them again for every block of weight rows.  The
+ * weight-streaming variant does not need it and leaves it untouched.
+ */
+moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_t *Wgu, const moe_bf16_t *Sgu,
+                                   const moe_bf16_t *Bgu, const moe_tiles_t *tiles, int32_t hidden,
+                                   int32_t inter, int32_t variant, moe_bf16_t *x_sorted_ws,
+                                   moe_bf16_t *h, cudaStream_t stream);
+
+/*
  * Steps a7-a8 -- gathered 4-bit down projection whose epilogue does the
  * router-weighted scatter-add back into token order (SharpAI/SwiftLM issue
  * #236, "Already on main": weightedExpertSum; Layr-Labs/mlx PR #4,

@@ -35,7 +35,8 @@ MAX_EXPERTS = 256
 ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
                "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc",
-               "moe_sort_and_build_tiles", "moe_layer_fused", "moe_layer_fused_supported")
+               "moe_sort_and_build_tiles", "moe_layer_fused", "moe_layer_fused_supported",
+               "moe_gather_qmm_geglu_ws")
 NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
@@ -89,6 +90,9 @@ def load(build_if_needed: bool = True):
         lib.moe_layer_fused.argtypes = [p, p, i32, i32, i32, p, p, p, p, p, p, p, i32, i32, i32,
                                         i32, p, p, p, p, p, p, p, p, p, p, p]
         lib.moe_layer_fused_supported.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.moe_gather_qmm_geglu_ws.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32,
+                                                i32, p, p, p]
+        lib.moe_gather_qmm_geglu_ws.restype = ctypes.c_int
         lib.moe_layer_fused_supported.restype = ctypes.c_int
         for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_sort_and_build_tiles",
                    "moe_gather_qmm_geglu", "moe_layer_fused",
@@ -210,6 +214,16 @@ def moe_gather_qmm_geglu(x, Wgu, Sgu, Bgu, routing, hidden, inter, h, variant=VA
         _tiles_arg(routing), hidden, inter, variant, _bf16(h, "h"), _stream(stream)))
 
 
+def moe_gather_qmm_geglu_ws(x, Wgu, Sgu, Bgu, routing, hidden, inter, x_sorted_ws, h,
+                            variant=VARIANT_AUTO, stream=None):
+    """moe_gather_qmm_geglu with the [A, hidden] bf16 workspace of the sorted activation
+    rows (used by the tensor-core variant)."""
+    _check(load().moe_gather_qmm_geglu_ws(
+        _bf16(x, "x"), _ptr(Wgu, torch.int32, "Wgu"), _bf16(Sgu, "Sgu"), _bf16(Bgu, "Bgu"),
+        _tiles_arg(routing), hidden, inter, variant,
+        _bf16(x_sorted_ws, "x_sorted_ws", routing.A * hidden), _bf16(h, "h"), _stream(stream)))
+
+
 def moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y_acc_ws, y,
                                variant=VARIANT_AUTO, stream=None):
     _check(load().moe_gather_qmm_down_unsort(
@@ -240,6 +254,16 @@ class MoeLayerBuffers:
                                  device=device)
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.H, self.I = H, I
+        self.device = device
+        self._x_sorted = None
+
+    @property
+    def x_sorted(self):
+        """[A, H] bf16 workspace of the gate/up tensor-core variant (allocated on first use)."""
+        if self._x_sorted is None:
+            self._x_sorted = torch.empty(self.routing.A, self.H, dtype=torch.bfloat16,
+                                         device=self.device)
+        return self._x_sorted
 
 
 def fused_layer_fits(num_tokens, top_k, num_experts, hidden, inter, tile_m=128) -> bool:
@@ -293,8 +317,13 @@ def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, varia
                              stream)
         moe_build_expert_tiles(r.sorted_ids, num_experts, tile_m, r.offsets, r.tiles,
                                r.tile_count, r.status, stream)
-    moe_gather_qmm_geglu(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I, b.h, variant,
-                         stream)
+    if variant == VARIANT_GEMV or (variant == VARIANT_AUTO and
+                                   r.A <= 16 * min(num_experts, r.A)):
+        moe_gather_qmm_geglu(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I, b.h,
+                             variant, stream)
+    else:  # the tensor-core variant loads the tiles' rows from the sorted copy
+        moe_gather_qmm_geglu_ws(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I,
+                                b.x_sorted, b.h, variant, stream)
     moe_gather_qmm_down_unsort(b.h, weights["Wd"], weights["Sd"], weights["Bd"], r, topk_weights,
                                H, I, b.y_acc, b.y, variant, stream)
     return b

@@ -100,6 +100,7 @@ struct Params {
   int32_t N_out;   // I (GEGLU) or H (DOWN)
   int32_t rows_per_expert;  // 2I (GEGLU) or H (DOWN)
   int32_t num_blocks;       // n-blocks per tile: I/64 (GEGLU) or ceil(H/128) (DOWN)
+  int32_t x_sorted;         // GEGLU: x is [A, H] in sorted-slot order (contiguous boxes)
 };
 
 struct Smem {
@@ -299,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int na = n_alloc_of(U.R);
       const int kbps = kMaxN / na;  // k-blocks per stage
       const int nst = (G + kbps - 1) / kbps;
-      if (MODE == GEGLU) {
+      const bool gather = MODE == GEGLU && !p.x_sorted;
+      if (gather) {
         __syncwarp();
         for (int r = lane; r < U.R; r += 32) S.tok[r] = p.perm[U.row0 + r] / p.top_k;
         __syncwarp();
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kb0 = si * kbps;
         const int nk = min(kbps, G - kb0);
         uint8_t *stage = ringB + sb * kBBytes;
-        if (MODE == GEGLU) {
+        if (gather) {
           // gathered rows, four per TMA (one-row boxes); the last group repeats a valid row
           const int ng = (U.R + 3) / 4;
           if (lane == 0) mbar_arrive_expect_tx(&S.b_full[sb], (uint32_t)(nk * ng * 512));
@@ -324,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         S.tok[min(j + 3, U.R - 1)], &S.b_full[sb]);
           }
         } else {
+          // contiguous sorted rows (h, or x gathered into slot order beforehand), 16 per box
           const int nbox = na / 16;
           if (lane == 0) mbar_arrive_expect_tx(&S.b_full[sb], (uint32_t)(nk * na * 128));
           __syncwarp();
@@ -557,6 +560,23 @@ static moe_status launch(const CUtensorMap &mw, const CUtensorMap &mx, const Par
   return check_launch(what);
 }
 
+// x_sorted[s, :] = x[perm[s] / top_k, :], 16 bytes per thread step: the activation rows of
+// every sorted slot made contiguous, so the GEMM loads a tile's rows as plain boxes.
+__global__ void gather_rows_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ perm,
+                                   int32_t top_k, int32_t A, int32_t row_u4,
+                                   uint4 *__restrict__ x_sorted,
+                                   const int32_t *__restrict__ status) {
+  griddep_wait();
+  griddep_launch();
+  if (load_status(status) != 0) return;
+  const int64_t n = (int64_t)A * row_u4;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t s = i / row_u4, c = i - s * row_u4;
+    x_sorted[i] = x[(int64_t)(perm[s] / top_k) * row_u4 + c];
+  }
+}
+
 }  // namespace tc
 
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m) {
@@ -594,6 +614,46 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
   p.N_out = I;
   p.rows_per_expert = 2 * I;
   p.num_blocks = I / 64;
+  return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
+}
+
+moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
+                                  const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
+                                  uint16_t *x_sorted, uint16_t *h, cudaStream_t stream) {
+  const char *what = "moe_gather_qmm_geglu_ws (tensor cores)";
+  const int row_u4 = H / 8;
+  int blocks = (int)(((int64_t)t.num_assignments * row_u4 + 255) / 256);
+  if (blocks > tc::num_sms() * 8) blocks = tc::num_sms() * 8;
+  if (blocks < 1) blocks = 1;
+  launch_pdl(tc::gather_rows_kernel, dim3(blocks), dim3(256), 0, stream,
+             reinterpret_cast<const uint4 *>(x), t.perm, t.top_k, t.num_assignments, row_u4,
+             reinterpret_cast<uint4 *>(x_sorted), (const int32_t *)t.status);
+  moe_status st = check_launch(what);
+  if (st != MOE_OK) return st;
+  CUtensorMap mw, mx;
+  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wgu, H / 8,
+                   (uint64_t)t.num_experts * 2 * I, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_sorted, H, t.num_assignments, 64,
+                   16, CU_TENSOR_MAP_SWIZZLE_128B)) {
+    set_error("%s: tensor map encoding failed", what);
+    return MOE_ERR_CUDA;
+  }
+  tc::Params p;
+  memset(&p, 0, sizeof p);
+  p.tiles = t.tiles;
+  p.tile_count = t.tile_count;
+  p.perm = t.perm;
+  p.status = t.status;
+  p.scales = Sgu;
+  p.biases = Bgu;
+  p.x = x_sorted;
+  p.h = h;
+  p.top_k = t.top_k;
+  p.K = H;
+  p.N_out = I;
+  p.rows_per_expert = 2 * I;
+  p.num_blocks = I / 64;
+  p.x_sorted = 1;
   return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
 }
 

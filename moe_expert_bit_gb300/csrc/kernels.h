@@ -40,6 +40,10 @@ bool gemv_supported(int32_t H, int32_t I);
 moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                            const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
                            uint16_t *h, cudaStream_t stream);
+// GEGLU through a workspace: x gathered into sorted-slot order first ([A, H] bf16)
+moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
+                                  const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
+                                  uint16_t *x_sorted, uint16_t *h, cudaStream_t stream);
 moe_status launch_down_tc(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                           const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                           int32_t H, int32_t I, float *y_acc, cudaStream_t stream);

@@ -120,6 +120,27 @@ extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *
   return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
 }
 
+extern "C" moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_t *Wgu,
+                                              const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
+                                              const moe_tiles_t *tiles, int32_t H, int32_t I,
+                                              int32_t variant, moe_bf16_t *x_sorted_ws,
+                                              moe_bf16_t *h, cudaStream_t stream) {
+  const char *fn = "moe_gather_qmm_geglu_ws";
+  clear_error();
+  moe_status st = validate_tiles(fn, tiles);
+  if (st != MOE_OK) return st;
+  if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
+  if (!x || !Wgu || !Sgu || !Bgu || !x_sorted_ws || !h) {
+    set_error("%s: null pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if ((st = validate_aligned(fn, {x, Wgu, Sgu, Bgu, x_sorted_ws, h})) != MOE_OK) return st;
+  if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
+  if (variant == MOE_VARIANT_TC)
+    return launch_geglu_tc_sorted(x, Wgu, Sgu, Bgu, *tiles, H, I, x_sorted_ws, h, stream);
+  return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
+}
+
 namespace moeqmm {
 
 moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,

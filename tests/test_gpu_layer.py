@@ -172,3 +172,28 @@ def test_gelu_hardware_tanh_against_libm():
     ref = oracle.layer(d)
     assert excess(bf16_to_f64(b.h), ref["h"]) <= 0.5  # well inside the 2e-2 bound
     assert REL == 2e-2
+
+
+@pytest.mark.parametrize("case", ["custom", "prefill_skewed"])
+def test_geglu_workspace_entry_equals_gathering_entry(case):
+    """The tensor-core gate/up through the sorted-row workspace gives h bit for bit as the
+    entry that gathers the rows inside the GEMM (the same B operand reaches the MMAs)."""
+    _variant_or_skip(mq.VARIANT_TC)
+    d = synth.make_custom(3, 256, 192, 300, 2, seed=4) if case == "custom" else synth.make(case)
+    dev = to_device(d)
+    H, I, E = d["H"], d["I"], d["E"]
+    r = mq.Routing(d["T"], d["k"], E, BENCH_TILE_M)
+    mq.moe_sort_and_build_tiles(dev["topk_ids"], E, BENCH_TILE_M, r.sorted_ids, r.perm,
+                                r.counts, r.offsets, r.tiles, r.tile_count, r.status)
+    h0 = torch.empty(r.A, I, dtype=torch.bfloat16, device="cuda")
+    h1 = torch.empty_like(h0)
+    xs = torch.empty(r.A, H, dtype=torch.bfloat16, device="cuda")
+    mq.moe_gather_qmm_geglu(dev["x"], dev["Wgu"], dev["Sgu"], dev["Bgu"], r, H, I, h0,
+                            mq.VARIANT_TC)
+    mq.moe_gather_qmm_geglu_ws(dev["x"], dev["Wgu"], dev["Sgu"], dev["Bgu"], r, H, I, xs, h1,
+                               mq.VARIANT_TC)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    assert torch.equal(h0, h1)
+    perm = r.perm.cpu().numpy()
+    assert torch.equal(xs.cpu(), dev["x"].cpu()[torch.from_numpy(perm // d["k"]).long()])
