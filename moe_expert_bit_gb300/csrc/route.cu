@@ -48,17 +48,20 @@ static int sort_threads(int64_t A) {
   return t < 64 ? 64 : t > kSortThreads ? kSortThreads : (int)t;
 }
 
-// Stable counting sort, one CTA.
-//  pass 1: histogram of expert ids in shared memory (+ range check);
-//  scan:   exclusive prefix over experts -> first slot of each expert;
-//  pass 2: rounds of blockDim consecutive assignments.  Inside a warp,
-//          __match_any_sync groups equal experts and a popcount of the lower
-//          lanes gives each element's rank; per-warp counts are scanned across
-//          the block's warps per expert and added to a running cursor, so slots
-//          follow ascending a within every expert.
+// Stable counting sort, one CTA, two passes over the ids with no block barrier inside a
+// pass.  Warp w owns a contiguous range of the flat indices (ranges ascend with w).
+//  pass 1: each warp counts its range's ids per expert, 32 at a time: __match_any_sync
+//          groups equal experts and the group's lowest lane adds the group size to the
+//          warp's counter of that expert (+ range check);
+//  scan:   per expert, its total over the warps; an exclusive scan over experts gives each
+//          expert's first slot; per expert, the warps' counts are scanned in warp order,
+//          giving each (warp, expert) the first slot of its ids;
+//  pass 2: each warp walks its range again: an id's slot is its (warp, expert) cursor plus
+//          its rank among equal ids of the same 32 (a popcount of the lower lanes), then
+//          the group's lowest lane advances the cursor.
+// Slots therefore follow ascending flat index within every expert.
 struct SortSmem {
   int32_t hist[MOE_MAX_EXPERTS];
-  int32_t cursor[MOE_MAX_EXPERTS];
   int32_t off[MOE_MAX_EXPERTS + 1];  // first slot of each expert (+ A)
   int32_t warp[kSortWarps][MOE_MAX_EXPERTS];
   int32_t sorted[kSmemSorted];  // copy of sorted_ids when A <= kSmemSorted
@@ -70,52 +73,61 @@ struct SortSmem {
 __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t A, int32_t E,
                           int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
                           int32_t *__restrict__ counts, int32_t *__restrict__ status) {
-  int32_t *s_hist = sm.hist, *s_cursor = sm.cursor;
-  int32_t(*s_warp)[MOE_MAX_EXPERTS] = sm.warp;
-  int32_t &s_bad = sm.bad;
+  int32_t(*cnt)[MOE_MAX_EXPERTS] = sm.warp;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nw = nthr >> 5;
+  // this warp's range, in whole rounds of 32
+  const int per = ((A + nw - 1) / nw + 31) & ~31;
+  const int w0 = min(A, warp * per), w1 = min(A, w0 + per);
+  const uint32_t lt_mask = (1u << lane) - 1u;
 
-  for (int e = tid; e < E; e += nthr) s_hist[e] = 0;
-  for (int i = tid; i < nw * MOE_MAX_EXPERTS; i += nthr) (&s_warp[0][0])[i] = 0;
-  if (tid == 0) s_bad = 0;
+  for (int i = tid; i < nw * MOE_MAX_EXPERTS; i += nthr) (&cnt[0][0])[i] = 0;
+  if (tid == 0) sm.bad = 0;
   __syncthreads();
 
-  for (int a = tid; a < A; a += nthr) {
-    int32_t e = ids[a];
-    if (e < 0 || e >= E)
-      s_bad = 1;
-    else
-      atomicAdd(&s_hist[e], 1);
+  bool bad = false;
+  for (int base = w0; base < w1; base += 32) {
+    const int a = base + lane;
+    int32_t e = a < w1 ? ids[a] : -1;
+    if (a < w1 && (e < 0 || e >= E)) {
+      bad = true;
+      e = -2;  // out of range: not counted
+    }
+    const uint32_t same = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (same & lt_mask) == 0) cnt[warp][e] += __popc(same);
   }
+  if (bad) sm.bad = 1;
   __syncthreads();
-  if (s_bad) {
+  if (sm.bad) {
     if (tid == 0) raise_status(status, MOE_ERR_RANGE);
     return false;
   }
-
-  // exclusive scan over E <= 256 experts by warp 0: 8 consecutive experts per lane
-  if (warp == 0) {
+  for (int ex = tid; ex < E; ex += nthr) {  // per-expert totals
+    int32_t t = 0;
+    for (int w = 0; w < nw; ++w) t += cnt[w][ex];
+    sm.hist[ex] = t;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive scan over <= 256 experts, 8 per lane
     int32_t local[8];
     int32_t sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      int e = lane * 8 + i;
-      local[i] = (e < E) ? s_hist[e] : 0;
+      const int e = lane * 8 + i;
+      local[i] = (e < E) ? sm.hist[e] : 0;
       sum += local[i];
     }
     int32_t incl = sum;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-      int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
       if (lane >= d) incl += v;
     }
     int32_t run = incl - sum;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      int e = lane * 8 + i;
+      const int e = lane * 8 + i;
       if (e < E) {
-        s_cursor[e] = run;
         sm.off[e] = run;
         counts[e] = local[i];
       }
@@ -124,38 +136,30 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
     if (lane == 31) sm.off[E] = run;
   }
   __syncthreads();
-
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int base = 0; base < A; base += nthr) {
-    const int a = base + tid;
-    const bool valid = a < A;
+  for (int ex = tid; ex < E; ex += nthr) {  // each (warp, expert): its first slot
+    int32_t run = sm.off[ex];
+    for (int w = 0; w < nw; ++w) {
+      const int32_t c = cnt[w][ex];
+      cnt[w][ex] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int base = w0; base < w1; base += 32) {
+    const int a = base + lane;
+    const bool valid = a < w1;
     const int32_t e = valid ? ids[a] : -1;
     const uint32_t same = __match_any_sync(0xffffffffu, e);
     const int32_t rank = __popc(same & lt_mask);
-    if (valid && rank == 0) s_warp[warp][e] = __popc(same);
-    __syncthreads();
-    for (int ex = tid; ex < E; ex += nthr) {  // per-expert scan over the warps
-      int32_t run = s_cursor[ex];
-      for (int w = 0; w < nw; ++w) {
-        int32_t c = s_warp[w][ex];
-        s_warp[w][ex] = run;
-        run += c;
-      }
-      s_cursor[ex] = run;
-    }
-    __syncthreads();
     if (valid) {
-      const int32_t slot = s_warp[warp][e] + rank;
+      const int32_t slot = cnt[warp][e] + rank;
       sorted_ids[slot] = e;
       perm[slot] = a;
       if (A <= kSmemSorted) sm.sorted[slot] = e;
     }
-    __syncthreads();
-    if (base + nthr < A) {
-      for (int ex = tid; ex < E; ex += nthr)
-        for (int w = 0; w < nw; ++w) s_warp[w][ex] = 0;
-      __syncthreads();
-    }
+    __syncwarp();
+    if (valid && rank == 0) cnt[warp][e] += __popc(same);
+    __syncwarp();
   }
   return true;
 }
