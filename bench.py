@@ -239,6 +239,8 @@ def main():
                     help="auto: the four calls with the library's own variant choice; "
                          "fused: the one-launch layer (decode-sized calls)")
     ap.add_argument("--tile-m", type=int, default=128)
+    ap.add_argument("--deterministic", action="store_true",
+                    help="the fixed-order un-sort (per-assignment rows, ordered k-sum)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-slots", type=int, default=0)
@@ -272,7 +274,8 @@ def main():
     x = x_h.to(dev)
     ids = ids_h.to(dev)
     tw = tw_h.to(dev)
-    buf = mq.MoeLayerBuffers(T, k, E, H, I, args.tile_m, device=dev)
+    buf = mq.MoeLayerBuffers(T, k, E, H, I, args.tile_m, device=dev,
+                             deterministic=args.deterministic)
     y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     evict = torch.ones(L2_FLUSH_BYTES // 8, dtype=torch.float32, device=dev)
@@ -315,7 +318,7 @@ def main():
         if ev is not None:
             ev[1].record(stream)
         mq.moe_gather_qmm_down_unsort(buf.h, W["Wd"], W["Sd"], W["Bd"], r, tw, H, I, buf.y_acc,
-                                      buf.y, variant, stream)
+                                      buf.y, variant, stream, args.deterministic)
         if ev is not None:
             ev[2].record(stream)
 
@@ -401,8 +404,9 @@ def main():
         geglu_avg = sum(route_ms) / len(route_ms)
         geglu_bytes = w_bytes + T * H * 2 + 2 * A * I * 2 + T * H * 2
     achieved = geglu_bytes / (geglu_avg * 1e-3) / 1e9
-    # route (1) + gate/up (1) + down (1) + cast (1 unless fused into the down kernel)
-    fused_cast = variant != mq.VARIANT_TC and T * H <= (1 << 20) and not (
+    # route (1) + gate/up (1) + down (1) + cast or ordered sum (1 unless in the down kernel)
+    acc_rows = A if args.deterministic else T  # the library's rule for the in-kernel cast
+    fused_cast = variant != mq.VARIANT_TC and acc_rows * H <= (1 << 20) and not (
         variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
     launches_per_step = 1 if use_fused else (3 if fused_cast else 4) + (1 if use_ws else 0)
     line = {
@@ -413,6 +417,8 @@ def main():
         "config": {"workload": workload_name(args.config, cfg), "assignments": A,
                    "experts_touched": touched, "tile_m": args.tile_m, "variant": args.variant,
                    "path": path,
+                   "unsort": "deterministic (per-assignment rows, fixed-order k-sum)"
+                             if args.deterministic else "fp32 atomics",
                    "l2": "flushed between steps outside the timed events: 512 MB write, "
                          "then 256 MB read (the flush's dirty lines written back)",
                    "parallelism": f"{world} independent replica(s), no collective"},

@@ -123,6 +123,16 @@ size_t moe_max_tiles(int32_t num_assignments, int32_t num_experts, int32_t tile_
 size_t moe_workspace_bytes(int32_t num_tokens, int32_t hidden);
 
 /*
+ * Bytes of workspace for the down projection's un-sort in either mode:
+ *   deterministic == 0: moe_workspace_bytes(T, H) (the shared [T, H] accumulator);
+ *   deterministic != 0: moe_workspace_bytes(T * k, H) -- one fp32 row per assignment
+ *                       ([A, H]) followed by the same counters.
+ * 0 for invalid sizes.
+ */
+size_t moe_unsort_workspace_bytes(int32_t num_tokens, int32_t top_k, int32_t hidden,
+                                  int32_t deterministic);
+
+/*
  * Step a1 -- flatten and stable-sort the assignments by expert
  * (Layr-Labs/mlx PR #4, "What": the gathered QMM reads contiguous sorted
  * indices).
@@ -219,26 +229,39 @@ moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_t *Wgu, con
  *   Wd  [E, H, I/8]  uint32 packed 4-bit down weights
  *   Sd, Bd [E, H, I/64] bf16
  *   topk_weights [T, k] fp32 router weights
- *   y_acc_ws [T, H]  fp32   caller-owned workspace of moe_workspace_bytes(T, H)
- *                           bytes, all zero on entry: clear it once after
- *                           allocating.  A call that completes leaves its
- *                           accumulator and counters zero again (no memset per
- *                           call; moe_layer_fused also keeps a grid-barrier
- *                           generation word after them, any value of which is
- *                           valid); after a call that set the status word, clear
- *                           it before reusing it.
+ *   y_acc_ws         fp32   caller-owned workspace of
+ *                           moe_unsort_workspace_bytes(T, k, H, deterministic)
+ *                           bytes whose counters are zero on entry: clear the
+ *                           whole workspace once after allocating.  A call that
+ *                           completes leaves the counters (and, when not
+ *                           deterministic, the accumulator) zero again, so no
+ *                           memset is needed per call; moe_layer_fused also keeps
+ *                           a grid-barrier generation word after them, any value
+ *                           of which is valid.  After a call that set the status
+ *                           word, clear it before reusing it.
+ *   deterministic    0 or 1 (else MOE_ERR_INVALID_ARG)
  *   y   [T, H]       bf16   out: y[t] = sum_j topk_weights[t, j] * (Wd[e] . h[s]),
  *                           s the slot of a = t*k + j, e = sorted_ids[s]
- * The k terms of a token are added with fp32 atomics, so the order of the
- * additions (and the last bits of y) may differ from run to run.  Tokens
- * whose weights are all zero get y = 0 exactly.  Requires H % 64 == 0 and
- * I % 64 == 0.  Does nothing if *status != 0.
+ * deterministic == 0: the k terms of a token are added into a shared [T, H]
+ * accumulator with fp32 atomics, so the order of the additions (and the last
+ * bits of y) may differ from run to run.
+ * deterministic == 1: each assignment's weighted row o[a] = topk_weights[a] *
+ * (Wd[e] . h[s]) is stored in row a of an [A, H] workspace, and then
+ * y[t] = bf16(o[t*k] + o[t*k + 1] + ... + o[t*k + k - 1]), added left to right
+ * in fp32 (the rows stay in the workspace after the call, so clear a workspace
+ * before handing it to the other mode).  Two calls with the same inputs,
+ * variant and sizes then give bit-identical y (Layr-Labs/mlx PR #4, the final
+ * merge-readiness pass: an exact output-invariance gate).  The two variants
+ * may still differ from each other in the last bits.
+ * Tokens whose weights are all zero get y = 0 exactly.  Requires H % 64 == 0
+ * and I % 64 == 0.  Does nothing if *status != 0.
  */
 moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
                                       const moe_bf16_t *Sd, const moe_bf16_t *Bd,
                                       const moe_tiles_t *tiles, const float *topk_weights,
                                       int32_t hidden, int32_t inter, int32_t variant,
-                                      float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream);
+                                      float *y_acc_ws, int32_t deterministic, moe_bf16_t *y,
+                                      cudaStream_t stream);
 
 /*
  * Variant of moe_gather_qmm_down_unsort that allocates nothing and takes no
@@ -250,22 +273,23 @@ moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
  *   The fp32 accumulator is a fixed array of MOE_NOALLOC_MAX_Y_ELEMENTS floats
  *   (16 MiB) of device memory inside the library, which every GPU that loads
  *   the library holds until the process exits.  A workspace of
- *   moe_workspace_bytes(T, H) above that maximum returns MOE_ERR_UNSUPPORTED
- *   before any launch.
+ *   moe_unsort_workspace_bytes(T, k, H, deterministic) above that maximum
+ *   returns MOE_ERR_UNSUPPORTED before any launch.
  *   The first call on a device looks up the array's device address (once per
  *   device, with that device current); make that first call before any
  *   stream capture.
  *   Every call on a device shares the one array: it is cleared at the start
- *   of each call, and calls that overlap on the GPU (two streams, or two host
- *   threads) race on it -- serialise them.
+ *   of each call (deterministic: its counters), and calls that overlap on the
+ *   GPU (two streams, or two host threads) race on it -- serialise them.
  * No cudaMalloc, cudaFree or allocating library routine is called.
  */
-#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304 /* floats; moe_workspace_bytes(T, H) / 4 must not exceed it */
+#define MOE_NOALLOC_MAX_Y_ELEMENTS 4194304 /* floats; the workspace size / 4 must not exceed it */
 moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_t *Wd,
                                               const moe_bf16_t *Sd, const moe_bf16_t *Bd,
                                               const moe_tiles_t *tiles, const float *topk_weights,
                                               int32_t hidden, int32_t inter, int32_t variant,
-                                              moe_bf16_t *y, cudaStream_t stream);
+                                              int32_t deterministic, moe_bf16_t *y,
+                                              cudaStream_t stream);
 
 /*
  * The whole layer of a decode-sized call in ONE launch (steps a1-a8 with the GEMV-style
@@ -281,7 +305,9 @@ moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_
  *   counts [E], offsets [E+1], tiles [max_tiles*3], tile_count [1]), tile_m and max_tiles
  *   as there; status: the device status word;
  *   h [A, I] bf16 out (sorted-slot order); y_acc_ws: a workspace of
- *   moe_workspace_bytes(T, H) bytes, zero on entry and left zero; y [T, H] bf16 out.
+ *   moe_unsort_workspace_bytes(T, k, H, deterministic) bytes, zero on entry and left zero
+ *   (deterministic: its counters), as for moe_gather_qmm_down_unsort; deterministic: 0 or 1,
+ *   the un-sort mode of moe_gather_qmm_down_unsort; y [T, H] bf16 out.
  * Limits: A = T*k <= 256, T <= 64, H and I multiples of 64 whose padded packed rows fit one
  * copy (K/2 + padding <= 2048 bytes); other calls return MOE_ERR_UNSUPPORTED before any
  * launch (use the four calls).  The launch is cooperative (one CTA per SM, all resident at
@@ -295,7 +321,8 @@ moe_status moe_layer_fused(const int32_t *topk_ids, const float *topk_weights, i
                            int32_t hidden, int32_t inter, int32_t tile_m, int32_t max_tiles,
                            int32_t *sorted_ids, int32_t *perm, int32_t *counts, int32_t *offsets,
                            int32_t *tiles, int32_t *tile_count, int32_t *status, moe_bf16_t *h,
-                           float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream);
+                           float *y_acc_ws, int32_t deterministic, moe_bf16_t *y,
+                           cudaStream_t stream);
 
 /*
  * MOE_OK if moe_layer_fused takes a call of this shape (T tokens, top-k, E experts, hidden,

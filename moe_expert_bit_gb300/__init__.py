@@ -36,7 +36,7 @@ ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
                "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc",
                "moe_sort_and_build_tiles", "moe_layer_fused", "moe_layer_fused_supported",
-               "moe_gather_qmm_geglu_ws")
+               "moe_gather_qmm_geglu_ws", "moe_unsort_workspace_bytes")
 NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
@@ -77,6 +77,8 @@ def load(build_if_needed: bool = True):
         lib.moe_max_tiles.restype = ctypes.c_size_t
         lib.moe_workspace_bytes.argtypes = [i32, i32]
         lib.moe_workspace_bytes.restype = ctypes.c_size_t
+        lib.moe_unsort_workspace_bytes.argtypes = [i32, i32, i32, i32]
+        lib.moe_unsort_workspace_bytes.restype = ctypes.c_size_t
         lib.moe_sort_assignments.argtypes = [p, i32, i32, i32, p, p, p, p, p]
         lib.moe_build_expert_tiles.argtypes = [p, i32, i32, i32, i32, p, p, p, p, p]
         lib.moe_sort_and_build_tiles.argtypes = [p, i32, i32, i32, i32, i32, p, p, p, p, p, p,
@@ -84,11 +86,11 @@ def load(build_if_needed: bool = True):
         lib.moe_gather_qmm_geglu.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32, i32,
                                              p, p]
         lib.moe_gather_qmm_down_unsort.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), p, i32,
-                                                   i32, i32, p, p, p]
+                                                   i32, i32, p, i32, p, p]
         lib.moe_gather_qmm_down_unsort_noalloc.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles),
-                                                           p, i32, i32, i32, p, p]
+                                                           p, i32, i32, i32, i32, p, p]
         lib.moe_layer_fused.argtypes = [p, p, i32, i32, i32, p, p, p, p, p, p, p, i32, i32, i32,
-                                        i32, p, p, p, p, p, p, p, p, p, p, p]
+                                        i32, p, p, p, p, p, p, p, p, p, i32, p, p]
         lib.moe_layer_fused_supported.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.moe_gather_qmm_geglu_ws.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32,
                                                 i32, p, p, p]
@@ -138,6 +140,14 @@ def moe_max_tiles(num_assignments: int, num_experts: int, tile_m: int) -> int:
 
 def moe_workspace_bytes(num_tokens: int, hidden: int) -> int:
     return int(load().moe_workspace_bytes(num_tokens, hidden))
+
+
+def moe_unsort_workspace_bytes(num_tokens: int, top_k: int, hidden: int,
+                               deterministic: bool = False) -> int:
+    """Workspace bytes of the down call: [T, H] fp32 + counters, or [T*k, H] when
+    deterministic."""
+    return int(load().moe_unsort_workspace_bytes(num_tokens, top_k, hidden,
+                                                 1 if deterministic else 0))
 
 
 def moe_sort_assignments(topk_ids, num_experts, sorted_ids, perm, counts, status, stream=None):
@@ -225,33 +235,38 @@ def moe_gather_qmm_geglu_ws(x, Wgu, Sgu, Bgu, routing, hidden, inter, x_sorted_w
 
 
 def moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y_acc_ws, y,
-                               variant=VARIANT_AUTO, stream=None):
+                               variant=VARIANT_AUTO, stream=None, deterministic=False):
+    """deterministic: y_acc_ws holds one fp32 row per assignment and y is the fixed-order sum
+    of each token's k rows (bit-identical from run to run)."""
     _check(load().moe_gather_qmm_down_unsort(
         _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
         _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
-        variant, _ptr(y_acc_ws, torch.float32, "y_acc_ws"), _bf16(y, "y"), _stream(stream)))
+        variant, _ptr(y_acc_ws, torch.float32, "y_acc_ws"), 1 if deterministic else 0,
+        _bf16(y, "y"), _stream(stream)))
 
 
 def moe_gather_qmm_down_unsort_noalloc(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y,
-                                       variant=VARIANT_AUTO, stream=None):
+                                       variant=VARIANT_AUTO, stream=None, deterministic=False):
     """moe_gather_qmm_down_unsort without a workspace argument: for callers that cannot
     allocate device memory.  The accumulator is the library's built-in fixed array
     (T * hidden <= NOALLOC_MAX_Y_ELEMENTS); calls that overlap on the GPU race on it."""
     _check(load().moe_gather_qmm_down_unsort_noalloc(
         _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
         _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
-        variant, _bf16(y, "y"), _stream(stream)))
+        variant, 1 if deterministic else 0, _bf16(y, "y"), _stream(stream)))
 
 
 class MoeLayerBuffers:
     """Every device buffer one layer call writes, allocated once and reused."""
 
-    def __init__(self, T, k, E, H, I, tile_m, device="cuda"):
+    def __init__(self, T, k, E, H, I, tile_m, device="cuda", deterministic=False):
         self.routing = Routing(T, k, E, tile_m, device)
         self.h = torch.empty(T * k, I, dtype=torch.bfloat16, device=device)
-        # the down call needs a zeroed workspace and leaves it zeroed
-        self.y_acc = torch.zeros((moe_workspace_bytes(T, H) + 3) // 4, dtype=torch.float32,
-                                 device=device)
+        # the down call needs a zeroed workspace and leaves it zeroed (deterministic: one
+        # row per assignment, overwritten by every call; its counters are left zeroed)
+        self.deterministic = bool(deterministic)
+        self.y_acc = torch.zeros((moe_unsort_workspace_bytes(T, k, H, deterministic) + 3) // 4,
+                                 dtype=torch.float32, device=device)
         self.y = torch.empty(T, H, dtype=torch.bfloat16, device=device)
         self.H, self.I = H, I
         self.device = device
@@ -292,18 +307,23 @@ def moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, buffers, st
         _ptr(r.tiles, torch.int32, "tiles", 3 * r.max_tiles),
         _ptr(r.tile_count, torch.int32, "tile_count", 1), _ptr(r.status, torch.int32, "status", 1),
         _bf16(buffers.h, "h"), _ptr(buffers.y_acc, torch.float32, "y_acc_ws"),
-        _bf16(buffers.y, "y"), _stream(stream)))
+        1 if buffers.deterministic else 0, _bf16(buffers.y, "y"), _stream(stream)))
 
 
 def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, variant=VARIANT_AUTO,
-              buffers=None, stream=None, fused_route=False, fused=False):
+              buffers=None, stream=None, fused_route=False, fused=False, deterministic=None):
     """Run the four calls on one stream (fused: the one-launch layer).  ``weights``: dict of
     Wgu, Sgu, Bgu, Wd, Sd, Bd device tensors (uint32 data as int32, bf16 scales/biases).
-    Returns the buffers."""
+    deterministic: the fixed-order un-sort (default: the mode the buffers were made for,
+    else False).  Returns the buffers."""
     T, k = topk_ids.shape
     H = x.shape[1]
     I = weights["Wd"].shape[2] * 8
-    b = buffers or MoeLayerBuffers(T, k, num_experts, H, I, tile_m, device=x.device)
+    if buffers is not None and deterministic is not None and \
+            bool(deterministic) != buffers.deterministic:
+        raise MoeError(MOE_ERR_INVALID_ARG, "buffers were allocated for the other un-sort mode")
+    b = buffers or MoeLayerBuffers(T, k, num_experts, H, I, tile_m, device=x.device,
+                                   deterministic=bool(deterministic))
     r = b.routing
     r.status.zero_()
     if fused:
@@ -325,5 +345,5 @@ def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, varia
         moe_gather_qmm_geglu_ws(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I,
                                 b.x_sorted, b.h, variant, stream)
     moe_gather_qmm_down_unsort(b.h, weights["Wd"], weights["Sd"], weights["Bd"], r, topk_weights,
-                               H, I, b.y_acc, b.y, variant, stream)
+                               H, I, b.y_acc, b.y, variant, stream, b.deterministic)
     return b

@@ -10,7 +10,8 @@
 //      writes the routing state out for the caller);
 //   2. gate/up + GeGLU exactly as the per-call GEMV (split-K teams, h to global memory);
 //   3. a grid barrier (the launch is cooperative, so every CTA is resident): h is complete;
-//   4. down + un-sort, reading h from L2, with the per-column-block cast.
+//   4. down + un-sort, reading h from L2, with the per-column-block cast (deterministic: one
+//      stored row per assignment, and the per-column-block sum of a token's k rows in order).
 // The producer warp is not held by the barrier: the ring is one stream of gate/up chunks
 // followed by down chunks, so the down weights flow into the buffers the last gate/up
 // chunks release while the grid waits for its slowest CTA.
@@ -114,6 +115,7 @@ __device__ __forceinline__ bool grid_barrier(int32_t *gbar, int32_t gen,
   return true;
 }
 
+template <bool DET>
 __global__ void __launch_bounds__(kFThreads, 1)
     fused_layer_kernel(const __grid_constant__ CUtensorMap tmap_gu,
                        const __grid_constant__ CUtensorMap tmap_d, const FArgs p) {
@@ -585,7 +587,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
           if (!ok) continue;
           if (flt_blk >= 0) {  // the count issued one chunk ago
             const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-            if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
+            if (old + flt_rows == p.A)
+              finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, flt_blk, lane);
             flt_blk = -1;
           }
           if (pend_blk >= 0) {  // count the previous chunk's reductions
@@ -601,9 +604,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             if (2 * t + c >= Rp) continue;
-            float *yrow = p.y_acc + (int64_t)(a_c[c] / p.k) * p.H + kFDownRows * j + row_lo;
-            atomicAdd(yrow + gq, w_c[c] * acc[c]);
-            atomicAdd(yrow + gq + 8, w_c[c] * acc[2 + c]);
+            if (DET) {  // this assignment's own row of the workspace
+              float *orow = p.y_acc + (int64_t)a_c[c] * p.H + kFDownRows * j + row_lo;
+              __stcg(orow + gq, w_c[c] * acc[c]);
+              __stcg(orow + gq + 8, w_c[c] * acc[2 + c]);
+            } else {
+              float *yrow = p.y_acc + (int64_t)(a_c[c] / p.k) * p.H + kFDownRows * j + row_lo;
+              atomicAdd(yrow + gq, w_c[c] * acc[c]);
+              atomicAdd(yrow + gq + 8, w_c[c] * acc[2 + c]);
+            }
           }
           pend_blk = (kFDownRows * j + row_lo) / 16;
           pend_rows = Rp;
@@ -615,7 +624,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
     if (ok) {  // drain the count pipeline
       if (flt_blk >= 0) {
         const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-        if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
+        if (old + flt_rows == p.A)
+          finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, flt_blk, lane);
       }
       if (pend_blk >= 0) {
         __syncwarp();
@@ -624,7 +634,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
           flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
         }
         const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-        if (old + pend_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, pend_blk, lane);
+        if (old + pend_rows == p.A)
+          finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, pend_blk, lane);
       }
     }
     if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
@@ -669,7 +680,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
                               int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
                               int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
                               int32_t *tile_count, int32_t *status, uint16_t *h, float *y_acc,
-                              uint16_t *y, cudaStream_t stream) {
+                              bool det, uint16_t *y, cudaStream_t stream) {
   const char *what = "moe_layer_fused";
   const int A = T * k;
   const int nbuf = fused_nbuf(H, I, T, A, E, max_tiles);
@@ -682,7 +693,9 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
     set_error("%s: cuTensorMapEncodeTiled failed for a weight tensor", what);
     return MOE_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute((const void *)fused_layer_kernel,
+  void (*kern)(const CUtensorMap, const CUtensorMap, const FArgs) =
+      det ? fused_layer_kernel<true> : fused_layer_kernel<false>;
+  if (cudaFuncSetAttribute((const void *)kern,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
     return check_launch(what);
   FArgs a;
@@ -711,7 +724,8 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   a.status = status;
   a.h = h;
   a.y_acc = y_acc;
-  a.cnt = reinterpret_cast<int32_t *>(y_acc + (int64_t)T * H);
+  // counters after the accumulator: T x H, or A x H per-assignment rows when deterministic
+  a.cnt = reinterpret_cast<int32_t *>(y_acc + (int64_t)(det ? A : T) * H);
   a.gbar = a.cnt + H / 16;
   a.y = y;
   // cooperative: every CTA resident at once (the grid barrier waits for all of them)
@@ -725,7 +739,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, fused_layer_kernel, mgu, md, a);
+  cudaLaunchKernelEx(&cfg, kern, mgu, md, a);
   return check_launch(what);
 }
 

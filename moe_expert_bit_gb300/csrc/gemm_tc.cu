@@ -7,7 +7,9 @@
 //          (SharpAI/SwiftLM issue #236, "Still missing": the GeGLU product fused
 //          into one dispatch; here it is the GEMM epilogue)
 //   DOWN:  y_acc[t_s, n] += w_s * sum_i Wd[e][n][i] h[s][i]
-//          (weightedExpertSum / direct weighted un-sort as the GEMM epilogue)
+//          (weightedExpertSum / direct weighted un-sort as the GEMM epilogue;
+//          per-slot mode stores o[a_s, n] = w_s * sum_i ... instead, for the
+//          deterministic un-sort that adds a token's k rows in a fixed order)
 //
 // The weights are the MMA's M side ("swap AB"): a work unit is one expert
 // tile (<= 128 token rows, the MMA's N rounded up to 16) times one n-block of
@@ -101,6 +103,7 @@ struct Params {
   int32_t rows_per_expert;  // 2I (GEGLU) or H (DOWN)
   int32_t num_blocks;       // n-blocks per tile: I/64 (GEGLU) or ceil(H/128) (DOWN)
   int32_t x_sorted;         // GEGLU: x is [A, H] in sorted-slot order (contiguous boxes)
+  int32_t per_slot;         // DOWN: y_acc is [A, H], one row per assignment, stored (not added)
 };
 
 struct Smem {
@@ -427,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float w = 0.f;
           if (c0 + lane < U.R) {
             const int a = p.perm[U.row0 + c0 + lane];
-            tok = a / p.top_k;
+            tok = p.per_slot ? a : a / p.top_k;
             w = p.topk_weights[a];
           }
           // transpose through shared memory: [column][32 rows]
@@ -442,9 +445,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float4 f = *reinterpret_cast<const float4 *>(scratch + j * 32 + 4 * m);
             const int tj = __shfl_sync(0xffffffffu, tok, j);
             const float wj = __shfl_sync(0xffffffffu, w, j);
-            if (c0 + j < U.R && n < p.N_out)
-              red_add_v4(p.y_acc + (int64_t)tj * p.N_out + n, wj * f.x, wj * f.y, wj * f.z,
-                         wj * f.w);
+            if (c0 + j < U.R && n < p.N_out) {
+              float *dst = p.y_acc + (int64_t)tj * p.N_out + n;
+              if (p.per_slot)
+                __stcg(reinterpret_cast<float4 *>(dst),
+                       make_float4(wj * f.x, wj * f.y, wj * f.z, wj * f.w));
+              else
+                red_add_v4(dst, wj * f.x, wj * f.y, wj * f.z, wj * f.w);
+            }
           }
           __syncwarp();
         }
@@ -659,7 +667,8 @@ moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const 
 
 moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
                           const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
-                          int32_t H, int32_t I, float *y_acc, cudaStream_t stream) {
+                          int32_t H, int32_t I, float *y_acc, bool per_slot,
+                          cudaStream_t stream) {
   const char *what = "moe_gather_qmm_down_unsort (tensor cores)";
   CUtensorMap mw, mx;
   if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wd, I / 8,
@@ -679,6 +688,7 @@ moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_
   p.biases = Bd;
   p.topk_weights = topk_weights;
   p.y_acc = y_acc;
+  p.per_slot = per_slot ? 1 : 0;
   p.top_k = t.top_k;
   p.K = I;
   p.N_out = H;

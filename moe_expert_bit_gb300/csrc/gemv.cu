@@ -5,6 +5,8 @@
 //
 //   gate/up:  h[s, n] = gelu_tanh(sum_k Wg[e][n][k] x_s[k]) * sum_k Wu[e][n][k] x_s[k]
 //   down:     y_acc[t, n] += w_a * sum_i Wd[e][n][i] h[s, i],  a = perm[s], t = a / top_k
+//             (deterministic: o[a, n] = w_a * sum_i ..., then y[t] = o[t k] + ... + o[t k + k - 1]
+//             in that order)
 // with w = scale * q + bias per 64-group (Layr-Labs/mlx PR #4, "What";
 // SharpAI/SwiftLM issue #236, "Still missing" and "Already on main").
 //
@@ -59,7 +61,7 @@ namespace moeqmm {
 // DOWN with a fused cast: the leader warp of each (tile, pass, chunk j) adds the pass's
 // row count to counter j (one per 16 output columns, zeroed with y_acc); the warp whose
 // addition reaches A has seen every contribution to those columns and writes them to y
-// as bf16.
+// as bf16 (deterministic: sums the k per-assignment rows of each token in order j = 0..k-1).
 constexpr int kSplitKTeam = 4;  // gate/up: warps sharing one 16-row chunk
 
 template <int MODE>
@@ -117,7 +119,7 @@ struct GemvArgs {
   uint16_t *y;
 };
 
-template <int MODE>
+template <int MODE, bool DET>
 __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
     gemv_persist_kernel(const __grid_constant__ CUtensorMap tmap_w, const GemvArgs p) {
   using namespace umma;
@@ -419,7 +421,8 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
         if (MODE == 1 && p.cnt) {
           if (flt_blk >= 0) {  // the count issued one chunk ago
             const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-            if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
+            if (old + flt_rows == p.A)
+              finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.top_k, p.H, flt_blk, lane);
             flt_blk = -1;
           }
           if (pend_blk >= 0) {  // count the previous chunk's reductions
@@ -441,6 +444,10 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
             const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
             p.h[(int64_t)(row0 + r0 + jr) * p.I + n] =
                 __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
+          } else if (DET) {  // this assignment's own row of the workspace
+            float *orow = p.y_acc + (int64_t)a_c[c] * p.H + Cfg::kRows * j + row_lo;
+            __stcg(orow + gq, w_c[c] * acc[c]);
+            __stcg(orow + gq + 8, w_c[c] * acc[2 + c]);
           } else {
             float *yrow = p.y_acc + (int64_t)(a_c[c] / p.top_k) * p.H + Cfg::kRows * j + row_lo;
             atomicAdd(yrow + gq, w_c[c] * acc[c]);
@@ -461,7 +468,8 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
   if (MODE == 1 && p.cnt && ok) {  // drain the count pipeline
     if (flt_blk >= 0) {
       const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-      if (old + flt_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, flt_blk, lane);
+      if (old + flt_rows == p.A)
+        finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.top_k, p.H, flt_blk, lane);
     }
     if (pend_blk >= 0) {
       __syncwarp();
@@ -470,7 +478,8 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
         flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
       }
       const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-      if (old + pend_rows == p.A) cast_block(p.y_acc, p.y, p.cnt, p.T, p.H, pend_blk, lane);
+      if (old + pend_rows == p.A)
+        finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.top_k, p.H, pend_blk, lane);
     }
   }
   if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
@@ -491,6 +500,33 @@ __global__ void cast_bf16_kernel(float *__restrict__ y_acc, uint16_t *__restrict
     o.x = *reinterpret_cast<uint32_t *>(&lo);
     o.y = *reinterpret_cast<uint32_t *>(&hi);
     reinterpret_cast<uint2 *>(y)[i] = o;
+  }
+}
+
+// Deterministic un-sort as its own pass: y[t, c..c+3] = bf16(sum_j o[t k + j, c..c+3]), the k
+// rows of a token added in order j = 0, 1, ..., k - 1 (fp32), four columns per thread step.
+__global__ void slot_sum_kernel(const float *__restrict__ o, uint16_t *__restrict__ y, int64_t n4,
+                                int32_t k, int32_t H4, const int32_t *__restrict__ status) {
+  if (load_status(status) != 0) return;
+  const float4 *o4 = reinterpret_cast<const float4 *>(o);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / H4;
+    const float4 *src = o4 + t * k * H4 + (i - t * H4);
+    float4 v = __ldcs(src);
+    for (int j = 1; j < k; ++j) {
+      const float4 u = __ldcs(src + (int64_t)j * H4);
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+    uint2 r;
+    r.x = *reinterpret_cast<uint32_t *>(&lo);
+    r.y = *reinterpret_cast<uint32_t *>(&hi);
+    reinterpret_cast<uint2 *>(y)[i] = r;
   }
 }
 
@@ -533,7 +569,7 @@ bool gemv_supported(int32_t H, int32_t I) {
   return pick_nbuf<0>(H, 4, 0) >= 2 && pick_nbuf<1>(I, 4, 0) >= 2;
 }
 
-template <int MODE>
+template <int MODE, bool DET>
 static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const uint16_t *Sc,
                                  const uint16_t *Bi, const moe_tiles_t &t, const float *tw,
                                  int32_t H, int32_t I, uint16_t *h, float *y_acc, uint16_t *y,
@@ -583,7 +619,7 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
     set_error("%s: cuTensorMapEncodeTiled failed for the weight tensor", what);
     return MOE_ERR_CUDA;
   }
-  if (cudaFuncSetAttribute((const void *)gemv_persist_kernel<MODE>,
+  if (cudaFuncSetAttribute((const void *)gemv_persist_kernel<MODE, DET>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, L.total) != cudaSuccess)
     return check_launch(what);
   const int64_t max_chunks = (int64_t)t.max_tiles * (MODE == 0 ? I / 8 : H / Cfg::kRows);
@@ -609,26 +645,33 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   a.whole = whole;
   a.h = h;
   a.y_acc = y_acc;
-  // the column-block counters follow the T x H accumulator in the workspace
-  a.cnt = (MODE == 1 && fused_cast) ? reinterpret_cast<int32_t *>(y_acc + (int64_t)T * H) : nullptr;
+  // the column-block counters follow the accumulator in the workspace: T x H, or one row
+  // per assignment (A x H) when deterministic
+  a.cnt = (MODE == 1 && fused_cast)
+              ? reinterpret_cast<int32_t *>(y_acc + (int64_t)(DET ? A : T) * H)
+              : nullptr;
   a.y = y;
-  launch_pdl(gemv_persist_kernel<MODE>, dim3(grid), dim3((nwc + 2) * 32), L.total, stream, tmap, a);
+  launch_pdl(gemv_persist_kernel<MODE, DET>, dim3(grid), dim3((nwc + 2) * 32), L.total, stream, tmap, a);
   return check_launch(what);
 }
 
 moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
                              uint16_t *h, cudaStream_t stream) {
-  return launch_persist<0>(x, Wgu, Sgu, Bgu, t, nullptr, H, I, h, nullptr, nullptr, false,
-                           stream, "moe_gather_qmm_geglu (gemv)");
+  return launch_persist<0, false>(x, Wgu, Sgu, Bgu, t, nullptr, H, I, h, nullptr, nullptr,
+                                  false, stream, "moe_gather_qmm_geglu (gemv)");
 }
 
 moe_status launch_down_gemv(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                             int32_t H, int32_t I, float *y_acc, uint16_t *y, bool fused_cast,
-                            cudaStream_t stream) {
-  return launch_persist<1>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y, fused_cast,
-                           stream, "moe_gather_qmm_down_unsort (gemv)");
+                            bool det, cudaStream_t stream) {
+  const char *what = "moe_gather_qmm_down_unsort (gemv)";
+  if (det)
+    return launch_persist<1, true>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y,
+                                   fused_cast, stream, what);
+  return launch_persist<1, false>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y,
+                                  fused_cast, stream, what);
 }
 
 moe_status launch_cast_bf16(float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
@@ -639,6 +682,16 @@ moe_status launch_cast_bf16(float *y_acc, uint16_t *y, int64_t n, const int32_t 
   if (blocks < 1) blocks = 1;
   cast_bf16_kernel<<<blocks, 256, 0, stream>>>(y_acc, y, n4, status);
   return check_launch("moe_gather_qmm_down_unsort (cast)");
+}
+
+moe_status launch_slot_sum(const float *o, uint16_t *y, int32_t T, int32_t k, int32_t H,
+                           const int32_t *status, cudaStream_t stream) {
+  const int64_t n4 = (int64_t)T * H / 4;  // H % 64 == 0
+  int blocks = (int)((n4 + 255) / 256);
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  slot_sum_kernel<<<blocks, 256, 0, stream>>>(o, y, n4, k, H / 4, status);
+  return check_launch("moe_gather_qmm_down_unsort (ordered sum)");
 }
 
 }  // namespace moeqmm

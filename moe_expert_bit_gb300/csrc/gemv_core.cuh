@@ -233,6 +233,35 @@ __device__ __forceinline__ void cast_block(float *y_acc, uint16_t *y, int32_t *c
   if (lane == 0) cnt[blk] = 0;
 }
 
+// The deterministic un-sort's counterpart of cast_block: the workspace holds one
+// router-weighted fp32 row per assignment, o[a] = w_a * (Wd[e] . h[s]) at a = t*k + j, and
+// y[t, 16 blk ..] = bf16(o[t k] + o[t k + 1] + ... + o[t k + k - 1]), added left to right in
+// fp32, so the result does not depend on which CTA finished first.  The rows are overwritten
+// by every call and need no clearing; the counter is cleared.
+__device__ __forceinline__ void sum_block(const float *o, uint16_t *y, int32_t *cnt, int T, int k,
+                                          int H, int blk, int lane) {
+  __threadfence();
+  for (int i = lane; i < T * 16; i += 32) {
+    const int t = i >> 4, col = 16 * blk + (i & 15);
+    const float *src = o + (int64_t)t * k * H + col;
+    float s = __ldcg(src);
+    for (int j = 1; j < k; ++j) s += __ldcg(src + (int64_t)j * H);
+    y[(int64_t)t * H + col] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+  }
+  if (lane == 0) cnt[blk] = 0;
+}
+
+// the end of a completed 16-column block: cast the shared accumulator (DET false) or sum the
+// per-assignment rows in a fixed order (DET true)
+template <bool DET>
+__device__ __forceinline__ void finish_block(float *ws, uint16_t *y, int32_t *cnt, int T, int k,
+                                             int H, int blk, int lane) {
+  if (DET)
+    sum_block(ws, y, cnt, T, k, H, blk, lane);
+  else
+    cast_block(ws, y, cnt, T, H, blk, lane);
+}
+
 // A ring whose buffers are shared by several consumer teams: chunk i uses buffer i % nbuf,
 // and its consumer waits on the buffer's barrier with the parity of its use.  That parity
 // also matches two uses back, so the consumer first waits until the producer has issued

@@ -14,16 +14,19 @@ moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint1
 // its last contribution lands, and clears the block; y_acc [T, H] is then followed by
 // H/16 int counters (the workspace layout of moe_workspace_bytes), zero on entry and
 // on exit.
+// det: the workspace holds one row per assignment, o[a] = w_a * (Wd[e] . h[s]) (A x H,
+// stored, not added), and a completed block is the fixed-order sum of each token's k rows.
 moe_status launch_down_gemv(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                             const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                             int32_t H, int32_t I, float *y_acc, uint16_t *y, bool fused_cast,
-                            cudaStream_t stream);
+                            bool det, cudaStream_t stream);
 // moe_gather_qmm_down_unsort behind the C ABI (fn names the entry point in errors);
 // clear_ws: zero the workspace first (after validation)
 moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,
                        const moe_bf16_t *Sd, const moe_bf16_t *Bd, const moe_tiles_t *tiles,
                        const float *topk_weights, int32_t H, int32_t I, int32_t variant,
-                       float *y_acc_ws, moe_bf16_t *y, bool clear_ws, cudaStream_t stream);
+                       float *y_acc_ws, int32_t deterministic, moe_bf16_t *y, bool clear_ws,
+                       cudaStream_t stream);
 // The fused decode layer (fused.cu): MOE_OK if a call of this shape fits it.
 moe_status fused_layer_check(int32_t T, int32_t k, int32_t E, int32_t H, int32_t I,
                              int32_t tile_m, int32_t max_tiles);
@@ -34,7 +37,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
                               int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
                               int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
                               int32_t *tile_count, int32_t *status, uint16_t *h, float *y_acc,
-                              uint16_t *y, cudaStream_t stream);
+                              bool det, uint16_t *y, cudaStream_t stream);
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m);
 bool gemv_supported(int32_t H, int32_t I);
 moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
@@ -46,9 +49,13 @@ moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const 
                                   uint16_t *x_sorted, uint16_t *h, cudaStream_t stream);
 moe_status launch_down_tc(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                           const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
-                          int32_t H, int32_t I, float *y_acc, cudaStream_t stream);
+                          int32_t H, int32_t I, float *y_acc, bool per_slot,
+                          cudaStream_t stream);
 // y = bf16(y_acc[0 .. n)); clears y_acc behind the reads
 moe_status launch_cast_bf16(float *y_acc, uint16_t *y, int64_t n, const int32_t *status,
                             cudaStream_t stream);
+// y[t] = bf16(o[t k] + o[t k + 1] + ... + o[t k + k - 1]) over rows of H fp32, in that order
+moe_status launch_slot_sum(const float *o, uint16_t *y, int32_t T, int32_t k, int32_t H,
+                           const int32_t *status, cudaStream_t stream);
 
 }  // namespace moeqmm

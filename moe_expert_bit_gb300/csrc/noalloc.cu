@@ -16,7 +16,8 @@
 
 namespace moeqmm {
 
-// The shared accumulator: [T, H] fp32, T * H <= MOE_NOALLOC_MAX_Y_ELEMENTS (16 MiB).
+// The shared accumulator: [T, H] fp32 (deterministic: [A, H]), at most
+// MOE_NOALLOC_MAX_Y_ELEMENTS floats (16 MiB) with its counters.
 static __device__ __align__(256) float g_noalloc_y_acc[MOE_NOALLOC_MAX_Y_ELEMENTS];
 
 constexpr int kMaxDevices = 64;
@@ -55,18 +56,25 @@ using namespace moeqmm;
 extern "C" moe_status moe_gather_qmm_down_unsort_noalloc(
     const moe_bf16_t *h, const uint32_t *Wd, const moe_bf16_t *Sd, const moe_bf16_t *Bd,
     const moe_tiles_t *tiles, const float *topk_weights, int32_t H, int32_t I, int32_t variant,
-    moe_bf16_t *y, cudaStream_t stream) {
+    int32_t deterministic, moe_bf16_t *y, cudaStream_t stream) {
   const char *fn = "moe_gather_qmm_down_unsort_noalloc";
   clear_error();
   if (!tiles) {
     set_error("%s: tiles is null", fn);
     return MOE_ERR_INVALID_ARG;
   }
-  if (tiles->num_tokens > 0 && H > 0 &&
-      moe_workspace_bytes(tiles->num_tokens, H) > sizeof(float) * MOE_NOALLOC_MAX_Y_ELEMENTS) {
-    set_error("%s: T*H = %lld exceeds the built-in accumulator of %d fp32 elements; "
+  if (deterministic != 0 && deterministic != 1) {
+    set_error("%s: deterministic must be 0 or 1 (got %d)", fn, deterministic);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (tiles->num_tokens > 0 && tiles->top_k > 0 && H > 0 &&
+      moe_unsort_workspace_bytes(tiles->num_tokens, tiles->top_k, H, deterministic) >
+          sizeof(float) * MOE_NOALLOC_MAX_Y_ELEMENTS) {
+    set_error("%s: %s*H = %lld exceeds the built-in accumulator of %d fp32 elements; "
               "use moe_gather_qmm_down_unsort with a caller workspace",
-              fn, (long long)tiles->num_tokens * H, MOE_NOALLOC_MAX_Y_ELEMENTS);
+              fn, deterministic ? "A" : "T",
+              (long long)(deterministic ? tiles->num_assignments : tiles->num_tokens) * H,
+              MOE_NOALLOC_MAX_Y_ELEMENTS);
     return MOE_ERR_UNSUPPORTED;
   }
   if (!h || !Wd || !Sd || !Bd || !topk_weights || !y) {
@@ -79,6 +87,6 @@ extern "C" moe_status moe_gather_qmm_down_unsort_noalloc(
   // The full validation and launch sequence of the workspace entry point, pointed at
   // the built-in accumulator, which is cleared first (after validation): a call that
   // stopped on a device error cannot leave it dirty for the next one.
-  return down_unsort(fn, h, Wd, Sd, Bd, tiles, topk_weights, H, I, variant, scratch, y, true,
-                     stream);
+  return down_unsort(fn, h, Wd, Sd, Bd, tiles, topk_weights, H, I, variant, scratch,
+                     deterministic, y, true, stream);
 }

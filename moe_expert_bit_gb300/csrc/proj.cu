@@ -146,10 +146,16 @@ namespace moeqmm {
 moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,
                        const moe_bf16_t *Sd, const moe_bf16_t *Bd, const moe_tiles_t *tiles,
                        const float *topk_weights, int32_t H, int32_t I, int32_t variant,
-                       float *y_acc_ws, moe_bf16_t *y, bool clear_ws, cudaStream_t stream) {
+                       float *y_acc_ws, int32_t deterministic, moe_bf16_t *y, bool clear_ws,
+                       cudaStream_t stream) {
   moe_status st = validate_tiles(fn, tiles);
   if (st != MOE_OK) return st;
   if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
+  if (deterministic != 0 && deterministic != 1) {
+    set_error("%s: deterministic must be 0 or 1 (got %d)", fn, deterministic);
+    return MOE_ERR_INVALID_ARG;
+  }
+  const bool det = deterministic != 0;
   if (!h || !Wd || !Sd || !Bd || !topk_weights || !y_acc_ws || !y) {
     set_error("%s: null pointer", fn);
     return MOE_ERR_INVALID_ARG;
@@ -159,21 +165,31 @@ moe_status down_unsort(const char *fn, const moe_bf16_t *h, const uint32_t *Wd,
   // The workspace arrives zeroed and is left zeroed: whoever converts a part of the
   // accumulator to y also clears it (and its completion counter), so a call needs no
   // memset in front of its kernels (clear_ws: clear it anyway, after validation).
-  const int64_t n = (int64_t)tiles->num_tokens * H;
-  if (clear_ws &&
-      cudaMemsetAsync(y_acc_ws, 0, moe_workspace_bytes(tiles->num_tokens, H), stream) !=
-          cudaSuccess)
-    return check_launch(fn);
+  // Deterministic: the workspace holds one row per assignment, each written whole by
+  // the down kernel, so only the counters after the rows need to be zero.
+  const int32_t T = tiles->num_tokens, k = tiles->top_k;
+  const int64_t n = (int64_t)T * H;
+  const int64_t rows_bytes = (int64_t)(det ? tiles->num_assignments : T) * H * 4;
+  const size_t ws_bytes = moe_unsort_workspace_bytes(T, k, H, deterministic);
+  if (clear_ws) {
+    const size_t from = det ? (size_t)rows_bytes : 0;
+    if (cudaMemsetAsync(reinterpret_cast<char *>(y_acc_ws) + from, 0, ws_bytes - from,
+                        stream) != cudaSuccess)
+      return check_launch(fn);
+  }
   if (variant == MOE_VARIANT_TC) {
-    st = launch_down_tc(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, stream);
+    st = launch_down_tc(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, det, stream);
     if (st != MOE_OK) return st;
+    if (det) return launch_slot_sum(y_acc_ws, y, T, k, H, tiles->status, stream);
     return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
   }
-  // small outputs: the down kernel itself casts each column block when it completes
-  const bool fuse_cast = n <= (int64_t(1) << 20);
-  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, y, fuse_cast,
+  // small outputs: the down kernel itself casts (or sums) each column block when it
+  // completes; the deterministic sum reads k rows per output, so its bound counts them
+  const bool fuse_cast = rows_bytes / 4 <= (int64_t(1) << 20);
+  st = launch_down_gemv(h, Wd, Sd, Bd, *tiles, topk_weights, H, I, y_acc_ws, y, fuse_cast, det,
                         stream);
   if (st != MOE_OK || fuse_cast) return st;
+  if (det) return launch_slot_sum(y_acc_ws, y, T, k, H, tiles->status, stream);
   return launch_cast_bf16(y_acc_ws, y, n, tiles->status, stream);
 }
 
@@ -183,11 +199,12 @@ extern "C" moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint
                                                  const moe_bf16_t *Sd, const moe_bf16_t *Bd,
                                                  const moe_tiles_t *tiles,
                                                  const float *topk_weights, int32_t H, int32_t I,
-                                                 int32_t variant, float *y_acc_ws, moe_bf16_t *y,
+                                                 int32_t variant, float *y_acc_ws,
+                                                 int32_t deterministic, moe_bf16_t *y,
                                                  cudaStream_t stream) {
   clear_error();
   return down_unsort("moe_gather_qmm_down_unsort", h, Wd, Sd, Bd, tiles, topk_weights, H, I,
-                     variant, y_acc_ws, y, false, stream);
+                     variant, y_acc_ws, deterministic, y, false, stream);
 }
 
 extern "C" moe_status moe_layer_fused(
@@ -196,9 +213,13 @@ extern "C" moe_status moe_layer_fused(
     const uint32_t *Wd, const moe_bf16_t *Sd, const moe_bf16_t *Bd, int32_t H, int32_t I,
     int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids, int32_t *perm, int32_t *counts,
     int32_t *offsets, int32_t *tiles, int32_t *tile_count, int32_t *status, moe_bf16_t *h,
-    float *y_acc_ws, moe_bf16_t *y, cudaStream_t stream) {
+    float *y_acc_ws, int32_t deterministic, moe_bf16_t *y, cudaStream_t stream) {
   const char *fn = "moe_layer_fused";
   clear_error();
+  if (deterministic != 0 && deterministic != 1) {
+    set_error("%s: deterministic must be 0 or 1 (got %d)", fn, deterministic);
+    return MOE_ERR_INVALID_ARG;
+  }
   if (!topk_ids || !topk_weights || !x || !Wgu || !Sgu || !Bgu || !Wd || !Sd || !Bd ||
       !sorted_ids || !perm || !counts || !offsets || !tiles || !tile_count || !status || !h ||
       !y_acc_ws || !y) {
@@ -235,7 +256,7 @@ extern "C" moe_status moe_layer_fused(
   }
   return launch_fused_layer(topk_ids, topk_weights, T, k, E, x, Wgu, Sgu, Bgu, Wd, Sd, Bd, H, I,
                             tile_m, max_tiles, sorted_ids, perm, counts, offsets, tiles,
-                            tile_count, status, h, y_acc_ws, y, stream);
+                            tile_count, status, h, y_acc_ws, deterministic != 0, y, stream);
 }
 
 extern "C" moe_status moe_layer_fused_supported(int32_t T, int32_t k, int32_t E, int32_t H,

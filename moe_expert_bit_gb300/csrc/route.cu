@@ -335,6 +335,15 @@ size_t moe_workspace_bytes(int32_t T, int32_t H) {
   return static_cast<size_t>(T) * static_cast<size_t>(H) * sizeof(float) + counters;
 }
 
+size_t moe_unsort_workspace_bytes(int32_t T, int32_t k, int32_t H, int32_t deterministic) {
+  if (T < 1 || k < 1 || H < 1) return 0;
+  if (!deterministic) return moe_workspace_bytes(T, H);
+  // one fp32 row per assignment instead of per token; the same counters after it
+  const int64_t A = static_cast<int64_t>(T) * k;
+  if (A > INT32_MAX) return 0;
+  return moe_workspace_bytes(static_cast<int32_t>(A), H);
+}
+
 moe_status moe_sort_assignments(const int32_t *topk_ids, int32_t T, int32_t k, int32_t E,
                                 int32_t *sorted_ids, int32_t *perm, int32_t *counts,
                                 int32_t *status, cudaStream_t stream) {

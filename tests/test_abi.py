@@ -47,6 +47,12 @@ def test_size_helpers():
     assert mq.moe_workspace_bytes(4, 64) == 4 * 64 * 4 + 32
     assert mq.moe_workspace_bytes(1, 192) == 192 * 4 + 64
     assert mq.moe_workspace_bytes(0, 2816) == 0
+    # the un-sort's workspace: per token, or one row per assignment when deterministic
+    assert mq.moe_unsort_workspace_bytes(4, 8, 2816) == mq.moe_workspace_bytes(4, 2816)
+    assert mq.moe_unsort_workspace_bytes(4, 8, 2816, True) == 32 * 2816 * 4 + 720
+    assert mq.moe_unsort_workspace_bytes(2048, 8, 2816, True) == 16384 * 2816 * 4 + 720
+    assert mq.moe_unsort_workspace_bytes(4, 0, 2816, True) == 0
+    assert mq.moe_unsort_workspace_bytes(1 << 20, 1 << 12, 64, True) == 0  # A beyond int32
 
 
 def _raw():
@@ -104,17 +110,30 @@ def test_projection_host_validation(tkw, H, I, variant, code):
         pytest.skip("a valid call would launch; covered by the GPU tests")
     st = _raw().moe_gather_qmm_geglu(1, 1, 1, 1, ctypes.byref(t), H, I, variant, 1, NULL)
     assert st == code
-    st = _raw().moe_gather_qmm_down_unsort(1, 1, 1, 1, ctypes.byref(t), 1, H, I, variant, 1, 1,
-                                           NULL)
-    assert st == code
+    for det in (0, 1):
+        st = _raw().moe_gather_qmm_down_unsort(1, 1, 1, 1, ctypes.byref(t), 1, H, I, variant, 1,
+                                               det, 1, NULL)
+        assert st == code
     assert _raw().moe_gather_qmm_geglu(NULL, 1, 1, 1, ctypes.byref(_tiles()), 128, 64, 0, 1,
                                        NULL) == mq.MOE_ERR_INVALID_ARG
+
+
+def test_deterministic_flag_validation():
+    """The un-sort mode is 0 or 1; anything else is refused before a launch."""
+    t = _tiles()
+    assert _raw().moe_gather_qmm_down_unsort(16, 16, 16, 16, ctypes.byref(t), 16, 128, 64, 0,
+                                             16, 2, 16, NULL) == mq.MOE_ERR_INVALID_ARG
+    assert _raw().moe_gather_qmm_down_unsort_noalloc(16, 16, 16, 16, ctypes.byref(t), 16, 128,
+                                                     64, 0, -1, 16,
+                                                     NULL) == mq.MOE_ERR_INVALID_ARG
+    assert _raw().moe_layer_fused(*_fused_args(det=5)) == mq.MOE_ERR_INVALID_ARG
+    assert "deterministic" in _raw().moe_last_error_string().decode()
 
 
 def _fused_args(**kw):
     a = dict(ids=1, w=1, T=4, k=8, E=128, x=16, Wgu=16, Sgu=16, Bgu=16, Wd=16, Sd=16, Bd=16,
              H=2816, I=704, tile_m=128, max_tiles=32, sorted=1, perm=1, counts=1, offsets=1,
-             tiles=1, tile_count=1, status=1, h=16, y_acc=16, y=16, stream=NULL)
+             tiles=1, tile_count=1, status=1, h=16, y_acc=16, det=0, y=16, stream=NULL)
     a.update(kw)
     return tuple(a.values())
 

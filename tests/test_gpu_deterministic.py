@@ -1,0 +1,174 @@
+"""The deterministic weighted un-sort (deterministic=1 on the down call and the fused layer).
+
+In this mode the down kernels store one router-weighted fp32 row per assignment,
+o[a] = w_a * (Wd[e] . h[s]), in row a = t*k + j of the workspace, and y[t] is the sum of
+the token's k rows added left to right in fp32, then rounded to bf16.  Checked here:
+  * y against the fp64 oracle (the bound of tests/_util.py), like the atomic mode;
+  * the per-assignment rows against the oracle's per-expert down projection;
+  * y equal, bit for bit, to that fixed-order sum of the rows recomputed on the CPU (IEEE
+    fp32 additions in the same order, round-to-nearest-even to bf16);
+  * two calls give bit-identical y, and the counters are left zero;
+  * the one-launch layer gives the same bits as the four calls with the GEMV variant.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import bf16_to_f64, excess, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import moe_expert_bit_gb300 as mq  # noqa: E402
+
+VARIANTS = [mq.VARIANT_GEMV, mq.VARIANT_TC]
+
+
+def run(d, variant, tile_m=128, dev=None, buffers=None, fused=False):
+    dev = dev or to_device(d)
+    b = buffers or mq.MoeLayerBuffers(d["T"], d["k"], d["E"], d["H"], d["I"], tile_m,
+                                      deterministic=True)
+    mq.moe_layer(dev["x"], dev["topk_ids"], dev["topk_weights"], dev, d["E"], tile_m=tile_m,
+                 variant=variant, buffers=b, fused=fused, deterministic=True)
+    torch.cuda.synchronize()
+    assert int(b.routing.status.item()) == 0
+    return b
+
+
+def rows_and_counters(b, d):
+    A, H = d["T"] * d["k"], d["H"]
+    ws = b.y_acc.cpu()
+    return ws[:A * H].view(A, H), ws[A * H:].view(torch.int32)
+
+
+def ordered_sum_bf16(rows, T, k):
+    """bf16(o[t k] + o[t k + 1] + ... + o[t k + k - 1]) in fp32, left to right."""
+    r = rows.view(T, k, -1)
+    s = r[:, 0].clone()
+    for j in range(1, k):
+        s = s + r[:, j]
+    return s.to(torch.bfloat16)
+
+
+def check(b, d, ref=None):
+    ref = ref or oracle.layer(d)
+    T, k = d["T"], d["k"]
+    out_rows = np.isin(np.arange(T), d["outlier_rows"])
+    assert excess(bf16_to_f64(b.y), ref["y"], out_rows) <= 1.0
+    rows, cnt = rows_and_counters(b, d)
+    assert int(cnt.abs().sum()) == 0
+    # y is exactly the fixed-order sum of the rows left in the workspace
+    assert torch.equal(ordered_sum_bf16(rows, T, k).view(torch.int16),
+                       b.y.cpu().view(torch.int16))
+    # each row is its assignment's weighted down projection
+    perm, sid = ref["perm"], ref["sorted_ids"]
+    w = d["topk_weights"].reshape(-1).astype(np.float64)
+    o_ref = np.empty((T * k, d["H"]))
+    for s in range(T * k):
+        o_ref[perm[s]] = w[perm[s]] * oracle.expert_down(ref["h"][s], int(sid[s]), d)
+    assert excess(rows.double().numpy(), o_ref, out_rows[np.arange(T * k) // k]) <= 1.0
+    return ref
+
+
+def _skip_if_unbuilt(variant):
+    if variant == mq.VARIANT_TC:
+        try:
+            run(synth.make("tiny"), variant)
+        except mq.MoeError as e:
+            if e.status == mq.MOE_ERR_UNSUPPORTED:
+                pytest.skip("tensor-core variant not built")
+            raise
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_deterministic_unsort_matches_oracle_and_its_definition(variant, name):
+    _skip_if_unbuilt(variant)
+    d = synth.make(name)
+    check(run(d, variant), d)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("E,H,I,T,k", [
+    (5, 192, 128, 37, 3),      # ragged everything, 3 K-groups
+    (1, 128, 64, 1, 1),        # one assignment
+    (3, 256, 192, 300, 2),     # tiles with many rows, ragged tail
+    (4, 128, 64, 16, 4),       # tiles of ~16 rows: several passes per tile
+])
+def test_deterministic_custom_shapes(variant, E, H, I, T, k):
+    _skip_if_unbuilt(variant)
+    d = synth.make_custom(E, H, I, T, k, seed=5)
+    for tile_m in (16, 128):
+        check(run(d, variant, tile_m), d)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_deterministic_runs_are_bit_identical(variant):
+    _skip_if_unbuilt(variant)
+    d = synth.make("decode")
+    dev = to_device(d)
+    b = run(d, variant, dev=dev)
+    y0 = b.y.clone()
+    for _ in range(3):
+        b.y.fill_(3.0)
+        run(d, variant, dev=dev, buffers=b)
+        assert torch.equal(b.y.view(torch.int16), y0.view(torch.int16))
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_deterministic_full_size_sampled(variant):
+    """The prefill workload (4096 assignments; the separate ordered-sum pass): sampled tokens
+    against the oracle, every output equal to the fixed-order sum of the rows."""
+    _skip_if_unbuilt(variant)
+    d = synth.make("prefill_uniform")
+    b = run(d, variant)
+    T, k = d["T"], d["k"]
+    rows, cnt = rows_and_counters(b, d)
+    assert int(cnt.abs().sum()) == 0
+    assert torch.equal(ordered_sum_bf16(rows, T, k).view(torch.int16),
+                       b.y.cpu().view(torch.int16))
+    toks = np.array([0, 1, 77, 200, 311, T - 1], np.int32)
+    ref = oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks)
+    assert excess(bf16_to_f64(b.y)[toks], ref["y"]) <= 1.0
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_deterministic_zero_weight_gives_exact_zero(variant):
+    _skip_if_unbuilt(variant)
+    d = dict(synth.make("tiny"))
+    w = d["topk_weights"].copy()
+    w[:6] = 0.0
+    d["topk_weights"] = w
+    b = run(d, variant, 32)
+    y = bf16_to_f64(b.y)
+    assert np.all(y[:6] == 0.0)
+    assert np.abs(y[6:]).max() > 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_fused_deterministic_equals_four_calls_bitwise(name):
+    """The one-launch layer computes each assignment's row exactly as the GEMV down kernel
+    (same h, same dot-product order), so with the fixed-order sum y matches bit for bit."""
+    d = synth.make(name)
+    dev = to_device(d)
+    if not mq.fused_layer_fits(d["T"], d["k"], d["E"], d["H"], d["I"]):
+        pytest.skip("beyond the fused kernel")
+    bf = run(d, mq.VARIANT_GEMV, dev=dev, fused=True)
+    b4 = run(d, mq.VARIANT_GEMV, dev=dev)
+    assert torch.equal(bf.h.view(torch.int16), b4.h.view(torch.int16))
+    assert torch.equal(bf.y.view(torch.int16), b4.y.view(torch.int16))
+    check(bf, d)
+
+
+def test_buffers_of_the_other_mode_are_refused():
+    d = synth.make("tiny")
+    dev = to_device(d)
+    b = mq.MoeLayerBuffers(d["T"], d["k"], d["E"], d["H"], d["I"], 32)
+    with pytest.raises(mq.MoeError) as ei:
+        mq.moe_layer(dev["x"], dev["topk_ids"], dev["topk_weights"], dev, d["E"], tile_m=32,
+                     buffers=b, deterministic=True)
+    assert ei.value.status == mq.MOE_ERR_INVALID_ARG

@@ -43,6 +43,27 @@ def test_noalloc_matches_workspace_entry_point_twice(name):
     assert np.abs(y_ref).max() > 0
 
 
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_noalloc_deterministic_equals_workspace_entry_point_bitwise(name):
+    """The fixed-order un-sort through the built-in array gives the same bits as through a
+    caller workspace (same variant, same inputs)."""
+    d = synth.make(name)
+    dev = to_device(d)
+    E, H, I, T, k = d["E"], d["H"], d["I"], d["T"], d["k"]
+    b = mq.moe_layer(dev["x"], dev["topk_ids"], dev["topk_weights"], dev, E, tile_m=128,
+                     variant=mq.VARIANT_GEMV, deterministic=True)
+    torch.cuda.synchronize()
+    assert int(b.routing.status.item()) == 0
+    for _ in range(2):
+        y = torch.full((T, H), 5.0, dtype=torch.bfloat16, device="cuda")
+        mq.moe_gather_qmm_down_unsort_noalloc(b.h, dev["Wd"], dev["Sd"], dev["Bd"], b.routing,
+                                              dev["topk_weights"], H, I, y, mq.VARIANT_GEMV,
+                                              deterministic=True)
+        torch.cuda.synchronize()
+        assert int(b.routing.status.item()) == 0
+        assert torch.equal(y.view(torch.int16), b.y.view(torch.int16))
+
+
 def test_noalloc_rejects_sizes_beyond_its_array():
     T, k, E, H, I = 4096, 1, 4, 2048, 64  # T * H = 8 Mi elements > 4 Mi
     r = mq.Routing(T, k, E, 32)
