@@ -175,6 +175,24 @@ __device__ __forceinline__ void one_group(const uint8_t *rA, const uint8_t *rB,
 // in block c) become the MMA B fragments {x0,x4 | x1,x5 | x2,x6 | x3,x7}, and the group's
 // sum goes to xs[r * G + g].  Units u = r * G + g, u = first, first + step, ...; a thread
 // visits its blocks in an order rotated by u, so neighbouring threads hit other banks.
+// The sum has one fixed order whatever the rotation: each block's eight elements left to
+// right, then the blocks as the pairwise tree ((b0 + b1) + (b2 + b3)) + ((b4 + b5) +
+// (b6 + b7)) -- the order of an xor butterfly over eight lanes holding one block each,
+// which is how the one-launch layer sums the rows it stages itself, so both give the
+// same bits.
+__device__ __forceinline__ float block_tree_sum(float (&part)[8], int rot) {
+  // part[c] holds block (c + rot) & 7: rotate back (a barrel shifter on rot's three bits)
+#pragma unroll
+  for (int bit = 1; bit < 8; bit <<= 1) {
+    float t[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) t[i] = (rot & bit) ? part[(i - bit) & 7] : part[i];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) part[i] = t[i];
+  }
+  return ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+}
+
 __device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb, int G, int nrows,
                                               int first, int step) {
   for (int u = first; u < nrows * G; u += step) {
@@ -183,15 +201,17 @@ __device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb,
     uint4 q[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) q[c] = *reinterpret_cast<const uint4 *>(base + ((c + u) & 7) * 16);
-    float sum = 0.f;
+    float part[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const uint32_t w[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
       auto el = [&](int k) -> uint32_t {
         return (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
       };
+      float sum = 0.f;
 #pragma unroll
       for (int k = 0; k < 8; ++k) sum += __uint_as_float(el(k) << 16);
+      part[c] = sum;
       uint4 o;
       o.x = el(0) | (el(4) << 16);
       o.y = el(1) | (el(5) << 16);
@@ -199,7 +219,7 @@ __device__ __forceinline__ void permute_units(uint8_t *xbuf, float *xs, int xrb,
       o.w = el(3) | (el(7) << 16);
       *reinterpret_cast<uint4 *>(base + ((c + u) & 7) * 16) = o;
     }
-    xs[u] = sum;
+    xs[u] = block_tree_sum(part, u & 7);
   }
 }
 

@@ -40,9 +40,11 @@ def run(d, variant, tile_m=128, dev=None, buffers=None, fused=False):
 
 
 def rows_and_counters(b, d):
+    """The per-assignment rows and the H/16 column-block counters after them (the one-launch
+    layer's grid-barrier words follow the counters and may hold any value)."""
     A, H = d["T"] * d["k"], d["H"]
     ws = b.y_acc.cpu()
-    return ws[:A * H].view(A, H), ws[A * H:].view(torch.int32)
+    return ws[:A * H].view(A, H), ws[A * H:A * H + H // 16].view(torch.int32)
 
 
 def ordered_sum_bf16(rows, T, k):
