@@ -32,9 +32,11 @@ constexpr int kFPassG = 8;                       // gate/up columns per pass (al
 constexpr int kFPassD = 4;                       // down rows staged per pass (two buffers)
 constexpr int kFMaxA = 256;                      // assignments the fused kernel takes
 constexpr int kFMaxT = 64;                       // token rows it stages
+constexpr int kFCountQ = 4;                      // down blocks counted per fence
 // named barriers: 1 compute + stager (grid barrier), 2 + 2p / 3 + 2p team p's combine,
-// 15 the start (compute + stager)
-constexpr int kFBarGrid = 1, kFBarStart = 15;
+// 10 the tile list is ready (the producer arrives, every other warp waits), 11 the
+// routing among the non-producer warps, 15 the start (compute + stager)
+constexpr int kFBarGrid = 1, kFBarTiles = 10, kFBarRoute = 11, kFBarStart = 15;
 
 struct FLayout {
   int Gh, Gi, Sh, Si, xrbh, xrbi, slot, nbuf, T, A, E, max_tiles;
@@ -65,11 +67,12 @@ struct FLayout {
     off_tok = off_perm + ((A * 4 + 15) & ~15);
     off_w = off_tok + ((A * 4 + 15) & ~15);
     off_bar = off_w + ((A * 4 + 15) & ~15);
-    off_misc = off_bar + (2 * nbuf + 6) * 8;
+    off_misc = off_bar + (2 * nbuf + 7) * 8;
     total = off_misc + 32;
   }
   // transient routing scratch, inside the last ring slot (no copy lands there before the
-  // routing is done): ids, weights by flat index, sorted ids, histogram, offsets, tile starts
+  // routing is done, which the producer waits for on its own barrier): ids, weights by flat
+  // index, sorted ids, histogram, offsets, tile starts
   __host__ __device__ int scratch_bytes() const { return (3 * A + 3 * (E + 1)) * 4; }
 };
 
@@ -89,29 +92,27 @@ struct FArgs {
 // The grid barrier (thread 0 of each CTA; the launch is cooperative), sense-reversing:
 // gbar[0] counts arrivals, gbar[1] is a generation word read before arriving.  The last
 // CTA to arrive clears the count (so it is zero again on exit) and advances the
-// generation, which releases the others.  The arrival carries release semantics for this
-// CTA's earlier stores (ordered before it by the block barrier); the acquire load that
-// sees the new generation makes every CTA's stores visible.
-__device__ __forceinline__ int32_t ld_acquire(const int32_t *p) {
-  int32_t v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
+// generation, which releases the others.  A fence before the arrival publishes this CTA's
+// earlier stores (ordered before it by the block barrier); the waiters poll the generation
+// with plain volatile loads and fence once they see it change, so that every CTA's stores
+// are visible to them.
 __device__ __forceinline__ bool grid_barrier(int32_t *gbar, int32_t gen,
                                              volatile int *abort_flag) {
-  int32_t old;
-  asm volatile("atom.add.acq_rel.gpu.global.s32 %0, [%1], 1;" : "=r"(old) : "l"(gbar) : "memory");
+  __threadfence();
+  const int32_t old = atomicAdd(gbar, 1);
+  volatile int32_t *vgen = gbar + 1;
   if (old == (int)gridDim.x - 1) {
     gbar[0] = 0;
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(gbar + 1), "r"(gen + 1) : "memory");
+    __threadfence();
+    *vgen = gen + 1;
     return true;
   }
   const uint64_t t0 = umma::globaltimer_ns();
-  for (uint32_t i = 1; ld_acquire(gbar + 1) == gen; ++i) {
+  for (uint32_t i = 1; *vgen == gen; ++i) {
     if ((i & 63u) == 0 && (*abort_flag || umma::globaltimer_ns() - t0 > 2000000000ull))
       return false;
   }
+  __threadfence();
   return true;
 }
 
@@ -137,11 +138,13 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint64_t *xfull = empty + nbuf;  // the token rows landed (tx)
   uint64_t *xready = xfull + 2;    // [2] down-phase h rows staged
   uint64_t *xempty = xready + 2;   // [2] every compute warp done with them
+  uint64_t *scratch_free = xempty + 2;  // the routing scratch in the last slot is released
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + L.off_misc);
   int *s_flags = reinterpret_cast<int *>(gsm + L.off_misc + 4);  // [0] range, [1] order
   int *s_ntiles = reinterpret_cast<int *>(gsm + L.off_misc + 12);
   uint32_t *issued = reinterpret_cast<uint32_t *>(gsm + L.off_misc + 16);  // chunks issued
   int32_t *s_gen = reinterpret_cast<int32_t *>(gsm + L.off_misc + 20);     // barrier generation
+  int *s_order_bad = reinterpret_cast<int *>(gsm + L.off_misc + 24);
   int32_t *sc_ids = reinterpret_cast<int32_t *>(gsm + (size_t)(nbuf - 1) * L.slot);
   float *sc_wa = reinterpret_cast<float *>(sc_ids + p.A);
   int32_t *sc_sorted = sc_ids + 2 * p.A;
@@ -149,7 +152,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
   int32_t *sc_off = sc_hist + (p.E + 1);
   int32_t *sc_tstart = sc_off + (p.E + 1);
 
-  if (load_status(p.status) != 0) return;
+  // The producer reads the status word and the ids first thing, before the set-up, so that
+  // their round trip overlaps it (A <= kFMaxA = 8 * 32: eight ids per lane).
+  int32_t st = 0, my_ids[kFMaxA / 32];
+  if (warp == nwc) {
+    st = load_status(p.status);
+#pragma unroll
+    for (int i = 0; i < kFMaxA / 32; ++i) {
+      const int a = lane + 32 * i;
+      my_ids[i] = a < p.A ? p.topk_ids[a] : 0;
+    }
+  }
   if (smem_addr(gsm) & 127) {
     if (tid == 0) raise_status(p.status, MOE_ERR_CUDA);
     return;
@@ -165,157 +178,177 @@ __global__ void __launch_bounds__(kFThreads, 1)
       mbar_init(&xready[i], 1);
       mbar_init(&xempty[i], nwc);
     }
+    mbar_init(scratch_free, 1);
     *abort_flag = 0;
+    *s_order_bad = 0;
     *issued = 0;
-    // the grid barrier's generation, read before any CTA can arrive (arrivals follow the
-    // gate/up phase of every CTA)
-    *s_gen = *reinterpret_cast<volatile int32_t *>(p.gbar + 1);
     s_flags[0] = s_flags[1] = 0;
     fence_mbar_init();
     // the token rows go out first: they depend on nothing
     mbar_arrive_expect_tx(&xfull[0], (uint32_t)p.T * xbytes_g);
   }
   __syncthreads();
-  if (warp == nwc + 1)
+  if (warp == nwc + 1) {
     for (int r = lane; r < p.T; r += 32)
       bulk_load(xall + (size_t)r * L.xrbh, p.x + (int64_t)r * p.H, xbytes_g, &xfull[0]);
+    // the grid barrier's generation, read before this CTA arrives there (and so before any
+    // CTA can complete the barrier): the start barrier of the compute warps and the stager
+    // orders it before the arrival
+    if (lane == 0) *s_gen = *reinterpret_cast<volatile int32_t *>(p.gbar + 1);
+  }
   if (warp == nwc && lane == 0) {
     prefetch_tensormap(&tmap_gu);
     prefetch_tensormap(&tmap_d);
   }
 
   // ------------------------------------------------ routing, every CTA (steps a1, a2)
-  // stable counting sort of the flat assignments by expert, ties by ascending index
-  for (int e = tid; e <= p.E; e += nthr) sc_hist[e] = 0;
-  for (int a = tid; a < p.A; a += nthr) {
-    const int32_t e = p.topk_ids[a];
-    sc_ids[a] = e;
-    sc_wa[a] = p.topk_weights[a];
-    if (e < 0 || e >= p.E) s_flags[0] = 1;
-  }
-  __syncthreads();
-  const bool range_bad = s_flags[0] != 0;
-  if (!range_bad)
-    for (int a = tid; a < p.A; a += nthr) atomicAdd(&sc_hist[sc_ids[a]], 1);
-  __syncthreads();
-  if (range_bad) {
-    if (blockIdx.x == 0 && tid == 0) {
-      *p.tile_count = 0;
-      raise_status(p.status, MOE_ERR_RANGE);
-    }
-    if (tid == 0) mbar_wait(&xfull[0], 0, nullptr, 200000000ull);  // the token rows in flight
-    return;
-  }
-  if (warp == 0) {  // exclusive scan over <= 256 experts, 8 per lane
-    int32_t loc[8], sum = 0;
+  // The producer warp computes what the weight stream needs -- the histogram, the expert
+  // offsets and the tile descriptors -- and starts streaming at once; the other warps wait
+  // for that tile list, then rank the assignments (the stable counting sort), run the
+  // builder's self-check and write the routing state out (CTA 0).
+  if (warp == nwc) {
+    for (int e = lane; e <= p.E; e += 32) sc_hist[e] = 0;
+    __syncwarp();
+    int bad = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane * 8 + i;
-      loc[i] = e < p.E ? sc_hist[e] : 0;
-      sum += loc[i];
+    for (int i = 0; i < kFMaxA / 32; ++i) {
+      const int a = lane + 32 * i;
+      if (a >= p.A) break;
+      const int32_t e = my_ids[i];
+      sc_ids[a] = e;
+      if (e < 0 || e >= p.E)
+        bad = 1;
+      else
+        atomicAdd(&sc_hist[e], 1);
     }
-    int32_t incl = sum;
+    bad = __any_sync(0xffffffffu, bad);
+    if (st != 0) bad = 2;  // an earlier call failed: do nothing
+    __syncwarp();
+    int n_tiles = 0;
+    const int bm_log2 = __ffs(p.BM) - 1;  // BM is a power of two (16 .. 256)
+    if (!bad) {
+      // exclusive scans over <= 256 experts, 8 per lane: offsets, then tiles per expert
+      int32_t loc[8], tl[8], sum = 0, tsum = 0;
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    int32_t run = incl - sum;
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        loc[i] = e < p.E ? sc_hist[e] : 0;
+        tl[i] = (loc[i] + p.BM - 1) >> bm_log2;
+        sum += loc[i];
+        tsum += tl[i];
+      }
+      int32_t incl = sum, tincl = tsum;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane * 8 + i;
-      if (e < p.E) sc_off[e] = run;
-      run += loc[i];
+      for (int d = 1; d < 32; d <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
+        const int32_t tv = __shfl_up_sync(0xffffffffu, tincl, d);
+        if (lane >= d) {
+          incl += v;
+          tincl += tv;
+        }
+      }
+      int32_t run = incl - sum, trun = tincl - tsum;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int e = lane * 8 + i;
+        if (e < p.E) {
+          sc_off[e] = run;
+          sc_tstart[e] = trun;
+        }
+        run += loc[i];
+        trun += tl[i];
+      }
+      if (lane == 31) {
+        sc_off[p.E] = incl;
+        sc_tstart[p.E] = tincl;
+      }
+      n_tiles = __shfl_sync(0xffffffffu, tincl, 31);
+      __syncwarp();
+      for (int i = lane; i < n_tiles; i += 32) {  // tile i: the last e with start <= i
+        int lo = 0, hi = p.E;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (sc_tstart[mid] <= i) lo = mid; else hi = mid;
+        }
+        const int r = i - sc_tstart[lo], c = sc_off[lo + 1] - sc_off[lo];
+        s_tiles[3 * i] = lo;
+        s_tiles[3 * i + 1] = sc_off[lo] + r * p.BM;
+        s_tiles[3 * i + 2] = min(p.BM, c - r * p.BM);
+      }
     }
-    if (lane == 31) sc_off[p.E] = incl;
+    if (lane == 0) {
+      s_flags[0] = bad;
+      *s_ntiles = n_tiles;
+    }
+    __syncwarp();
+    named_arrive(kFBarTiles, nthr);
+    if (bad) return;  // nothing issued; the others report a range error
+  } else {
+    const int nr = nthr - 32;  // every warp but the producer (the second-to-last warp)
+    const int rtid = warp < nwc ? tid : tid - 32;
+    for (int a = rtid; a < p.A; a += nr) sc_wa[a] = p.topk_weights[a];
+    named_sync(kFBarTiles, nthr);
+    if (s_flags[0]) {
+      if (s_flags[0] == 1 && blockIdx.x == 0 && rtid == 0) {
+        *p.tile_count = 0;
+        raise_status(p.status, MOE_ERR_RANGE);
+      }
+      if (rtid == 0) mbar_wait(&xfull[0], 0, nullptr, 200000000ull);  // the token rows
+      return;
+    }
+    // slot of assignment a: its expert's first slot + the earlier assignments of that expert
+    for (int a = rtid; a < p.A; a += nr) {
+      const int32_t e = sc_ids[a];
+      int r = 0;
+      for (int b2 = 0; b2 < a; ++b2) r += sc_ids[b2] == e;
+      const int s2 = sc_off[e] + r;
+      sc_sorted[s2] = e;
+      s_perm[s2] = a;
+      s_tok[s2] = a / p.k;
+      s_w[s2] = sc_wa[a];
+    }
+    named_sync(kFBarRoute, nr);
+    // the builder's self-check on the sorted ids (range was checked above)
+    for (int s2 = rtid; s2 + 1 < p.A; s2 += nr)
+      if (sc_sorted[s2] > sc_sorted[s2 + 1]) *s_order_bad = 1;
+    named_sync(kFBarRoute, nr);
+    if (*s_order_bad) {
+      if (blockIdx.x == 0 && rtid == 0) {
+        *p.tile_count = 0;
+        raise_status(p.status, MOE_ERR_UNSORTED);
+      }
+      if (rtid == 0) {
+        *abort_flag = 2;  // the producer stops (without a timeout) and drains its copies
+        mbar_wait(&xfull[0], 0, nullptr, 200000000ull);
+      }
+      return;
+    }
+    const int n_tiles = *s_ntiles;
+    if (blockIdx.x == 0) {  // the routing state for the caller
+      for (int s2 = rtid; s2 < p.A; s2 += nr) {
+        p.sorted_ids[s2] = sc_sorted[s2];
+        p.perm[s2] = s_perm[s2];
+      }
+      for (int e = rtid; e <= p.E; e += nr) {
+        p.offsets[e] = sc_off[e];
+        if (e < p.E) p.counts[e] = sc_off[e + 1] - sc_off[e];
+      }
+      for (int i = rtid; i < 3 * n_tiles; i += nr) p.tiles[i] = s_tiles[i];
+      if (rtid == 0) *p.tile_count = n_tiles;
+    }
+    named_sync(kFBarRoute, nr);
+    if (rtid == 0) mbar_arrive(scratch_free);  // the last slot may now take a copy
   }
-  __syncthreads();
-  // slot of assignment a: its expert's first slot + the earlier assignments of that expert
-  for (int a = tid; a < p.A; a += nthr) {
-    const int32_t e = sc_ids[a];
-    int r = 0;
-    for (int b2 = 0; b2 < a; ++b2) r += sc_ids[b2] == e;
-    const int s = sc_off[e] + r;
-    sc_sorted[s] = e;
-    s_perm[s] = a;
-    s_tok[s] = a / p.k;
-    s_w[s] = sc_wa[a];
-  }
-  __syncthreads();
-  // the builder's self-check on the sorted ids (range was checked above)
-  int order_bad = 0;
-  for (int s = tid; s + 1 < p.A; s += nthr) order_bad |= sc_sorted[s] > sc_sorted[s + 1];
-  order_bad = __syncthreads_or(order_bad);
-  if (order_bad) {
-    if (blockIdx.x == 0 && tid == 0) {
-      *p.tile_count = 0;
-      raise_status(p.status, MOE_ERR_UNSORTED);
-    }
-    if (tid == 0) mbar_wait(&xfull[0], 0, nullptr, 200000000ull);  // the token rows in flight
-    return;
-  }
-  if (warp == 0) {  // tiles per expert and their exclusive scan
-    int32_t loc[8], sum = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane * 8 + i;
-      const int c = e < p.E ? sc_off[e + 1] - sc_off[e] : 0;
-      loc[i] = (c + p.BM - 1) / p.BM;
-      sum += loc[i];
-    }
-    int32_t incl = sum;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int32_t v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    int32_t run = incl - sum;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int e = lane * 8 + i;
-      if (e < p.E) sc_tstart[e] = run;
-      run += loc[i];
-    }
-    if (lane == 31) {
-      sc_tstart[p.E] = incl;
-      *s_ntiles = incl;
-    }
-  }
-  __syncthreads();
   const int n_tiles = *s_ntiles;
-  for (int i = tid; i < n_tiles; i += nthr) {  // tile i belongs to the last e with start <= i
-    int lo = 0, hi = p.E;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sc_tstart[mid] <= i) lo = mid; else hi = mid;
-    }
-    const int r = i - sc_tstart[lo], c = sc_off[lo + 1] - sc_off[lo];
-    s_tiles[3 * i] = lo;
-    s_tiles[3 * i + 1] = sc_off[lo] + r * p.BM;
-    s_tiles[3 * i + 2] = min(p.BM, c - r * p.BM);
-  }
-  __syncthreads();
-  if (blockIdx.x == 0) {  // the routing state for the caller
-    for (int s = tid; s < p.A; s += nthr) {
-      p.sorted_ids[s] = sc_sorted[s];
-      p.perm[s] = s_perm[s];
-    }
-    for (int e = tid; e <= p.E; e += nthr) {
-      p.offsets[e] = sc_off[e];
-      if (e < p.E) p.counts[e] = sc_off[e + 1] - sc_off[e];
-    }
-    for (int i = tid; i < 3 * n_tiles; i += nthr) p.tiles[i] = s_tiles[i];
-    if (tid == 0) *p.tile_count = n_tiles;
-  }
-  __syncthreads();  // the scratch slot is free from here on
 
   // work ranges of the two phases (contiguous chunk ranges per CTA)
   const int cpt_g = p.I / 8, cpt_d = p.H / kFDownRows;
   const int tot_g = n_tiles * cpt_g, tot_d = n_tiles * cpt_d;
-  const int g0 = (int)((int64_t)tot_g * blockIdx.x / gridDim.x);
-  const int g1 = (int)((int64_t)tot_g * (blockIdx.x + 1) / gridDim.x);
-  const int d0 = (int)((int64_t)tot_d * blockIdx.x / gridDim.x);
-  const int d1 = (int)((int64_t)tot_d * (blockIdx.x + 1) / gridDim.x);
+  // (32-bit: tot_g * gridDim < 512 tiles * 504 chunks * 1024 CTAs < 2^31)
+  const int g0 = (int)((uint32_t)tot_g * blockIdx.x / gridDim.x);
+  const int g1 = (int)((uint32_t)tot_g * (blockIdx.x + 1) / gridDim.x);
+  const int d0 = (int)((uint32_t)tot_d * blockIdx.x / gridDim.x);
+  const int d1 = (int)((uint32_t)tot_d * (blockIdx.x + 1) / gridDim.x);
 
   if (warp == nwc) {
     // ------------------------------------------------ producer: gate/up chunks, then down
@@ -333,6 +366,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         for (int r0 = 0; ok && r0 < R; r0 += pass) {
           for (int j = j0; j < j1; ++j) {
             ok = mbar_wait(&empty[b], ph ^ 1, abort_flag);
+            if (ok && it == (uint32_t)(nbuf - 1)) ok = mbar_wait(scratch_free, 0, abort_flag);
             if (!(ok = __all_sync(0xffffffffu, ok))) break;
             uint8_t *buf = gsm + (size_t)b * L.slot;
             if (lane == 0) {
@@ -372,7 +406,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
         }
       }
     }
-    if (!ok && lane == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+    if (!ok && lane == 0 && *abort_flag != 2) raise_status(p.status, MOE_ERR_TIMEOUT);
     __syncwarp();
     if (lane == 0)
       for (uint32_t i = (it > (uint32_t)nbuf ? it - nbuf : 0); i < it; ++i)
@@ -530,7 +564,25 @@ __global__ void __launch_bounds__(kFThreads, 1)
   {
     const int row_lo = 16 * member;
     const bool pair_loads = (Gi % 2) == 0;
-    int pend_blk = -1, pend_rows = 0, flt_blk = -1, flt_rows = 0, flt_old = 0;
+    // Column blocks this warp has added to and not yet counted: entry n is held by lane n
+    // (q_blk, q_rows).  They are counted in batches of up to kFCountQ, with one fence per
+    // batch instead of one per chunk (the fence waits for the warp's reductions to land).
+    int q_blk = 0, q_rows = 0, qn = 0;
+    auto count_blocks = [&]() {
+      __syncwarp();
+      int old = 0;
+      if (lane < qn) {
+        __threadfence();
+        old = atomicAdd(p.cnt + q_blk, q_rows);
+      }
+      for (int n = 0; n < qn; ++n) {
+        const int o = __shfl_sync(0xffffffffu, old, n);
+        const int bl = __shfl_sync(0xffffffffu, q_blk, n);
+        const int rw = __shfl_sync(0xffffffffu, q_rows, n);
+        if (o + rw == p.A) finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, bl, lane);
+      }
+      qn = 0;
+    };
     uint32_t xit = 0;
     for (int tile = d0 / cpt_d; tile * cpt_d < d1; ++tile) {
       const int row0 = s_tiles[3 * tile + 1], R = s_tiles[3 * tile + 2];
@@ -585,22 +637,6 @@ __global__ void __launch_bounds__(kFThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[b]);
           if (!ok) continue;
-          if (flt_blk >= 0) {  // the count issued one chunk ago
-            const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-            if (old + flt_rows == p.A)
-              finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, flt_blk, lane);
-            flt_blk = -1;
-          }
-          if (pend_blk >= 0) {  // count the previous chunk's reductions
-            __syncwarp();
-            if (lane == 0) {
-              __threadfence();
-              flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
-            }
-            flt_blk = pend_blk;
-            flt_rows = pend_rows;
-            pend_blk = -1;
-          }
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
             if (2 * t + c >= Rp) continue;
@@ -614,30 +650,17 @@ __global__ void __launch_bounds__(kFThreads, 1)
               atomicAdd(yrow + gq + 8, w_c[c] * acc[2 + c]);
             }
           }
-          pend_blk = (kFDownRows * j + row_lo) / 16;
-          pend_rows = Rp;
+          if (lane == qn) {
+            q_blk = (kFDownRows * j + row_lo) / 16;  // this warp's 16 columns
+            q_rows = Rp;
+          }
+          if (++qn == kFCountQ) count_blocks();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&xempty[xb]);
       }
     }
-    if (ok) {  // drain the count pipeline
-      if (flt_blk >= 0) {
-        const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-        if (old + flt_rows == p.A)
-          finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, flt_blk, lane);
-      }
-      if (pend_blk >= 0) {
-        __syncwarp();
-        if (lane == 0) {
-          __threadfence();
-          flt_old = atomicAdd(p.cnt + pend_blk, pend_rows);
-        }
-        const int old = __shfl_sync(0xffffffffu, flt_old, 0);
-        if (old + pend_rows == p.A)
-          finish_block<DET>(p.y_acc, p.y, p.cnt, p.T, p.k, p.H, pend_blk, lane);
-      }
-    }
+    if (ok && qn) count_blocks();
     if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
   }
 }
