@@ -235,8 +235,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="decode", choices=synth.CONFIG_ORDER)
-    ap.add_argument("--variant", default="auto", choices=["auto", "fused", "gemv", "tc"],
-                    help="auto: the four calls with the library's own variant choice; "
+    ap.add_argument("--variant", default="best", choices=["best", "auto", "fused", "gemv", "tc"],
+                    help="best: the one-launch layer where it takes the workload, else the "
+                         "four calls with the library's own variant choice (auto); "
                          "fused: the one-launch layer (decode-sized calls)")
     ap.add_argument("--tile-m", type=int, default=128)
     ap.add_argument("--deterministic", action="store_true",
@@ -260,8 +261,8 @@ def main():
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local if world > 1 else 0)
     torch.cuda.set_device(dev)
-    variant = {"auto": mq.VARIANT_AUTO, "fused": mq.VARIANT_AUTO, "gemv": mq.VARIANT_GEMV,
-               "tc": mq.VARIANT_TC}[args.variant]
+    variant = {"best": mq.VARIANT_AUTO, "auto": mq.VARIANT_AUTO, "fused": mq.VARIANT_AUTO,
+               "gemv": mq.VARIANT_GEMV, "tc": mq.VARIANT_TC}[args.variant]
 
     cfg = synth.CONFIGS[args.config]
     d = synth.make(args.config)
@@ -288,14 +289,16 @@ def main():
     r = buf.routing
     r.status.zero_()
 
-    # the one-launch layer when asked for (it measures no faster than the four calls yet)
-    use_fused = args.variant == "fused" and mq.fused_layer_fits(T, k, E, H, I, args.tile_m)
+    # the one-launch layer when asked for, or by default where it takes the workload
+    fits = mq.fused_layer_fits(T, k, E, H, I, args.tile_m)
+    use_fused = args.variant in ("fused", "best") and fits
     if args.variant == "fused" and not use_fused:
         raise SystemExit("the fused layer does not take this workload")
     # the library's AUTO rule: the weight-streaming GEMV for small tiles, else tensor cores
     tc_path = variant == mq.VARIANT_TC or (variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
     use_ws = tc_path and not use_fused
-    path = "moe_layer_fused" if use_fused else f"four calls, variant {args.variant}"
+    path = ("moe_layer_fused" if use_fused else
+            f"four calls, variant {'auto' if args.variant == 'best' else args.variant}")
 
     def step(ev=None):
         if use_fused:
