@@ -236,9 +236,11 @@ moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_t *Wgu, con
  *                           completes leaves the counters (and, when not
  *                           deterministic, the accumulator) zero again, so no
  *                           memset is needed per call; moe_layer_fused also keeps
- *                           a grid-barrier generation word after them, any value
- *                           of which is valid.  After a call that set the status
- *                           word, clear it before reusing it.
+ *                           a 64-bit count of grid-barrier arrivals after them,
+ *                           which every call that completes leaves a multiple of
+ *                           the GPU's SM count (zero is such a value; use one
+ *                           workspace on one GPU).  After a call that set the
+ *                           status word, clear it before reusing it.
  *   deterministic    0 or 1 (else MOE_ERR_INVALID_ARG)
  *   y   [T, H]       bf16   out: y[t] = sum_j topk_weights[t, j] * (Wd[e] . h[s]),
  *                           s the slot of a = t*k + j, e = sorted_ids[s]

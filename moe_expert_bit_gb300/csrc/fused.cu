@@ -68,7 +68,7 @@ struct FLayout {
     off_w = off_tok + ((A * 4 + 15) & ~15);
     off_bar = off_w + ((A * 4 + 15) & ~15);
     off_misc = off_bar + (2 * nbuf + 7) * 8;
-    total = off_misc + 32;
+    total = off_misc + 48;
   }
   // transient routing scratch, inside the last ring slot (no copy lands there before the
   // routing is done, which the producer waits for on its own barrier): ids, weights by flat
@@ -85,30 +85,25 @@ struct FArgs {
   uint16_t *h;
   float *y_acc;
   int32_t *cnt;   // H/16 column-block counters, after y_acc
-  int32_t *gbar;  // grid barrier: arrivals, generation
+  unsigned long long *gbar;  // grid barrier: arrivals of every call so far (monotonic)
   uint16_t *y;
 };
 
-// The grid barrier (thread 0 of each CTA; the launch is cooperative), sense-reversing:
-// gbar[0] counts arrivals, gbar[1] is a generation word read before arriving.  The last
-// CTA to arrive clears the count (so it is zero again on exit) and advances the
-// generation, which releases the others.  A fence before the arrival publishes this CTA's
-// earlier stores (ordered before it by the block barrier); the waiters poll the generation
-// with plain volatile loads and fence once they see it change, so that every CTA's stores
-// are visible to them.
-__device__ __forceinline__ bool grid_barrier(int32_t *gbar, int32_t gen,
+// The grid barrier (thread 0 of each CTA; the launch is cooperative).  gbar counts the
+// arrivals of every call so far: it is a multiple of the grid size N between calls, so a CTA
+// that reads it at its start (before its own arrival, hence while fewer than N CTAs of this
+// call have arrived) finds base + f with f < N, and every CTA of the call derives the same
+// target, base + N.  A CTA publishes its earlier stores with a fence (they are ordered
+// before it by the block barrier), adds its arrival, and polls with plain volatile loads
+// until the count reaches the target; a fence after the wait makes every CTA's stores
+// visible to it.  No CTA has to act after the others have arrived.
+__device__ __forceinline__ bool grid_barrier(unsigned long long *gbar, unsigned long long target,
                                              volatile int *abort_flag) {
   __threadfence();
-  const int32_t old = atomicAdd(gbar, 1);
-  volatile int32_t *vgen = gbar + 1;
-  if (old == (int)gridDim.x - 1) {
-    gbar[0] = 0;
-    __threadfence();
-    *vgen = gen + 1;
-    return true;
-  }
+  atomicAdd(gbar, 1ull);
+  volatile unsigned long long *vc = gbar;
   const uint64_t t0 = umma::globaltimer_ns();
-  for (uint32_t i = 1; *vgen == gen; ++i) {
+  for (uint32_t i = 1; *vc < target; ++i) {
     if ((i & 63u) == 0 && (*abort_flag || umma::globaltimer_ns() - t0 > 2000000000ull))
       return false;
   }
@@ -143,7 +138,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   int *s_flags = reinterpret_cast<int *>(gsm + L.off_misc + 4);  // [0] range, [1] order
   int *s_ntiles = reinterpret_cast<int *>(gsm + L.off_misc + 12);
   uint32_t *issued = reinterpret_cast<uint32_t *>(gsm + L.off_misc + 16);  // chunks issued
-  int32_t *s_gen = reinterpret_cast<int32_t *>(gsm + L.off_misc + 20);     // barrier generation
+  unsigned long long *s_gbase =  // the barrier count read at the start
+      reinterpret_cast<unsigned long long *>(gsm + L.off_misc + 32);
   int *s_order_bad = reinterpret_cast<int *>(gsm + L.off_misc + 24);
   int32_t *sc_ids = reinterpret_cast<int32_t *>(gsm + (size_t)(nbuf - 1) * L.slot);
   float *sc_wa = reinterpret_cast<float *>(sc_ids + p.A);
@@ -191,10 +187,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
   if (warp == nwc + 1) {
     for (int r = lane; r < p.T; r += 32)
       bulk_load(xall + (size_t)r * L.xrbh, p.x + (int64_t)r * p.H, xbytes_g, &xfull[0]);
-    // the grid barrier's generation, read before this CTA arrives there (and so before any
-    // CTA can complete the barrier): the start barrier of the compute warps and the stager
-    // orders it before the arrival
-    if (lane == 0) *s_gen = *reinterpret_cast<volatile int32_t *>(p.gbar + 1);
+    // the grid barrier's count, read before this CTA arrives there (the start barrier of the
+    // compute warps and the stager orders it before the arrival)
+    if (lane == 0) *s_gbase = *reinterpret_cast<volatile unsigned long long *>(p.gbar);
   }
   if (warp == nwc && lane == 0) {
     prefetch_tensormap(&tmap_gu);
@@ -505,7 +500,10 @@ __global__ void __launch_bounds__(kFThreads, 1)
 
   // ------------------------------------------------ grid barrier: h is complete
   named_sync(kFBarGrid, nt);
-  if (tid == 0) s_flags[1] = grid_barrier(p.gbar, *s_gen, abort_flag) ? 0 : 1;
+  if (tid == 0) {
+    const unsigned long long n = gridDim.x;
+    s_flags[1] = grid_barrier(p.gbar, (*s_gbase / n + 1) * n, abort_flag) ? 0 : 1;
+  }
   named_sync(kFBarGrid, nt);
   if (s_flags[1]) {
     ok = false;
@@ -749,7 +747,8 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   a.y_acc = y_acc;
   // counters after the accumulator: T x H, or A x H per-assignment rows when deterministic
   a.cnt = reinterpret_cast<int32_t *>(y_acc + (int64_t)(det ? A : T) * H);
-  a.gbar = a.cnt + H / 16;
+  // after the counters, 16-byte aligned (the counters take H / 16 * 4 bytes, H % 64 == 0)
+  a.gbar = reinterpret_cast<unsigned long long *>(a.cnt + H / 16);
   a.y = y;
   // cooperative: every CTA resident at once (the grid barrier waits for all of them)
   cudaLaunchConfig_t cfg = {};
