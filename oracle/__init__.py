@@ -59,6 +59,13 @@ def _load():
         lib.oracle_gelu_tanh.argtypes = [f64]
         lib.oracle_gelu_tanh.restype = f64
         lib.oracle_gelu_tanh_array.argtypes = [p, i64, p]
+        lib.oracle_silu.argtypes = [f64]
+        lib.oracle_silu.restype = f64
+        lib.oracle_silu_array.argtypes = [p, i64, p]
+        lib.oracle_expert_glu.argtypes = [p, i32, i32, i32, p, p, p, i32, p]
+        lib.oracle_glu_slots.argtypes = [p, i32, i32, i32, p, p, p, p, p, p, i32, i32, p]
+        lib.oracle_moe_layer_tokens_act.argtypes = [p, p, p, i32, i32, i32, p, p, p, p, p, p,
+                                                    p, i32, i32, p]
         lib.oracle_round_bf16.argtypes = [f64]
         lib.oracle_round_bf16.restype = f64
         lib.oracle_round_bf16_array.argtypes = [p, i64, p]
@@ -112,6 +119,24 @@ def gelu_tanh(z) -> np.ndarray:
     return out
 
 
+def silu(z) -> np.ndarray:
+    """SiLU z * sigmoid(z), elementwise (the gate activation of the SwiGLU product)."""
+    z, pz = _c(np.atleast_1d(z), np.float64)
+    out = np.empty_like(z)
+    _load().oracle_silu_array(pz, z.size, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+# gate activations of the gated product: geluApproximate (GeGLU) or SiLU (SwiGLU)
+ACTIVATIONS = {"gelu_tanh": 0, "silu": 1}
+
+
+def _act(activation) -> int:
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"unknown activation {activation!r}")
+    return ACTIVATIONS[activation]
+
+
 def round_bf16(v) -> np.ndarray:
     v, pv = _c(v, np.float64)
     out = np.empty_like(v)
@@ -162,17 +187,19 @@ def _weights(d, names):
     return arrs
 
 
-def expert_geglu(x_row, e: int, d) -> np.ndarray:
-    """h = gelu_tanh(Wg[e] x) * (Wu[e] x) for one bf16-bits activation row."""
+def expert_geglu(x_row, e: int, d, activation="gelu_tanh") -> np.ndarray:
+    """h = act(Wg[e] x) * (Wu[e] x) for one bf16-bits activation row (act: gelu_tanh or
+    silu)."""
     H, I = d["H"], d["I"]
     (_, pW), (_, pS), (_, pB) = _weights(d, ["Wgu", "Sgu", "Bgu"])
     x, px = _c(x_row, np.uint16)
     h = np.empty(I, np.float64)
-    _load().oracle_expert_geglu(px, e, H, I, pW, pS, pB, h.ctypes.data_as(ctypes.c_void_p))
+    _load().oracle_expert_glu(px, e, H, I, pW, pS, pB, _act(activation),
+                              h.ctypes.data_as(ctypes.c_void_p))
     return h
 
 
-def geglu_slots(d, sorted_ids, perm, slots) -> np.ndarray:
+def geglu_slots(d, sorted_ids, perm, slots, activation="gelu_tanh") -> np.ndarray:
     """h rows [len(slots), I] (fp64) for sorted slots of workload dict ``d``."""
     H, I, k = d["H"], d["I"], d["k"]
     (_, pW), (_, pS), (_, pB) = _weights(d, ["Wgu", "Sgu", "Bgu"])
@@ -181,8 +208,8 @@ def geglu_slots(d, sorted_ids, perm, slots) -> np.ndarray:
     pm, ppm = _c(perm, np.int32)
     sl, psl = _c(slots, np.int32)
     h = np.empty((sl.size, I), np.float64)
-    _load().oracle_geglu_slots(px, H, I, k, pW, pS, pB, psid, ppm, psl, sl.size,
-                               h.ctypes.data_as(ctypes.c_void_p))
+    _load().oracle_glu_slots(px, H, I, k, pW, pS, pB, psid, ppm, psl, sl.size, _act(activation),
+                             h.ctypes.data_as(ctypes.c_void_p))
     return h
 
 
@@ -210,7 +237,8 @@ def down_unsort(d, h, sorted_ids, perm, tokens, topk_weights=None) -> np.ndarray
     return y
 
 
-def moe_layer_tokens(d, tokens, topk_weights=None, topk_ids=None) -> np.ndarray:
+def moe_layer_tokens(d, tokens, topk_weights=None, topk_ids=None,
+                     activation="gelu_tanh") -> np.ndarray:
     """y rows [len(tokens), H] by the direct per-token definition (no sort)."""
     H, I, k = d["H"], d["I"], d["k"]
     (_, pWgu), (_, pSgu), (_, pBgu), (_, pWd), (_, pSd), (_, pBd) = _weights(
@@ -220,12 +248,13 @@ def moe_layer_tokens(d, tokens, topk_weights=None, topk_ids=None) -> np.ndarray:
     tw, ptw = _c(d["topk_weights"] if topk_weights is None else topk_weights, np.float32)
     tk, ptk = _c(tokens, np.int32)
     y = np.empty((tk.size, H), np.float64)
-    _load().oracle_moe_layer_tokens(px, pids, ptw, k, H, I, pWgu, pSgu, pBgu, pWd, pSd, pBd, ptk,
-                                    tk.size, y.ctypes.data_as(ctypes.c_void_p))
+    _load().oracle_moe_layer_tokens_act(px, pids, ptw, k, H, I, pWgu, pSgu, pBgu, pWd, pSd, pBd,
+                                        ptk, tk.size, _act(activation),
+                                        y.ctypes.data_as(ctypes.c_void_p))
     return y
 
 
-def layer(d, slots=None, tokens=None):
+def layer(d, slots=None, tokens=None, activation="gelu_tanh"):
     """Sort, tiles-free sorted route for the listed slots/tokens (default: all).
 
     Returns dict(sorted_ids, perm, counts, h (rows for ``slots``), y (rows for ``tokens``)).
@@ -245,7 +274,7 @@ def layer(d, slots=None, tokens=None):
     need = np.unique(np.concatenate([np.asarray(slots, np.int32),
                                      slot_of[(tokens[:, None] * d["k"]
                                               + np.arange(d["k"])[None, :]).ravel()]]))
-    h_need = geglu_slots(d, sorted_ids, perm, need)
+    h_need = geglu_slots(d, sorted_ids, perm, need, activation)
     h_full = np.zeros((A, d["I"]), np.float64)
     h_full[need] = h_need
     y = down_unsort(d, h_full, sorted_ids, perm, tokens)

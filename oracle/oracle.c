@@ -27,6 +27,11 @@
  *              router-weighted sum of each token's expert outputs.
  *  [P3-Meas]   Layr-Labs/mlx PR #4, "Measured standing": direct weighted
  *              un-sort back to token order.
+ *  [P1-Swi]    SharpAI/SwiftLM issue #236, "What #27 set out to do" (item 2,
+ *              the silu-mul and gelu-mul products, compiledSwiGLU) and
+ *              "Already on main" (compiledSiluProduct, SwitchGLU's
+ *              activationProduct): the same gated product with SiLU in place
+ *              of geluApproximate.
  *
  * Readings where the pages are silent (each is also listed in the design
  * notes of the repository):
@@ -37,6 +42,8 @@
  *    w = scale * q + bias with the group g = k / 64;
  *  - geluApproximate is the tanh form 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3)))
  *    (Hendrycks & Gimpel, "Gaussian Error Linear Units", 2016);
+ *  - SiLU is z * sigmoid(z) = z / (1 + exp(-z)) (Elfwing, Uchibe & Doya 2018; the
+ *    swish of Ramachandran, Zoph & Le with beta = 1);
  *  - tile descriptors are {expert, row_begin, rows} with experts ascending,
  *    remainder rows forming one short tile;
  *  - self-check outcome: tile_count = 0 and a status code, out-of-range ids
@@ -94,6 +101,19 @@ double oracle_gelu_tanh(double z) {
 
 void oracle_gelu_tanh_array(const double *z, int64_t n, double *out) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_gelu_tanh(z[i]);
+}
+
+/* SiLU, z * sigmoid(z) [P1-Swi]. */
+double oracle_silu(double z) { return z / (1.0 + exp(-z)); }
+
+void oracle_silu_array(const double *z, int64_t n, double *out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_silu(z[i]);
+}
+
+/* The gate activation of the gated product: 0 geluApproximate, 1 SiLU. */
+enum { ORACLE_ACT_GELU_TANH = 0, ORACLE_ACT_SILU = 1 };
+static double oracle_act(int32_t act, double z) {
+  return act == ORACLE_ACT_SILU ? oracle_silu(z) : oracle_gelu_tanh(z);
 }
 
 /* Round a double to the nearest bf16 value, ties to even (test-input helper). */
@@ -211,11 +231,11 @@ int oracle_build_expert_tiles(const int32_t *sorted_ids, int32_t A, int32_t E, i
  * For one activation row x (length H, bf16 bits) and expert e:
  *   g[n] = sum_kk Wgu[e][n][kk]     * x[kk],  n in [0, I)   (gate rows)
  *   u[n] = sum_kk Wgu[e][I + n][kk] * x[kk]                  (up rows)
- *   h[n] = gelu_tanh(g[n]) * u[n]                  [P1-Miss; P3-What]
+ *   h[n] = act(g[n]) * u[n], act = gelu_tanh [P1-Miss; P3-What] or silu [P1-Swi]
  */
-void oracle_expert_geglu(const uint16_t *x_row, int32_t e, int32_t H, int32_t I,
-                         const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
-                         double *h) {
+void oracle_expert_glu(const uint16_t *x_row, int32_t e, int32_t H, int32_t I,
+                       const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                       int32_t act, double *h) {
   const int64_t rows = 2 * (int64_t)I;
   const uint32_t *P = Wgu + (int64_t)e * rows * (H / 8);
   const uint16_t *S = Sgu + (int64_t)e * rows * (H / 64);
@@ -227,8 +247,14 @@ void oracle_expert_geglu(const uint16_t *x_row, int32_t e, int32_t H, int32_t I,
       g += oracle_dequant(P, S, B, H, n, kk) * xv;
       u += oracle_dequant(P, S, B, H, (int64_t)I + n, kk) * xv;
     }
-    h[n] = oracle_gelu_tanh(g) * u;
+    h[n] = oracle_act(act, g) * u;
   }
+}
+
+void oracle_expert_geglu(const uint16_t *x_row, int32_t e, int32_t H, int32_t I,
+                         const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                         double *h) {
+  oracle_expert_glu(x_row, e, H, I, Wgu, Sgu, Bgu, ORACLE_ACT_GELU_TANH, h);
 }
 
 /*
@@ -236,17 +262,25 @@ void oracle_expert_geglu(const uint16_t *x_row, int32_t e, int32_t H, int32_t I,
  * x[perm[s] / k] and expert sorted_ids[s] (the gather of [P3-What]).
  * h_out is [n_slots, I] in the order of `slots`.
  */
-void oracle_geglu_slots(const uint16_t *x, int32_t H, int32_t I, int32_t k,
-                        const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
-                        const int32_t *sorted_ids, const int32_t *perm, const int32_t *slots,
-                        int32_t n_slots, double *h_out) {
+void oracle_glu_slots(const uint16_t *x, int32_t H, int32_t I, int32_t k,
+                      const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                      const int32_t *sorted_ids, const int32_t *perm, const int32_t *slots,
+                      int32_t n_slots, int32_t act, double *h_out) {
 #pragma omp parallel for schedule(dynamic, 1)
   for (int32_t i = 0; i < n_slots; ++i) {
     int32_t s = slots[i];
     int32_t t = perm[s] / k;
-    oracle_expert_geglu(x + (int64_t)t * H, sorted_ids[s], H, I, Wgu, Sgu, Bgu,
-                        h_out + (int64_t)i * I);
+    oracle_expert_glu(x + (int64_t)t * H, sorted_ids[s], H, I, Wgu, Sgu, Bgu, act,
+                      h_out + (int64_t)i * I);
   }
+}
+
+void oracle_geglu_slots(const uint16_t *x, int32_t H, int32_t I, int32_t k,
+                        const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                        const int32_t *sorted_ids, const int32_t *perm, const int32_t *slots,
+                        int32_t n_slots, double *h_out) {
+  oracle_glu_slots(x, H, I, k, Wgu, Sgu, Bgu, sorted_ids, perm, slots, n_slots,
+                   ORACLE_ACT_GELU_TANH, h_out);
 }
 
 /* ---- a7: down projection of one h row ---- */
@@ -302,14 +336,16 @@ void oracle_down_unsort(const double *h, const int32_t *sorted_ids, const int32_
 /* ---- the whole layer, by its plain per-token definition (no sort) ---- */
 
 /*
- * y[t] = sum_j w[t,j] * Wd[e] . ( gelu_tanh(Wg[e] x_t) * (Wu[e] x_t) ),
- * e = topk_ids[t, j], for the listed tokens (y_out [n_tokens, H]).
+ * y[t] = sum_j w[t,j] * Wd[e] . ( act(Wg[e] x_t) * (Wu[e] x_t) ),
+ * e = topk_ids[t, j], for the listed tokens (y_out [n_tokens, H]); act as in
+ * oracle_expert_glu.
  */
-void oracle_moe_layer_tokens(const uint16_t *x, const int32_t *topk_ids,
-                             const float *topk_weights, int32_t k, int32_t H, int32_t I,
-                             const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
-                             const uint32_t *Wd, const uint16_t *Sd, const uint16_t *Bd,
-                             const int32_t *tokens, int32_t n_tokens, double *y_out) {
+void oracle_moe_layer_tokens_act(const uint16_t *x, const int32_t *topk_ids,
+                                 const float *topk_weights, int32_t k, int32_t H, int32_t I,
+                                 const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                                 const uint32_t *Wd, const uint16_t *Sd, const uint16_t *Bd,
+                                 const int32_t *tokens, int32_t n_tokens, int32_t act,
+                                 double *y_out) {
 #pragma omp parallel
   {
     double *h = (double *)malloc(sizeof(double) * (size_t)I);
@@ -321,7 +357,7 @@ void oracle_moe_layer_tokens(const uint16_t *x, const int32_t *topk_ids,
       for (int32_t n = 0; n < H; ++n) y[n] = 0.0;
       for (int32_t j = 0; j < k; ++j) {
         int32_t e = topk_ids[t * k + j];
-        oracle_expert_geglu(x + (int64_t)t * H, e, H, I, Wgu, Sgu, Bgu, h);
+        oracle_expert_glu(x + (int64_t)t * H, e, H, I, Wgu, Sgu, Bgu, act, h);
         oracle_expert_down(h, e, H, I, Wd, Sd, Bd, o);
         double w = (double)topk_weights[t * k + j];
         for (int32_t n = 0; n < H; ++n) y[n] += w * o[n];
@@ -330,6 +366,15 @@ void oracle_moe_layer_tokens(const uint16_t *x, const int32_t *topk_ids,
     free(h);
     free(o);
   }
+}
+
+void oracle_moe_layer_tokens(const uint16_t *x, const int32_t *topk_ids,
+                             const float *topk_weights, int32_t k, int32_t H, int32_t I,
+                             const uint32_t *Wgu, const uint16_t *Sgu, const uint16_t *Bgu,
+                             const uint32_t *Wd, const uint16_t *Sd, const uint16_t *Bd,
+                             const int32_t *tokens, int32_t n_tokens, double *y_out) {
+  oracle_moe_layer_tokens_act(x, topk_ids, topk_weights, k, H, I, Wgu, Sgu, Bgu, Wd, Sd, Bd,
+                              tokens, n_tokens, ORACLE_ACT_GELU_TANH, y_out);
 }
 
 void oracle_round_bf16_array(const double *v, int64_t n, double *out) {

@@ -104,6 +104,58 @@ def test_gelu_is_the_tanh_approximation_of_erf_gelu():
     assert d.max() > 4e-4
 
 
+# ---------------------------------------------------------------- SiLU (the SwiGLU gate)
+
+
+def test_silu_at_logs_of_rationals():
+    # sigmoid(ln a) = a / (1 + a) exactly, so silu(ln a) = ln a * a / (1 + a): a sign error in
+    # the exponent, or a product with (1 - sigmoid), fails these
+    for a in (2.0, 3.0, 4.0, 0.5, 1.0 / 3.0):
+        z = math.log(a)
+        assert abs(oracle.silu(np.array([z]))[0] - z * a / (1.0 + a)) < 1e-15
+
+
+def test_silu_limits_and_odd_part():
+    z = np.array([0.0, 40.0, -40.0])
+    v = oracle.silu(z)
+    assert v[0] == 0.0 and abs(v[1] - 40.0) < 1e-12 and abs(v[2]) < 1e-12
+    # silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1)
+    zz = np.linspace(-12, 12, 2401)
+    assert np.max(np.abs(oracle.silu(zz) - oracle.silu(-zz) - zz)) < 1e-13
+    # and it is not the GELU: they differ by ~0.11 at z = 1
+    assert abs(oracle.silu(np.array([1.0]))[0] - oracle.gelu_tanh(np.array([1.0]))[0]) > 0.1
+
+
+def test_swiglu_one_hot_and_gate_rows_first():
+    H, I = 128, 64
+    N = 2 * I
+    packed = np.tile(np.array([0x76543210, 0xFEDCBA98], np.uint32), (N, H // 16))
+    s = np.array([[bf16_bits((n + 1) / 16.0)] * (H // 64) for n in range(N)], np.uint16)
+    b = np.zeros((N, H // 64), np.uint16)
+    d = dict(H=H, I=I, Wgu=packed[None], Sgu=s[None], Bgu=b[None])
+    for i in (0, 9, 64, 127):
+        x = np.zeros(H, np.uint16)
+        x[i] = bf16_bits(1.0)
+        h = oracle.expert_geglu(x, 0, d, activation="silu")
+        g = np.array([(n + 1) * (i % 16) / 16.0 for n in range(I)])
+        u = np.array([(I + n + 1) * (i % 16) / 16.0 for n in range(I)])
+        assert np.allclose(h, oracle.silu(g) * u, rtol=1e-15, atol=0)
+    # gate rows 2^-6, up rows 2^-7, x = ones -> g = 2, u = 1: h = silu(2) = 2 / (1 + e^-2)
+    packed, s, b = _const_rows(2 * I, H, [2.0**-6] * I + [2.0**-7] * I)
+    d = dict(H=H, I=I, Wgu=packed[None], Sgu=s[None], Bgu=b[None])
+    h = oracle.expert_geglu(np.full(H, bf16_bits(1.0), np.uint16), 0, d, activation="silu")
+    assert np.allclose(h, 2.0 / (1.0 + math.exp(-2.0)), rtol=1e-15)
+
+
+def test_swiglu_sorted_route_equals_direct_definition_tiny():
+    d = synth.make("tiny")
+    r = oracle.layer(d, activation="silu")
+    y_direct = oracle.moe_layer_tokens(d, np.arange(d["T"]), activation="silu")
+    assert np.max(np.abs(r["y"] - y_direct)) < 1e-12
+    r_g = oracle.layer(d)
+    assert np.max(np.abs(r["y"] - r_g["y"])) > 1e-3  # a different layer from the GeGLU one
+
+
 def test_round_bf16_ties_to_even():
     v = np.array([1.0 + 2.0**-8, 1.0 + 3 * 2.0**-8, -(1.0 + 2.0**-8), 1.0 + 2.0**-9, 3.0])
     r = oracle.round_bf16(v)
