@@ -171,7 +171,8 @@ def run_reference(args, world, rank):
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
-        r = oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks)
+        r = oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks,
+                         activation=args.activation)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             times.append(dt)
@@ -202,7 +203,7 @@ def workload_name(name, cfg):
             f"A={cfg['T'] * cfg['k']}, 4-bit gs64 affine, bf16 scales/biases, router={cfg['router']}")
 
 
-def cpu_baseline(d, seconds):
+def cpu_baseline(d, seconds, activation="gelu_tanh"):
     """The oracle, as it stands, timed on the host cores on whole tokens of the workload."""
     import oracle
     toks_all = np.arange(d["T"], dtype=np.int32)
@@ -214,7 +215,7 @@ def cpu_baseline(d, seconds):
     while True:
         toks = np.sort(rng.choice(toks_all, size=min(n, d["T"]), replace=False)).astype(np.int32)
         t1 = time.perf_counter()
-        oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks)
+        oracle.layer(d, slots=np.zeros(0, np.int32), tokens=toks, activation=activation)
         elapsed += time.perf_counter() - t1
         done_tokens += toks.size
         if time.perf_counter() - t0 > seconds or done_tokens >= 64 * d["T"]:
@@ -240,6 +241,9 @@ def main():
                          "four calls with the library's own variant choice (auto); "
                          "fused: the one-launch layer (decode-sized calls)")
     ap.add_argument("--tile-m", type=int, default=128)
+    ap.add_argument("--activation", default="gelu_tanh", choices=["gelu_tanh", "silu"],
+                    help="the gate activation: gelu_tanh (GeGLU, the Gemma-4 experts) or silu "
+                         "(SwiGLU)")
     ap.add_argument("--deterministic", action="store_true",
                     help="the fixed-order un-sort (per-assignment rows, ordered k-sum)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -302,7 +306,7 @@ def main():
 
     def step(ev=None):
         if use_fused:
-            mq.moe_layer_fused(x, ids, tw, W, E, buf, stream)
+            mq.moe_layer_fused(x, ids, tw, W, E, buf, stream, args.activation)
             if ev is not None:
                 for e in ev:
                     e.record(stream)
@@ -312,12 +316,9 @@ def main():
                                     r.offsets, r.tiles, r.tile_count, r.status, stream)
         if ev is not None:
             ev[0].record(stream)
-        if use_ws:  # the tensor-core variant loads tile rows from the sorted copy of x
-            mq.moe_gather_qmm_geglu_ws(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.x_sorted,
-                                       buf.h, variant, stream)
-        else:
-            mq.moe_gather_qmm_geglu(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.h, variant,
-                                    stream)
+        # (the tensor-core variant loads tile rows from the sorted copy of x)
+        mq.moe_gather_qmm_glu(x, W["Wgu"], W["Sgu"], W["Bgu"], r, H, I, buf.h, args.activation,
+                              buf.x_sorted if use_ws else None, variant, stream)
         if ev is not None:
             ev[1].record(stream)
         mq.moe_gather_qmm_down_unsort(buf.h, W["Wd"], W["Sd"], W["Bd"], r, tw, H, I, buf.y_acc,
@@ -419,7 +420,7 @@ def main():
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_name(args.config, cfg), "assignments": A,
                    "experts_touched": touched, "tile_m": args.tile_m, "variant": args.variant,
-                   "path": path,
+                   "path": path, "activation": args.activation,
                    "unsort": "deterministic (per-assignment rows, fixed-order k-sum)"
                              if args.deterministic else "fp32 atomics",
                    "l2": "flushed between steps outside the timed events: 512 MB write, "
@@ -453,7 +454,7 @@ def main():
         "wall_s_timed": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(d, args.cpu_seconds, args.activation)
     elif rank == 0:
         line["cpu_baseline"] = None
     if world > 1:

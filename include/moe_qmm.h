@@ -79,6 +79,12 @@ typedef enum {
   MOE_VARIANT_TC = 2    /* tcgen05 tensor-core grouped GEMM */
 } moe_variant;
 
+/* The gate activation of the gated product h = act(gate) * up. */
+typedef enum {
+  MOE_ACT_GELU_TANH = 0, /* geluApproximate, the tanh form (GeGLU; the Gemma-4 experts) */
+  MOE_ACT_SILU = 1       /* z * sigmoid(z) (SwiGLU) */
+} moe_activation;
+
 #define MOE_MAX_EXPERTS 256
 
 /*
@@ -221,6 +227,23 @@ moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_t *Wgu, con
                                    moe_bf16_t *h, cudaStream_t stream);
 
 /*
+ * The gated product with either gate activation (SharpAI/SwiftLM issue #236: "What #27 set
+ * out to do", item 2, fuses both the silu-mul and the gelu-mul products; "Already on main"
+ * names compiledSiluProduct and SwitchGLU's activationProduct).  The arguments and result
+ * of moe_gather_qmm_geglu_ws, plus
+ *   activation   MOE_ACT_GELU_TANH: h = gelu_tanh(g) * u (exactly moe_gather_qmm_geglu_ws);
+ *                MOE_ACT_SILU: h = silu(g) * u, silu(z) = z / (1 + exp(-z)), evaluated in
+ *                fp32 as 0.5 z (1 + tanh(z / 2)) with the hardware tanh;
+ *                other values: MOE_ERR_INVALID_ARG
+ *   x_sorted_ws  as for moe_gather_qmm_geglu_ws, or NULL: the tensor-core variant then
+ *                gathers the activation rows inside the GEMM (as moe_gather_qmm_geglu)
+ */
+moe_status moe_gather_qmm_glu(const moe_bf16_t *x, const uint32_t *Wgu, const moe_bf16_t *Sgu,
+                              const moe_bf16_t *Bgu, const moe_tiles_t *tiles, int32_t hidden,
+                              int32_t inter, int32_t variant, int32_t activation,
+                              moe_bf16_t *x_sorted_ws, moe_bf16_t *h, cudaStream_t stream);
+
+/*
  * Steps a7-a8 -- gathered 4-bit down projection whose epilogue does the
  * router-weighted scatter-add back into token order (SharpAI/SwiftLM issue
  * #236, "Already on main": weightedExpertSum; Layr-Labs/mlx PR #4,
@@ -308,8 +331,9 @@ moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_
  *   as there; status: the device status word;
  *   h [A, I] bf16 out (sorted-slot order); y_acc_ws: a workspace of
  *   moe_unsort_workspace_bytes(T, k, H, deterministic) bytes, zero on entry and left zero
- *   (deterministic: its counters), as for moe_gather_qmm_down_unsort; deterministic: 0 or 1,
- *   the un-sort mode of moe_gather_qmm_down_unsort; y [T, H] bf16 out.
+ *   (deterministic: its counters), as for moe_gather_qmm_down_unsort; activation: the gate
+ *   activation, as for moe_gather_qmm_glu; deterministic: 0 or 1, the un-sort mode of
+ *   moe_gather_qmm_down_unsort; y [T, H] bf16 out.
  * Limits: A = T*k <= 256, T <= 64, H and I multiples of 64 whose padded packed rows fit one
  * copy (K/2 + padding <= 2048 bytes); other calls return MOE_ERR_UNSUPPORTED before any
  * launch (use the four calls).  The launch is cooperative (one CTA per SM, all resident at
@@ -323,8 +347,8 @@ moe_status moe_layer_fused(const int32_t *topk_ids, const float *topk_weights, i
                            int32_t hidden, int32_t inter, int32_t tile_m, int32_t max_tiles,
                            int32_t *sorted_ids, int32_t *perm, int32_t *counts, int32_t *offsets,
                            int32_t *tiles, int32_t *tile_count, int32_t *status, moe_bf16_t *h,
-                           float *y_acc_ws, int32_t deterministic, moe_bf16_t *y,
-                           cudaStream_t stream);
+                           float *y_acc_ws, int32_t activation, int32_t deterministic,
+                           moe_bf16_t *y, cudaStream_t stream);
 
 /*
  * MOE_OK if moe_layer_fused takes a call of this shape (T tokens, top-k, E experts, hidden,

@@ -11,6 +11,7 @@ Entry points (same names as the C ABI):
 * :func:`moe_sort_assignments`        top-k ids -> sorted ids, permutation, counts
 * :func:`moe_build_expert_tiles`      sorted ids -> offsets, tile descriptors, count
 * :func:`moe_gather_qmm_geglu`        gathered 4-bit gate/up + gelu_tanh(gate) * up -> h
+* :func:`moe_gather_qmm_glu`          the same with a choice of gate activation (SwiGLU)
 * :func:`moe_gather_qmm_down_unsort`  gathered 4-bit down + weighted un-sort -> y
 
 and :func:`moe_layer`, which runs the four on fresh output buffers.
@@ -29,6 +30,8 @@ LIB_PATH = os.path.join(_HERE, "libmoeqmm.so")
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA = 0, 1, 2, 3
 MOE_ERR_UNSORTED, MOE_ERR_RANGE, MOE_ERR_TIMEOUT = 4, 5, 6
 VARIANT_AUTO, VARIANT_GEMV, VARIANT_TC = 0, 1, 2
+ACT_GELU_TANH, ACT_SILU = 0, 1  # the gate activation of the gated product (GeGLU, SwiGLU)
+ACTIVATIONS = {"gelu_tanh": ACT_GELU_TANH, "silu": ACT_SILU}
 MAX_EXPERTS = 256
 
 # every symbol include/moe_qmm.h declares
@@ -36,7 +39,7 @@ ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
                "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc",
                "moe_sort_and_build_tiles", "moe_layer_fused", "moe_layer_fused_supported",
-               "moe_gather_qmm_geglu_ws", "moe_unsort_workspace_bytes")
+               "moe_gather_qmm_geglu_ws", "moe_unsort_workspace_bytes", "moe_gather_qmm_glu")
 NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
@@ -90,11 +93,14 @@ def load(build_if_needed: bool = True):
         lib.moe_gather_qmm_down_unsort_noalloc.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles),
                                                            p, i32, i32, i32, i32, p, p]
         lib.moe_layer_fused.argtypes = [p, p, i32, i32, i32, p, p, p, p, p, p, p, i32, i32, i32,
-                                        i32, p, p, p, p, p, p, p, p, p, i32, p, p]
+                                        i32, p, p, p, p, p, p, p, p, p, i32, i32, p, p]
         lib.moe_layer_fused_supported.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.moe_gather_qmm_geglu_ws.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32,
                                                 i32, p, p, p]
         lib.moe_gather_qmm_geglu_ws.restype = ctypes.c_int
+        lib.moe_gather_qmm_glu.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32, i32,
+                                           i32, p, p, p]
+        lib.moe_gather_qmm_glu.restype = ctypes.c_int
         lib.moe_layer_fused_supported.restype = ctypes.c_int
         for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_sort_and_build_tiles",
                    "moe_gather_qmm_geglu", "moe_layer_fused",
@@ -234,6 +240,25 @@ def moe_gather_qmm_geglu_ws(x, Wgu, Sgu, Bgu, routing, hidden, inter, x_sorted_w
         _bf16(x_sorted_ws, "x_sorted_ws", routing.A * hidden), _bf16(h, "h"), _stream(stream)))
 
 
+def _activation(activation) -> int:
+    if isinstance(activation, str):
+        if activation not in ACTIVATIONS:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"unknown activation {activation!r}")
+        return ACTIVATIONS[activation]
+    return int(activation)
+
+
+def moe_gather_qmm_glu(x, Wgu, Sgu, Bgu, routing, hidden, inter, h, activation="gelu_tanh",
+                       x_sorted_ws=None, variant=VARIANT_AUTO, stream=None):
+    """The gated product with either gate activation ("gelu_tanh": GeGLU, "silu": SwiGLU);
+    x_sorted_ws ([A, hidden] bf16) is optional (the tensor-core variant's sorted rows)."""
+    _check(load().moe_gather_qmm_glu(
+        _bf16(x, "x"), _ptr(Wgu, torch.int32, "Wgu"), _bf16(Sgu, "Sgu"), _bf16(Bgu, "Bgu"),
+        _tiles_arg(routing), hidden, inter, variant, _activation(activation),
+        _bf16(x_sorted_ws, "x_sorted_ws", routing.A * hidden) if x_sorted_ws is not None
+        else None, _bf16(h, "h"), _stream(stream)))
+
+
 def moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y_acc_ws, y,
                                variant=VARIANT_AUTO, stream=None, deterministic=False):
     """deterministic: y_acc_ws holds one fp32 row per assignment and y is the fixed-order sum
@@ -287,7 +312,8 @@ def fused_layer_fits(num_tokens, top_k, num_experts, hidden, inter, tile_m=128) 
                                             tile_m) == MOE_OK
 
 
-def moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, buffers, stream=None):
+def moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, buffers, stream=None,
+                    activation="gelu_tanh"):
     """The whole layer of a decode-sized call in one launch (writes the same buffers as the
     four calls).  Raises MoeError(MOE_ERR_UNSUPPORTED) for calls beyond its limits."""
     T, k = topk_ids.shape
@@ -307,15 +333,18 @@ def moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, buffers, st
         _ptr(r.tiles, torch.int32, "tiles", 3 * r.max_tiles),
         _ptr(r.tile_count, torch.int32, "tile_count", 1), _ptr(r.status, torch.int32, "status", 1),
         _bf16(buffers.h, "h"), _ptr(buffers.y_acc, torch.float32, "y_acc_ws"),
-        1 if buffers.deterministic else 0, _bf16(buffers.y, "y"), _stream(stream)))
+        _activation(activation), 1 if buffers.deterministic else 0, _bf16(buffers.y, "y"),
+        _stream(stream)))
 
 
 def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, variant=VARIANT_AUTO,
-              buffers=None, stream=None, fused_route=False, fused=False, deterministic=None):
+              buffers=None, stream=None, fused_route=False, fused=False, deterministic=None,
+              activation="gelu_tanh"):
     """Run the four calls on one stream (fused: the one-launch layer).  ``weights``: dict of
     Wgu, Sgu, Bgu, Wd, Sd, Bd device tensors (uint32 data as int32, bf16 scales/biases).
     deterministic: the fixed-order un-sort (default: the mode the buffers were made for,
-    else False).  Returns the buffers."""
+    else False).  activation: the gate activation, "gelu_tanh" (GeGLU) or "silu" (SwiGLU).
+    Returns the buffers."""
     T, k = topk_ids.shape
     H = x.shape[1]
     I = weights["Wd"].shape[2] * 8
@@ -327,7 +356,7 @@ def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, varia
     r = b.routing
     r.status.zero_()
     if fused:
-        moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, b, stream)
+        moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, b, stream, activation)
         return b
     if fused_route:
         moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, r.sorted_ids, r.perm, r.counts,
@@ -337,13 +366,11 @@ def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, varia
                              stream)
         moe_build_expert_tiles(r.sorted_ids, num_experts, tile_m, r.offsets, r.tiles,
                                r.tile_count, r.status, stream)
-    if variant == VARIANT_GEMV or (variant == VARIANT_AUTO and
-                                   r.A <= 16 * min(num_experts, r.A)):
-        moe_gather_qmm_geglu(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I, b.h,
-                             variant, stream)
-    else:  # the tensor-core variant loads the tiles' rows from the sorted copy
-        moe_gather_qmm_geglu_ws(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I,
-                                b.x_sorted, b.h, variant, stream)
+    gemv = variant == VARIANT_GEMV or (variant == VARIANT_AUTO and
+                                       r.A <= 16 * min(num_experts, r.A))
+    # the tensor-core variant loads the tiles' rows from the sorted copy
+    moe_gather_qmm_glu(x, weights["Wgu"], weights["Sgu"], weights["Bgu"], r, H, I, b.h,
+                       activation, None if gemv else b.x_sorted, variant, stream)
     moe_gather_qmm_down_unsort(b.h, weights["Wd"], weights["Sd"], weights["Bd"], r, topk_weights,
                                H, I, b.y_acc, b.y, variant, stream, b.deterministic)
     return b

@@ -71,4 +71,16 @@ __device__ __forceinline__ float gelu_tanh(float z) {
   return 0.5f * z * (1.0f + tanh_approx(inner));
 }
 
+// SiLU, z * sigmoid(z), with sigmoid(z) = (1 + tanh(z / 2)) / 2: the gate activation of the
+// SwiGLU product (SharpAI/SwiftLM issue #236, "What #27 set out to do" and "Already on
+// main": the silu-mul product), on the same hardware tanh.
+__device__ __forceinline__ float silu_f(float z) {
+  return 0.5f * z * (1.0f + tanh_approx(0.5f * z));
+}
+
+// the gate activation of the gated product: MOE_ACT_GELU_TANH or MOE_ACT_SILU
+__device__ __forceinline__ float glu_act(float z, int act) {
+  return act == MOE_ACT_SILU ? silu_f(z) : gelu_tanh(z);
+}
+
 }  // namespace moeqmm

@@ -1,5 +1,6 @@
 // The whole expert layer of a decode-sized call in one launch: routing (steps a1, a2),
-// gate/up + GeGLU (a3-a6) and down + weighted un-sort (a7, a8), the GEMV-style variant (a9).
+// gate/up + GeGLU or SwiGLU (a3-a6) and down + weighted un-sort (a7, a8), the GEMV-style
+// variant (a9).
 //
 // Per-call kernels pay, at each of their boundaries, for the grid to drain, the next one to
 // start, and a start-up chain of dependent loads (status, tile count, tiles, first copy).
@@ -81,6 +82,7 @@ struct FArgs {
   const float *topk_weights;
   const uint16_t *x, *Sgu, *Bgu, *Sd, *Bd;
   int32_t T, k, A, E, H, I, BM, max_tiles, nbuf;
+  int32_t act;  // the gate activation of the gated product (MOE_ACT_*)
   int32_t *sorted_ids, *perm, *counts, *offsets, *tiles, *tile_count, *status;
   uint16_t *h;
   float *y_acc;
@@ -491,7 +493,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
             if (jr >= Rp) continue;
             const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
             p.h[(int64_t)(row0 + r0 + jr) * p.I + n] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
+                __bfloat16_as_ushort(__float2bfloat16_rn(glu_act(acc[c], p.act) * acc[2 + c]));
           }
         }
       }
@@ -701,7 +703,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
                               int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
                               int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
                               int32_t *tile_count, int32_t *status, uint16_t *h, float *y_acc,
-                              bool det, uint16_t *y, cudaStream_t stream) {
+                              int32_t act, bool det, uint16_t *y, cudaStream_t stream) {
   const char *what = "moe_layer_fused";
   const int A = T * k;
   const int nbuf = fused_nbuf(H, I, T, A, E, max_tiles);
@@ -736,6 +738,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   a.BM = tile_m;
   a.max_tiles = max_tiles;
   a.nbuf = nbuf;
+  a.act = act;
   a.sorted_ids = sorted_ids;
   a.perm = perm;
   a.counts = counts;

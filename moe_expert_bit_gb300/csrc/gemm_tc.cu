@@ -3,7 +3,8 @@
 // quantized matmul per sorted expert tile, affine 4-bit group-64 weights,
 // bf16 activations).  Two modes share the kernel:
 //
-//   GEGLU: h[s, n] = gelu_tanh(sum_k Wg[e][n][k] x[t_s][k]) * sum_k Wu[e][n][k] x[t_s][k]
+//   GEGLU: h[s, n] = act(sum_k Wg[e][n][k] x[t_s][k]) * sum_k Wu[e][n][k] x[t_s][k]
+//          (act = gelu_tanh, or silu for the SwiGLU product)
 //          (SharpAI/SwiftLM issue #236, "Still missing": the GeGLU product fused
 //          into one dispatch; here it is the GEMM epilogue)
 //   DOWN:  y_acc[t_s, n] += w_s * sum_i Wd[e][n][i] h[s][i]
@@ -104,6 +105,7 @@ struct Params {
   int32_t num_blocks;       // n-blocks per tile: I/64 (GEGLU) or ceil(H/128) (DOWN)
   int32_t x_sorted;         // GEGLU: x is [A, H] in sorted-slot order (contiguous boxes)
   int32_t per_slot;         // DOWN: y_acc is [A, H], one row per assignment, stored (not added)
+  int32_t act;              // GEGLU: the gate activation (MOE_ACT_*)
 };
 
 struct Smem {
@@ -419,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float g = odd ? other : mine;
             const float uu = odd ? mine : other;
             if ((j & 1) == odd && c0 + j < U.R) {
-              const float hv = gelu_tanh(g) * uu;
+              const float hv = glu_act(g, p.act) * uu;
               p.h[(int64_t)(U.row0 + c0 + j) * p.N_out + n] =
                   __bfloat16_as_ushort(__float2bfloat16_rn(hv));
             }
@@ -597,8 +599,8 @@ moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m) {
 
 moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                            const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
-                           uint16_t *h, cudaStream_t stream) {
-  const char *what = "moe_gather_qmm_geglu (tensor cores)";
+                           int32_t act, uint16_t *h, cudaStream_t stream) {
+  const char *what = "moe_gather_qmm_glu (tensor cores)";
   CUtensorMap mw, mx;
   if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wgu, H / 8,
                        (uint64_t)t.num_experts * 2 * I, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -622,13 +624,15 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
   p.N_out = I;
   p.rows_per_expert = 2 * I;
   p.num_blocks = I / 64;
+  p.act = act;
   return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
 }
 
 moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                                   const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
-                                  uint16_t *x_sorted, uint16_t *h, cudaStream_t stream) {
-  const char *what = "moe_gather_qmm_geglu_ws (tensor cores)";
+                                  int32_t act, uint16_t *x_sorted, uint16_t *h,
+                                  cudaStream_t stream) {
+  const char *what = "moe_gather_qmm_glu (tensor cores, sorted rows)";
   const int row_u4 = H / 8;
   int blocks = (int)(((int64_t)t.num_assignments * row_u4 + 255) / 256);
   if (blocks > tc::num_sms() * 8) blocks = tc::num_sms() * 8;
@@ -661,6 +665,7 @@ moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const 
   p.N_out = I;
   p.rows_per_expert = 2 * I;
   p.num_blocks = I / 64;
+  p.act = act;
   p.x_sorted = 1;
   return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
 }

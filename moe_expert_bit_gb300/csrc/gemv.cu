@@ -3,7 +3,8 @@
 // packed 4-bit weights from HBM, so what counts is the work per weight on
 // the CUDA cores and on shared memory, not matrix throughput.
 //
-//   gate/up:  h[s, n] = gelu_tanh(sum_k Wg[e][n][k] x_s[k]) * sum_k Wu[e][n][k] x_s[k]
+//   gate/up:  h[s, n] = act(sum_k Wg[e][n][k] x_s[k]) * sum_k Wu[e][n][k] x_s[k],
+//             act = gelu_tanh (GeGLU) or silu (SwiGLU)
 //   down:     y_acc[t, n] += w_a * sum_i Wd[e][n][i] h[s, i],  a = perm[s], t = a / top_k
 //             (deterministic: o[a, n] = w_a * sum_i ..., then y[t] = o[t k] + ... + o[t k + k - 1]
 //             in that order)
@@ -113,6 +114,7 @@ struct GemvArgs {
   const float *topk_weights;
   int32_t *status;
   int32_t T, A, top_k, H, I, ktok, nbuf, nxrows, whole;
+  int32_t gate_act;  // gate/up: the gate activation (MOE_ACT_*)
   uint16_t *h;
   float *y_acc;
   int32_t *cnt;  // DOWN: per-16-column counters (fused cast), or null
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(GemvCfg<MODE>::kThreads, 1)
           if (MODE == 0) {
             const int n = 8 * j + gq;  // acc[c]: gate, acc[2 + c]: up
             p.h[(int64_t)(row0 + r0 + jr) * p.I + n] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(gelu_tanh(acc[c]) * acc[2 + c]));
+                __bfloat16_as_ushort(__float2bfloat16_rn(glu_act(acc[c], p.gate_act) * acc[2 + c]));
           } else if (DET) {  // this assignment's own row of the workspace
             float *orow = p.y_acc + (int64_t)a_c[c] * p.H + Cfg::kRows * j + row_lo;
             __stcg(orow + gq, w_c[c] * acc[c]);
@@ -573,7 +575,8 @@ template <int MODE, bool DET>
 static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const uint16_t *Sc,
                                  const uint16_t *Bi, const moe_tiles_t &t, const float *tw,
                                  int32_t H, int32_t I, uint16_t *h, float *y_acc, uint16_t *y,
-                                 bool fused_cast, cudaStream_t stream, const char *what) {
+                                 bool fused_cast, int32_t gate_act, cudaStream_t stream,
+                                 const char *what) {
   using Cfg = GemvCfg<MODE>;
   const int K = MODE == 0 ? H : I;
   const int T = t.num_tokens, A = t.num_assignments;
@@ -626,7 +629,7 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   int grid = sm_count();
   if (max_chunks < grid) grid = (int)(max_chunks > 0 ? max_chunks : 1);
   GemvArgs a;
-  a.act = act;
+  a.gate_act = gate_act;
   a.Sc = Sc;
   a.Bi = Bi;
   a.tiles = t.tiles;
@@ -643,6 +646,7 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
   a.nbuf = nbuf;
   a.nxrows = nxrows;
   a.whole = whole;
+  a.act = act;
   a.h = h;
   a.y_acc = y_acc;
   // the column-block counters follow the accumulator in the workspace: T x H, or one row
@@ -657,9 +661,9 @@ static moe_status launch_persist(const uint16_t *act, const uint32_t *Wq, const 
 
 moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
-                             uint16_t *h, cudaStream_t stream) {
+                             int32_t act, uint16_t *h, cudaStream_t stream) {
   return launch_persist<0, false>(x, Wgu, Sgu, Bgu, t, nullptr, H, I, h, nullptr, nullptr,
-                                  false, stream, "moe_gather_qmm_geglu (gemv)");
+                                  false, act, stream, "moe_gather_qmm_glu (gemv)");
 }
 
 moe_status launch_down_gemv(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
@@ -669,9 +673,9 @@ moe_status launch_down_gemv(const uint16_t *hin, const uint32_t *Wd, const uint1
   const char *what = "moe_gather_qmm_down_unsort (gemv)";
   if (det)
     return launch_persist<1, true>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y,
-                                   fused_cast, stream, what);
+                                   fused_cast, 0, stream, what);
   return launch_persist<1, false>(hin, Wd, Sd, Bd, t, topk_weights, H, I, nullptr, y_acc, y,
-                                  fused_cast, stream, what);
+                                  fused_cast, 0, stream, what);
 }
 
 moe_status launch_cast_bf16(float *y_acc, uint16_t *y, int64_t n, const int32_t *status,

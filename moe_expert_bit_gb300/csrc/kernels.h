@@ -7,9 +7,10 @@
 
 namespace moeqmm {
 
+// act: the gate activation of the gated product (MOE_ACT_GELU_TANH or MOE_ACT_SILU)
 moe_status launch_geglu_gemv(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                              const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
-                             uint16_t *h, cudaStream_t stream);
+                             int32_t act, uint16_t *h, cudaStream_t stream);
 // fused_cast: the kernel also writes y = bf16(y_acc), each 16-column block as soon as
 // its last contribution lands, and clears the block; y_acc [T, H] is then followed by
 // H/16 int counters (the workspace layout of moe_workspace_bytes), zero on entry and
@@ -37,16 +38,17 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
                               int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids,
                               int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
                               int32_t *tile_count, int32_t *status, uint16_t *h, float *y_acc,
-                              bool det, uint16_t *y, cudaStream_t stream);
+                              int32_t act, bool det, uint16_t *y, cudaStream_t stream);
 moe_status tc_supported(int32_t H, int32_t I, int32_t tile_m);
 bool gemv_supported(int32_t H, int32_t I);
 moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                            const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
-                           uint16_t *h, cudaStream_t stream);
+                           int32_t act, uint16_t *h, cudaStream_t stream);
 // GEGLU through a workspace: x gathered into sorted-slot order first ([A, H] bf16)
 moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
                                   const uint16_t *Bgu, const moe_tiles_t &t, int32_t H, int32_t I,
-                                  uint16_t *x_sorted, uint16_t *h, cudaStream_t stream);
+                                  int32_t act, uint16_t *x_sorted, uint16_t *h,
+                                  cudaStream_t stream);
 moe_status launch_down_tc(const uint16_t *h, const uint32_t *Wd, const uint16_t *Sd,
                           const uint16_t *Bd, const moe_tiles_t &t, const float *topk_weights,
                           int32_t H, int32_t I, float *y_acc, bool per_slot,

@@ -101,23 +101,38 @@ static moe_status resolve_variant(const char *fn, const moe_tiles_t *t, int32_t 
 
 using namespace moeqmm;
 
-extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu,
-                                           const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
-                                           const moe_tiles_t *tiles, int32_t H, int32_t I,
-                                           int32_t variant, moe_bf16_t *h, cudaStream_t stream) {
-  const char *fn = "moe_gather_qmm_geglu";
+static moe_status glu_call(const char *fn, const moe_bf16_t *x, const uint32_t *Wgu,
+                           const moe_bf16_t *Sgu, const moe_bf16_t *Bgu, const moe_tiles_t *tiles,
+                           int32_t H, int32_t I, int32_t variant, int32_t act,
+                           moe_bf16_t *x_sorted_ws, moe_bf16_t *h, cudaStream_t stream) {
   clear_error();
   moe_status st = validate_tiles(fn, tiles);
   if (st != MOE_OK) return st;
   if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
+  if (act != MOE_ACT_GELU_TANH && act != MOE_ACT_SILU) {
+    set_error("%s: unknown activation %d", fn, act);
+    return MOE_ERR_INVALID_ARG;
+  }
   if (!x || !Wgu || !Sgu || !Bgu || !h) {
     set_error("%s: null pointer", fn);
     return MOE_ERR_INVALID_ARG;
   }
   if ((st = validate_aligned(fn, {x, Wgu, Sgu, Bgu, h})) != MOE_OK) return st;
+  if (x_sorted_ws && (st = validate_aligned(fn, {x_sorted_ws})) != MOE_OK) return st;
   if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
-  if (variant == MOE_VARIANT_TC) return launch_geglu_tc(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
-  return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
+  if (variant == MOE_VARIANT_TC)
+    return x_sorted_ws
+               ? launch_geglu_tc_sorted(x, Wgu, Sgu, Bgu, *tiles, H, I, act, x_sorted_ws, h, stream)
+               : launch_geglu_tc(x, Wgu, Sgu, Bgu, *tiles, H, I, act, h, stream);
+  return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, act, h, stream);
+}
+
+extern "C" moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu,
+                                           const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
+                                           const moe_tiles_t *tiles, int32_t H, int32_t I,
+                                           int32_t variant, moe_bf16_t *h, cudaStream_t stream) {
+  return glu_call("moe_gather_qmm_geglu", x, Wgu, Sgu, Bgu, tiles, H, I, variant,
+                  MOE_ACT_GELU_TANH, nullptr, h, stream);
 }
 
 extern "C" moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_t *Wgu,
@@ -125,20 +140,23 @@ extern "C" moe_status moe_gather_qmm_geglu_ws(const moe_bf16_t *x, const uint32_
                                               const moe_tiles_t *tiles, int32_t H, int32_t I,
                                               int32_t variant, moe_bf16_t *x_sorted_ws,
                                               moe_bf16_t *h, cudaStream_t stream) {
-  const char *fn = "moe_gather_qmm_geglu_ws";
-  clear_error();
-  moe_status st = validate_tiles(fn, tiles);
-  if (st != MOE_OK) return st;
-  if ((st = validate_dims(fn, H, I, variant)) != MOE_OK) return st;
-  if (!x || !Wgu || !Sgu || !Bgu || !x_sorted_ws || !h) {
-    set_error("%s: null pointer", fn);
+  if (!x_sorted_ws) {
+    clear_error();
+    set_error("moe_gather_qmm_geglu_ws: null pointer");
     return MOE_ERR_INVALID_ARG;
   }
-  if ((st = validate_aligned(fn, {x, Wgu, Sgu, Bgu, x_sorted_ws, h})) != MOE_OK) return st;
-  if ((st = resolve_variant(fn, tiles, H, I, &variant)) != MOE_OK) return st;
-  if (variant == MOE_VARIANT_TC)
-    return launch_geglu_tc_sorted(x, Wgu, Sgu, Bgu, *tiles, H, I, x_sorted_ws, h, stream);
-  return launch_geglu_gemv(x, Wgu, Sgu, Bgu, *tiles, H, I, h, stream);
+  return glu_call("moe_gather_qmm_geglu_ws", x, Wgu, Sgu, Bgu, tiles, H, I, variant,
+                  MOE_ACT_GELU_TANH, x_sorted_ws, h, stream);
+}
+
+extern "C" moe_status moe_gather_qmm_glu(const moe_bf16_t *x, const uint32_t *Wgu,
+                                         const moe_bf16_t *Sgu, const moe_bf16_t *Bgu,
+                                         const moe_tiles_t *tiles, int32_t H, int32_t I,
+                                         int32_t variant, int32_t activation,
+                                         moe_bf16_t *x_sorted_ws, moe_bf16_t *h,
+                                         cudaStream_t stream) {
+  return glu_call("moe_gather_qmm_glu", x, Wgu, Sgu, Bgu, tiles, H, I, variant, activation,
+                  x_sorted_ws, h, stream);
 }
 
 namespace moeqmm {
@@ -213,11 +231,16 @@ extern "C" moe_status moe_layer_fused(
     const uint32_t *Wd, const moe_bf16_t *Sd, const moe_bf16_t *Bd, int32_t H, int32_t I,
     int32_t tile_m, int32_t max_tiles, int32_t *sorted_ids, int32_t *perm, int32_t *counts,
     int32_t *offsets, int32_t *tiles, int32_t *tile_count, int32_t *status, moe_bf16_t *h,
-    float *y_acc_ws, int32_t deterministic, moe_bf16_t *y, cudaStream_t stream) {
+    float *y_acc_ws, int32_t activation, int32_t deterministic, moe_bf16_t *y,
+    cudaStream_t stream) {
   const char *fn = "moe_layer_fused";
   clear_error();
   if (deterministic != 0 && deterministic != 1) {
     set_error("%s: deterministic must be 0 or 1 (got %d)", fn, deterministic);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (activation != MOE_ACT_GELU_TANH && activation != MOE_ACT_SILU) {
+    set_error("%s: unknown activation %d", fn, activation);
     return MOE_ERR_INVALID_ARG;
   }
   if (!topk_ids || !topk_weights || !x || !Wgu || !Sgu || !Bgu || !Wd || !Sd || !Bd ||
@@ -256,7 +279,8 @@ extern "C" moe_status moe_layer_fused(
   }
   return launch_fused_layer(topk_ids, topk_weights, T, k, E, x, Wgu, Sgu, Bgu, Wd, Sd, Bd, H, I,
                             tile_m, max_tiles, sorted_ids, perm, counts, offsets, tiles,
-                            tile_count, status, h, y_acc_ws, deterministic != 0, y, stream);
+                            tile_count, status, h, y_acc_ws, activation, deterministic != 0, y,
+                            stream);
 }
 
 extern "C" moe_status moe_layer_fused_supported(int32_t T, int32_t k, int32_t E, int32_t H,

@@ -130,10 +130,28 @@ def test_deterministic_flag_validation():
     assert "deterministic" in _raw().moe_last_error_string().decode()
 
 
+def test_activation_validation():
+    """The gate activation is MOE_ACT_GELU_TANH or MOE_ACT_SILU; anything else is refused
+    before a launch."""
+    t = _tiles()
+    for bad in (2, -1):
+        assert _raw().moe_gather_qmm_glu(16, 16, 16, 16, ctypes.byref(t), 128, 64, 0, bad, NULL,
+                                         16, NULL) == mq.MOE_ERR_INVALID_ARG
+        assert "activation" in _raw().moe_last_error_string().decode()
+        assert _raw().moe_layer_fused(*_fused_args(act=bad)) == mq.MOE_ERR_INVALID_ARG
+    # the glu call validates like the geglu call (the same shape errors)
+    assert _raw().moe_gather_qmm_glu(16, 16, 16, 16, ctypes.byref(t), 96, 64, 0, 1, NULL, 16,
+                                     NULL) == mq.MOE_ERR_UNSUPPORTED
+    assert _raw().moe_gather_qmm_geglu_ws(16, 16, 16, 16, ctypes.byref(t), 128, 64, 0, NULL,
+                                          16, NULL) == mq.MOE_ERR_INVALID_ARG
+    with pytest.raises(mq.MoeError):
+        mq._activation("relu")
+
+
 def _fused_args(**kw):
     a = dict(ids=1, w=1, T=4, k=8, E=128, x=16, Wgu=16, Sgu=16, Bgu=16, Wd=16, Sd=16, Bd=16,
              H=2816, I=704, tile_m=128, max_tiles=32, sorted=1, perm=1, counts=1, offsets=1,
-             tiles=1, tile_count=1, status=1, h=16, y_acc=16, det=0, y=16, stream=NULL)
+             tiles=1, tile_count=1, status=1, h=16, y_acc=16, act=0, det=0, y=16, stream=NULL)
     a.update(kw)
     return tuple(a.values())
 

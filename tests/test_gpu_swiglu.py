@@ -1,0 +1,90 @@
+"""GPU parity of the SwiGLU gate activation (h = silu(gate) * up) against the fp64 oracle.
+
+The same gathered 4-bit projections as the GeGLU layer with the other gate activation of the
+gated product: moe_gather_qmm_glu(activation = MOE_ACT_SILU) through both kernel variants,
+and the one-launch layer.  Bound: tests/_util.py (2e-2 * max(1, |oracle|) elementwise).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import bf16_to_f64, excess, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import moe_expert_bit_gb300 as mq  # noqa: E402
+
+VARIANTS = [mq.VARIANT_GEMV, mq.VARIANT_TC]
+
+
+def run(d, variant=mq.VARIANT_AUTO, tile_m=128, fused=False, activation="silu"):
+    dev = to_device(d)
+    b = mq.moe_layer(dev["x"], dev["topk_ids"], dev["topk_weights"], dev, d["E"], tile_m=tile_m,
+                     variant=variant, fused=fused, activation=activation)
+    torch.cuda.synchronize()
+    assert int(b.routing.status.item()) == 0
+    return b
+
+
+def compare(b, d, slots=None, tokens=None):
+    ref = oracle.layer(d, slots=slots, tokens=tokens, activation="silu")
+    out_rows = np.isin(np.arange(d["T"]), d["outlier_rows"])
+    h = bf16_to_f64(b.h) if slots is None else bf16_to_f64(b.h)[slots]
+    y = bf16_to_f64(b.y) if tokens is None else bf16_to_f64(b.y)[tokens]
+    slot_rows = out_rows[ref["perm"][ref["slots"]] // d["k"]]
+    assert excess(h, ref["h"], slot_rows) <= 1.0
+    assert excess(y, ref["y"], out_rows[ref["tokens"]]) <= 1.0
+    return ref
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_swiglu_layer_matches_oracle(variant, name):
+    d = synth.make(name)
+    compare(run(d, variant), d)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("E,H,I,T,k", [
+    (5, 192, 128, 37, 3),      # ragged everything, 3 K-groups
+    (1, 128, 64, 1, 1),        # one assignment
+    (3, 256, 192, 300, 2),     # tiles with many rows, ragged tail
+])
+def test_swiglu_custom_shapes(variant, E, H, I, T, k):
+    d = synth.make_custom(E, H, I, T, k, seed=6)
+    for tile_m in (16, 128):
+        compare(run(d, variant, tile_m), d)
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode"])
+def test_swiglu_one_launch_layer(name):
+    d = synth.make(name)
+    compare(run(d, fused=True), d)
+
+
+def test_swiglu_differs_from_geglu_and_the_one_launch_layer_matches_the_calls():
+    d = synth.make("decode")
+    b_s = run(d, mq.VARIANT_GEMV)
+    h_s = b_s.h.clone()
+    b_g = run(d, mq.VARIANT_GEMV, activation="gelu_tanh")
+    assert not torch.equal(h_s, b_g.h)
+    # same partition of every dot product: h bit for bit between the one-launch layer and
+    # the GEMV calls
+    b_f = run(d, fused=True)
+    assert torch.equal(b_f.h, h_s)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_swiglu_full_size_sampled(variant):
+    d = synth.make("prefill_uniform")
+    b = run(d, variant)
+    rng = np.random.default_rng(5)
+    A = d["T"] * d["k"]
+    slots = np.sort(rng.choice(A, size=16, replace=False)).astype(np.int32)
+    toks = np.sort(rng.choice(d["T"], size=6, replace=False)).astype(np.int32)
+    compare(b, d, slots=slots, tokens=toks)
