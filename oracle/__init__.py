@@ -69,6 +69,8 @@ def _load():
         lib.oracle_round_bf16.argtypes = [f64]
         lib.oracle_round_bf16.restype = f64
         lib.oracle_round_bf16_array.argtypes = [p, i64, p]
+        lib.oracle_router_topk.argtypes = [p, i32, i32, i32, p, p]
+        lib.oracle_router_topk.restype = ctypes.c_int
         lib.oracle_sort_assignments.argtypes = [p, i32, i32, i32, p, p, p]
         lib.oracle_sort_assignments.restype = ctypes.c_int
         lib.oracle_build_expert_tiles.argtypes = [p, i32, i32, i32, i32, p, p, p]
@@ -142,6 +144,19 @@ def round_bf16(v) -> np.ndarray:
     out = np.empty_like(v)
     _load().oracle_round_bf16_array(pv, v.size, out.ctypes.data_as(ctypes.c_void_p))
     return out
+
+
+def router_topk(logits, k: int):
+    """Router logits [T, E] (fp32) -> (status, topk_ids [T, k] int32, topk_weights [T, k]
+    fp32): the k largest logits per token, descending, ties to the lower expert id, and the
+    softmax over them."""
+    lg, pl = _c(logits, np.float32)
+    T, E = lg.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float32)
+    st = _load().oracle_router_topk(pl, T, E, k, ids.ctypes.data_as(ctypes.c_void_p),
+                                    w.ctypes.data_as(ctypes.c_void_p))
+    return int(st), ids, w
 
 
 def sort_assignments(topk_ids, E: int):

@@ -27,6 +27,10 @@
  *              router-weighted sum of each token's expert outputs.
  *  [P3-Meas]   Layr-Labs/mlx PR #4, "Measured standing": direct weighted
  *              un-sort back to token order.
+ *  [P2-TopK]   fengmk2/mlx-node activity, the perf(qwen3.5) change: a fused
+ *              top-16 candidate selection (with an argpartition fallback); here
+ *              the router's top-k of each token's expert logits and the softmax
+ *              over the chosen k, the step before the sort.
  *  [P1-Swi]    SharpAI/SwiftLM issue #236, "What #27 set out to do" (item 2,
  *              the silu-mul and gelu-mul products, compiledSwiGLU) and
  *              "Already on main" (compiledSiluProduct, SwitchGLU's
@@ -42,6 +46,9 @@
  *    w = scale * q + bias with the group g = k / 64;
  *  - geluApproximate is the tanh form 0.5 z (1 + tanh(sqrt(2/pi)(z + 0.044715 z^3)))
  *    (Hendrycks & Gimpel, "Gaussian Error Linear Units", 2016);
+ *  - router top-k: the k largest logits of a token in descending order, equal logits
+ *    in ascending expert id; the weights are the softmax over those k logits; a NaN or
+ *    +inf logit, or a token whose chosen logits are all -inf, is a range error;
  *  - SiLU is z * sigmoid(z) = z / (1 + exp(-z)) (Elfwing, Uchibe & Doya 2018; the
  *    swish of Ramachandran, Zoph & Le with beta = 1);
  *  - tile descriptors are {expert, row_begin, rows} with experts ascending,
@@ -123,6 +130,55 @@ double oracle_round_bf16(double v) {
   double m = frexp(v, &e); /* v = m * 2^e, 0.5 <= |m| < 1 */
   double r = nearbyint(ldexp(m, 8)); /* 8 significant bits; default mode is to-even */
   return ldexp(r, e - 8);
+}
+
+/* ---- the router's top-k and softmax, the step before a1 [P2-TopK] ---- */
+
+/*
+ * For each token t: the k experts with the largest logits[t][e], in descending logit order,
+ * equal logits in ascending e (a plain selection: k passes over the row, each taking the
+ * best expert not yet taken), and weights w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0) in
+ * fp64 over the k chosen logits l_0 >= l_1 >= ..., rounded to fp32.
+ * Returns ORACLE_ERR_RANGE (and writes nothing for that token) if a logit of the token is
+ * NaN or +inf or if its chosen logits are all -inf; the other tokens are still written.
+ */
+int oracle_router_topk(const float *logits, int32_t T, int32_t E, int32_t k, int32_t *topk_ids,
+                       float *topk_weights) {
+  int status = ORACLE_OK;
+  unsigned char *taken = (unsigned char *)malloc((size_t)(E > 0 ? E : 1));
+  double *chosen = (double *)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+  for (int32_t t = 0; t < T; ++t) {
+    const float *row = logits + (int64_t)t * E;
+    int bad = 0;
+    for (int32_t e = 0; e < E; ++e)
+      if (isnan(row[e]) || (isinf(row[e]) && row[e] > 0)) bad = 1;
+    if (bad) {
+      status = ORACLE_ERR_RANGE;
+      continue;
+    }
+    memset(taken, 0, (size_t)E);
+    for (int32_t j = 0; j < k; ++j) {
+      int32_t best = -1;
+      for (int32_t e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || (double)row[e] > (double)row[best]) best = e;
+      }
+      taken[best] = 1;
+      topk_ids[(int64_t)t * k + j] = best;
+      chosen[j] = (double)row[best];
+    }
+    if (isinf(chosen[0])) { /* every chosen logit is -inf */
+      status = ORACLE_ERR_RANGE;
+      continue;
+    }
+    double z = 0.0;
+    for (int32_t j = 0; j < k; ++j) z += exp(chosen[j] - chosen[0]);
+    for (int32_t j = 0; j < k; ++j)
+      topk_weights[(int64_t)t * k + j] = (float)(exp(chosen[j] - chosen[0]) / z);
+  }
+  free(chosen);
+  free(taken);
+  return status;
 }
 
 /* ---- a1: flatten + stable sort by expert [P3-What: sorted indices] ---- */

@@ -165,6 +165,61 @@ def test_round_bf16_ties_to_even():
 # ---------------------------------------------------------------- sort
 
 
+# ---------------------------------------------------------------- router top-k + softmax
+
+
+@pytest.mark.parametrize("T,E,k,seed", [(64, 8, 2, 0), (40, 128, 8, 1), (9, 256, 16, 2)])
+def test_router_topk_ids_against_a_lexicographic_sort(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    logits = np.round(rng.normal(size=(T, E)) * 4) / 4  # coarse grid: many ties
+    logits = logits.astype(np.float32)
+    st, ids, w = oracle.router_topk(logits, k)
+    assert st == oracle.OK
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -logits[t].astype(np.float64)))  # value desc, id asc
+        assert np.array_equal(ids[t], order[:k])
+        assert np.all(np.diff(w[t]) <= 0)  # weights follow the logits
+        assert abs(float(w[t].astype(np.float64).sum()) - 1.0) < 1e-6
+
+
+def test_router_softmax_closed_forms():
+    ln3 = math.log(3.0)
+    cases = [
+        ([ln3, 0.0, -50.0, -60.0], 2, [0.75, 0.25]),        # e^ln3 : e^0 = 3 : 1
+        ([0.5, 0.5, 0.5, 0.5], 4, [0.25] * 4),              # equal logits
+        ([2.0, -math.inf, 1.0, -math.inf], 1, [1.0]),        # k = 1: weight 1
+    ]
+    for row, k, want in cases:
+        st, ids, w = oracle.router_topk(np.array([row], np.float32), k)
+        assert st == oracle.OK
+        assert np.allclose(w[0], want, rtol=2e-7, atol=0), (row, w)
+    # shift invariance, on logits that stay exact in fp32 after the shift
+    row = np.array([[1.5, 0.25, -2.0, 0.75]], np.float32)
+    _, ids0, w0 = oracle.router_topk(row, 3)
+    _, ids1, w1 = oracle.router_topk(row + np.float32(64.0), 3)
+    assert np.array_equal(ids0, ids1) and np.allclose(w0, w1, rtol=1e-7, atol=0)
+    # a -inf logit is never chosen while finite ones remain; chosen -inf logits weigh 0
+    st, ids, w = oracle.router_topk(np.array([[-math.inf, 1.0, 2.0]], np.float32), 3)
+    assert st == oracle.OK and list(ids[0]) == [2, 1, 0] and w[0][2] == 0.0
+
+
+def test_router_range_errors():
+    for row in ([1.0, math.nan, 0.0], [1.0, math.inf, 0.0], [-math.inf, -math.inf, -math.inf]):
+        st, _, _ = oracle.router_topk(np.array([row], np.float32), 2)
+        assert st == oracle.ERR_RANGE
+
+
+def test_router_matches_the_input_generators_choice():
+    # the generator's top-k + softmax (a separate implementation, in fp64) on fp32-exact
+    # scores gives the same ids and the same fp32 weights
+    rng = np.random.default_rng(3)
+    scores = rng.normal(size=(50, 128)).astype(np.float32)
+    ids_g, w_g = synth.topk_softmax(scores.astype(np.float64), 8)
+    st, ids, w = oracle.router_topk(scores, 8)
+    assert st == oracle.OK
+    assert np.array_equal(ids, ids_g) and np.array_equal(w, w_g)
+
+
 def test_sort_hand_worked_example():
     g = _golden("tiles_example.json")["sort_example"]
     st, sid, perm, counts = oracle.sort_assignments(np.array(g["topk_ids"]), g["E"])
