@@ -244,6 +244,9 @@ def main():
     ap.add_argument("--activation", default="gelu_tanh", choices=["gelu_tanh", "silu"],
                     help="the gate activation: gelu_tanh (GeGLU, the Gemma-4 experts) or silu "
                          "(SwiGLU)")
+    ap.add_argument("--router-logits", action="store_true",
+                    help="route from the router logits (top-k + softmax, then the sort and "
+                         "the tiles) instead of given top-k ids; the four calls")
     ap.add_argument("--deterministic", action="store_true",
                     help="the fixed-order un-sort (per-assignment rows, ordered k-sum)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -279,6 +282,8 @@ def main():
     x = x_h.to(dev)
     ids = ids_h.to(dev)
     tw = tw_h.to(dev)
+    logits_h = torch.from_numpy(d["router_logits"]).pin_memory()
+    logits = logits_h.to(dev)
     buf = mq.MoeLayerBuffers(T, k, E, H, I, args.tile_m, device=dev,
                              deterministic=args.deterministic)
     y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
@@ -295,7 +300,7 @@ def main():
 
     # the one-launch layer when asked for, or by default where it takes the workload
     fits = mq.fused_layer_fits(T, k, E, H, I, args.tile_m)
-    use_fused = args.variant in ("fused", "best") and fits
+    use_fused = args.variant in ("fused", "best") and fits and not args.router_logits
     if args.variant == "fused" and not use_fused:
         raise SystemExit("the fused layer does not take this workload")
     # the library's AUTO rule: the weight-streaming GEMV for small tiles, else tensor cores
@@ -312,8 +317,11 @@ def main():
                     e.record(stream)
             return
         # the four library calls; events (if given) bracket the gate/up launch
-        mq.moe_sort_and_build_tiles(ids, E, args.tile_m, r.sorted_ids, r.perm, r.counts,
-                                    r.offsets, r.tiles, r.tile_count, r.status, stream)
+        if args.router_logits:  # ids and weights are outputs here
+            mq.moe_route_logits(logits, k, args.tile_m, ids, tw, r, stream)
+        else:
+            mq.moe_sort_and_build_tiles(ids, E, args.tile_m, r.sorted_ids, r.perm, r.counts,
+                                        r.offsets, r.tiles, r.tile_count, r.status, stream)
         if ev is not None:
             ev[0].record(stream)
         # (the tensor-core variant loads tile rows from the sorted copy of x)
@@ -328,8 +336,11 @@ def main():
 
     def e2e_step():
         x.copy_(x_h, non_blocking=True)
-        ids.copy_(ids_h, non_blocking=True)
-        tw.copy_(tw_h, non_blocking=True)
+        if args.router_logits:
+            logits.copy_(logits_h, non_blocking=True)
+        else:
+            ids.copy_(ids_h, non_blocking=True)
+            tw.copy_(tw_h, non_blocking=True)
         step()
         y_h.copy_(buf.y, non_blocking=True)
 
@@ -413,6 +424,8 @@ def main():
     fused_cast = variant != mq.VARIANT_TC and acc_rows * H <= (1 << 20) and not (
         variant == mq.VARIANT_AUTO and A > 16 * min(E, A))
     launches_per_step = 1 if use_fused else (3 if fused_cast else 4) + (1 if use_ws else 0)
+    if args.router_logits and T > 64:
+        launches_per_step += 1  # the router over every SM, then the sort
     line = {
         "metric": "MoE layer assignments/s", "value": world * A / (ms * 1e-3),
         "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -421,6 +434,8 @@ def main():
         "config": {"workload": workload_name(args.config, cfg), "assignments": A,
                    "experts_touched": touched, "tile_m": args.tile_m, "variant": args.variant,
                    "path": path, "activation": args.activation,
+                   "route": "from router logits (top-k, softmax, sort, tiles)"
+                            if args.router_logits else "from top-k ids (sort, tiles)",
                    "unsort": "deterministic (per-assignment rows, fixed-order k-sum)"
                              if args.deterministic else "fp32 atomics",
                    "l2": "flushed between steps outside the timed events: 512 MB write, "
@@ -434,7 +449,8 @@ def main():
                            else "tensor", "peaks": peak_src},
         "kernels_us": {"moe_layer_fused (every step, one launch)": 1e3 * statistics.median(route_ms)}
         if use_fused else
-        {"route (sort + tiles, one launch)": 1e3 * statistics.median(route_ms),
+        {("route (top-k + softmax + sort + tiles)" if args.router_logits else
+          "route (sort + tiles, one launch)"): 1e3 * statistics.median(route_ms),
                        "gather_qmm_geglu": 1e3 * statistics.median(geglu_ms),
                        "gather_qmm_down_unsort (+cast)": 1e3 * statistics.median(down_ms),
                        "note": "separate pass with events between the calls (serialised)"},
@@ -446,7 +462,8 @@ def main():
                                                 "gather_qmm_geglu_") + args.config),
                      "algorithmic_bytes": geglu_bytes},
         "e2e": {"value": world * A / (e2e_total_ms / args.steps * 1e-3), "unit": "assignments/s",
-                "h2d_bytes_per_step": int(x_h.numel() * 2 + ids_h.numel() * 4 + tw_h.numel() * 4),
+                "h2d_bytes_per_step": int(x_h.numel() * 2 + (logits_h.numel() * 4 if args.router_logits
+                                          else ids_h.numel() * 4 + tw_h.numel() * 4)),
                 "d2h_bytes_per_step": int(y_h.numel() * 2)},
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,

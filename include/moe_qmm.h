@@ -192,6 +192,36 @@ moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t num_tokens,
                                     int32_t *status, cudaStream_t stream);
 
 /*
+ * The step before a1: the router's top-k and its softmax (fengmk2/mlx-node activity, the
+ * perf(qwen3.5) change: a fused top-16 candidate selection in one Metal dispatch, with an
+ * argpartition fallback).
+ *   logits       [T, E] fp32  router logits (row-major)
+ *   topk_ids     [T, k] int32 out: per token the k experts with the largest logits, in
+ *                             descending logit order; equal logits in ascending expert id
+ *   topk_weights [T, k] fp32  out: softmax over the token's k chosen logits,
+ *                             w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0), in fp32
+ * -inf logits are allowed (chosen only when fewer than k finite ones remain; weight 0).  A
+ * NaN or +inf logit, or a token whose chosen logits are all -inf, sets MOE_ERR_RANGE in
+ * *status (that token's outputs are not written).  Requires 1 <= k <= min(E, 32) and
+ * E <= MOE_MAX_EXPERTS (MOE_ERR_UNSUPPORTED beyond).  Does nothing if *status != 0.
+ */
+moe_status moe_router_topk(const float *logits, int32_t num_tokens, int32_t num_experts,
+                           int32_t top_k, int32_t *topk_ids, float *topk_weights,
+                           int32_t *status, cudaStream_t stream);
+
+/*
+ * The router's top-k and softmax followed by steps a1 and a2: exactly moe_router_topk, then
+ * moe_sort_and_build_tiles on its ids (same outputs and status codes).  Calls of at most 64
+ * tokens run in one single-CTA launch (the router, the sort and the builder back to back);
+ * larger ones in two (the router over every SM, then the sort and the builder).
+ */
+moe_status moe_route_logits(const float *logits, int32_t num_tokens, int32_t num_experts,
+                            int32_t top_k, int32_t tile_m, int32_t max_tiles,
+                            int32_t *topk_ids, float *topk_weights, int32_t *sorted_ids,
+                            int32_t *perm, int32_t *counts, int32_t *offsets, int32_t *tiles,
+                            int32_t *tile_count, int32_t *status, cudaStream_t stream);
+
+/*
  * Steps a3-a6 -- gathered 4-bit gate/up projection with the GeGLU product
  * in its epilogue (Layr-Labs/mlx PR #4, "What"; SharpAI/SwiftLM issue #236,
  * "Still missing": geluApproximate(x_gate) * x_up in one dispatch).

@@ -39,7 +39,8 @@ ABI_SYMBOLS = ("moe_max_tiles", "moe_workspace_bytes", "moe_sort_assignments",
                "moe_build_expert_tiles", "moe_gather_qmm_geglu", "moe_gather_qmm_down_unsort",
                "moe_last_error_string", "moe_gather_qmm_down_unsort_noalloc",
                "moe_sort_and_build_tiles", "moe_layer_fused", "moe_layer_fused_supported",
-               "moe_gather_qmm_geglu_ws", "moe_unsort_workspace_bytes", "moe_gather_qmm_glu")
+               "moe_gather_qmm_geglu_ws", "moe_unsort_workspace_bytes", "moe_gather_qmm_glu",
+               "moe_router_topk", "moe_route_logits")
 NOALLOC_MAX_Y_ELEMENTS = 4194304
 
 
@@ -101,6 +102,11 @@ def load(build_if_needed: bool = True):
         lib.moe_gather_qmm_glu.argtypes = [p, p, p, p, ctypes.POINTER(MoeTiles), i32, i32, i32,
                                            i32, p, p, p]
         lib.moe_gather_qmm_glu.restype = ctypes.c_int
+        lib.moe_router_topk.argtypes = [p, i32, i32, i32, p, p, p, p]
+        lib.moe_router_topk.restype = ctypes.c_int
+        lib.moe_route_logits.argtypes = [p, i32, i32, i32, i32, i32, p, p, p, p, p, p, p, p, p,
+                                         p]
+        lib.moe_route_logits.restype = ctypes.c_int
         lib.moe_layer_fused_supported.restype = ctypes.c_int
         for fn in ("moe_sort_assignments", "moe_build_expert_tiles", "moe_sort_and_build_tiles",
                    "moe_gather_qmm_geglu", "moe_layer_fused",
@@ -189,6 +195,32 @@ def moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, sorted_ids, perm, co
         _ptr(offsets, torch.int32, "offsets", num_experts + 1), _ptr(tiles, torch.int32, "tiles"),
         _ptr(tile_count, torch.int32, "tile_count", 1), _ptr(status, torch.int32, "status", 1),
         _stream(stream)))
+
+
+def moe_router_topk(logits, top_k, topk_ids, topk_weights, status, stream=None):
+    """Router logits [T, E] fp32 -> top-k ids (descending logit, ties to the lower id) and
+    the softmax over the chosen logits."""
+    T, E = logits.shape
+    _check(load().moe_router_topk(
+        _ptr(logits, torch.float32, "logits"), T, E, top_k,
+        _ptr(topk_ids, torch.int32, "topk_ids", T * top_k),
+        _ptr(topk_weights, torch.float32, "topk_weights", T * top_k),
+        _ptr(status, torch.int32, "status", 1), _stream(stream)))
+
+
+def moe_route_logits(logits, top_k, tile_m, topk_ids, topk_weights, routing, stream=None):
+    """moe_router_topk, then the sort and the tile builder into ``routing`` (a Routing)."""
+    T, E = logits.shape
+    r = routing
+    _check(load().moe_route_logits(
+        _ptr(logits, torch.float32, "logits"), T, E, top_k, tile_m, r.tiles.numel() // 3,
+        _ptr(topk_ids, torch.int32, "topk_ids", T * top_k),
+        _ptr(topk_weights, torch.float32, "topk_weights", T * top_k),
+        _ptr(r.sorted_ids, torch.int32, "sorted_ids", T * top_k),
+        _ptr(r.perm, torch.int32, "perm", T * top_k), _ptr(r.counts, torch.int32, "counts", E),
+        _ptr(r.offsets, torch.int32, "offsets", E + 1), _ptr(r.tiles, torch.int32, "tiles"),
+        _ptr(r.tile_count, torch.int32, "tile_count", 1),
+        _ptr(r.status, torch.int32, "status", 1), _stream(stream)))
 
 
 class Routing:

@@ -314,6 +314,142 @@ __global__ void __launch_bounds__(kSortThreads)
              tile_count, status, ssm.off);
 }
 
+// ---------------------------------------------------------------- router top-k + softmax
+// The step before a1 (fengmk2/mlx-node activity, the perf(qwen3.5) change: a fused top-16
+// candidate selection in one dispatch): per token, the k largest of its E expert logits in
+// descending order, equal logits in ascending expert id, and the softmax over those k.
+// One warp per token; lane l holds logits l, l + 32, ... (E <= 256: at most 8 per lane).
+constexpr int kRouterMaxK = 32;
+
+// Writes the token's ids and weights; returns false (nothing written) if a logit is NaN or
+// +inf, or if the chosen logits are all -inf.
+__device__ bool router_token(const float *__restrict__ row, int E, int k,
+                             int32_t *__restrict__ ids_out, float *__restrict__ w_out, int lane) {
+  float v[8];
+  uint32_t avail = 0;
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = 0.f;
+    if (e < E) {
+      v[i] = __ldg(row + e);
+      avail |= 1u << i;
+      bad |= (v[i] != v[i]) || (v[i] == INFINITY);
+    }
+  }
+  if (__any_sync(0xffffffffu, bad)) return false;
+  float my_v = 0.f, top = 0.f;
+  int my_e = 0;
+  for (int j = 0; j < k; ++j) {
+    // the lane's best untaken logit (ids ascend with i, so a strict > keeps the lower id)
+    bool have = false;
+    float bv = 0.f;
+    int be = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if ((avail >> i) & 1u)
+        if (!have || v[i] > bv) {
+          have = true;
+          bv = v[i];
+          be = lane + 32 * i;
+        }
+    // warp arg-max: larger logit, then lower expert id
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      const bool oh = __shfl_xor_sync(0xffffffffu, have, off);
+      if (oh && (!have || ov > bv || (ov == bv && oe < be))) {
+        have = true;
+        bv = ov;
+        be = oe;
+      }
+    }
+    if (lane == (be & 31)) avail &= ~(1u << (be >> 5));
+    if (j == 0) top = bv;
+    if (lane == j) {
+      my_v = bv;
+      my_e = be;
+    }
+  }
+  if (top == -INFINITY) return false;
+  // softmax over the chosen logits, relative to the largest
+  const float ex = lane < k ? expf(my_v - top) : 0.f;
+  float z = ex;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+  if (lane < k) {
+    ids_out[lane] = my_e;
+    w_out[lane] = ex / z;
+  }
+  return true;
+}
+
+// Router top-k + softmax over every token, one warp per token (grid-stride).
+__global__ void __launch_bounds__(256)
+    router_topk_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k,
+                       int32_t *__restrict__ topk_ids, float *__restrict__ topk_weights,
+                       int32_t *__restrict__ status) {
+  griddep_wait();
+  griddep_launch();
+  if (load_status(status) != 0) return;
+  const int lane = threadIdx.x & 31;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += nw)
+    if (!router_token(logits + (int64_t)t * E, E, k, topk_ids + (int64_t)t * k,
+                      topk_weights + (int64_t)t * k, lane) &&
+        lane == 0)
+      raise_status(status, MOE_ERR_RANGE);
+}
+
+// The router, the sort and the tile builder in one launch (one CTA): for calls whose
+// tokens one block covers quickly.  The sort reads the ids this block just wrote (a block
+// barrier makes them visible to it).
+__global__ void __launch_bounds__(kSortThreads)
+    route_logits_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k,
+                        int32_t BM, int32_t *__restrict__ topk_ids,
+                        float *__restrict__ topk_weights, int32_t *__restrict__ sorted_ids,
+                        int32_t *__restrict__ perm, int32_t *__restrict__ counts,
+                        int32_t *__restrict__ offsets, int32_t *__restrict__ tiles,
+                        int32_t *__restrict__ tile_count, int32_t *__restrict__ status) {
+  __shared__ SortSmem ssm;
+  __shared__ TileSmem tsm;
+  __shared__ int s_bad;
+  griddep_wait();
+  griddep_launch();
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  if (load_status(status) != 0) {
+    if (threadIdx.x == 0) *tile_count = 0;
+    return;
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int t = warp; t < T; t += nw)
+    if (!router_token(logits + (int64_t)t * E, E, k, topk_ids + (int64_t)t * k,
+                      topk_weights + (int64_t)t * k, lane) &&
+        lane == 0)
+      s_bad = 1;
+  __syncthreads();
+  if (s_bad) {
+    if (threadIdx.x == 0) {
+      *tile_count = 0;
+      raise_status(status, MOE_ERR_RANGE);
+    }
+    return;
+  }
+  const int32_t A = T * k;
+  if (!sort_body(ssm, topk_ids, A, E, sorted_ids, perm, counts, status)) {
+    if (threadIdx.x == 0) *tile_count = 0;
+    return;
+  }
+  __syncthreads();
+  build_body(tsm, A <= kSmemSorted ? ssm.sorted : sorted_ids, A, E, BM, offsets, tiles,
+             tile_count, status, ssm.off);
+}
+
+constexpr int kRouteOneLaunchTokens = 64;  // at most this many tokens: one launch
+
 }  // namespace moeqmm
 
 using namespace moeqmm;
@@ -437,6 +573,89 @@ moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t T, int32_t 
              static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets, tiles,
              tile_count, status);
   return check_launch("moe_sort_and_build_tiles");
+}
+
+static moe_status router_validate(const char *fn, const float *logits, int32_t T, int32_t E,
+                                  int32_t k, const int32_t *topk_ids, const float *topk_weights,
+                                  const int32_t *status) {
+  if (!logits || !topk_ids || !topk_weights || !status) {
+    set_error("%s: null pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (E < 1 || E > MOE_MAX_EXPERTS) {
+    set_error("%s: num_experts %d outside [1, %d]", fn, E, MOE_MAX_EXPERTS);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (T < 1 || k < 1 || k > E) {
+    set_error("%s: need T >= 1 and 1 <= k <= E (T=%d k=%d E=%d)", fn, T, k, E);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (k > kRouterMaxK) {
+    set_error("%s: top_k %d above %d", fn, k, kRouterMaxK);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if ((int64_t)T * k > (int64_t(1) << 24)) {
+    set_error("%s: %lld assignments exceed 2^24", fn, (long long)T * k);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+static void launch_router(const float *logits, int32_t T, int32_t E, int32_t k,
+                          int32_t *topk_ids, float *topk_weights, int32_t *status,
+                          cudaStream_t stream) {
+  int blocks = (T + 7) / 8;  // 8 tokens (warps) per block
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  launch_pdl(router_topk_kernel, dim3(blocks), dim3(256), 0, stream, logits, T, E, k, topk_ids,
+             topk_weights, status);
+}
+
+moe_status moe_router_topk(const float *logits, int32_t T, int32_t E, int32_t k,
+                           int32_t *topk_ids, float *topk_weights, int32_t *status,
+                           cudaStream_t stream) {
+  clear_error();
+  moe_status st = router_validate("moe_router_topk", logits, T, E, k, topk_ids, topk_weights,
+                                  status);
+  if (st != MOE_OK) return st;
+  launch_router(logits, T, E, k, topk_ids, topk_weights, status, stream);
+  return check_launch("moe_router_topk");
+}
+
+moe_status moe_route_logits(const float *logits, int32_t T, int32_t E, int32_t k,
+                            int32_t tile_m, int32_t max_tiles, int32_t *topk_ids,
+                            float *topk_weights, int32_t *sorted_ids, int32_t *perm,
+                            int32_t *counts, int32_t *offsets, int32_t *tiles,
+                            int32_t *tile_count, int32_t *status, cudaStream_t stream) {
+  const char *fn = "moe_route_logits";
+  clear_error();
+  moe_status st = router_validate(fn, logits, T, E, k, topk_ids, topk_weights, status);
+  if (st != MOE_OK) return st;
+  if (!sorted_ids || !perm || !counts || !offsets || !tiles || !tile_count) {
+    set_error("%s: null pointer", fn);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (tile_m != 16 && tile_m != 32 && tile_m != 64 && tile_m != 128 && tile_m != 256) {
+    set_error("%s: tile_m %d not in {16, 32, 64, 128, 256}", fn, tile_m);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  const int64_t A = static_cast<int64_t>(T) * k;
+  const size_t need = moe_max_tiles(static_cast<int32_t>(A), E, tile_m);
+  if (max_tiles < 0 || static_cast<size_t>(max_tiles) < need) {
+    set_error("%s: max_tiles %d < required %zu", fn, max_tiles, need);
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (T <= kRouteOneLaunchTokens) {
+    launch_pdl(route_logits_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, logits, T, E, k,
+               tile_m, topk_ids, topk_weights, sorted_ids, perm, counts, offsets, tiles,
+               tile_count, status);
+    return check_launch(fn);
+  }
+  launch_router(logits, T, E, k, topk_ids, topk_weights, status, stream);
+  if ((st = check_launch(fn)) != MOE_OK) return st;
+  launch_pdl(route_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, topk_ids,
+             static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets, tiles,
+             tile_count, status);
+  return check_launch(fn);
 }
 
 }  // extern "C"

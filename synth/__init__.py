@@ -169,8 +169,8 @@ def weights(kind: str, E: int, H: int, I: int, seed: int = 0) -> dict:
     return w
 
 
-def router(name: str, T: int, E: int, k: int, seed: int = 0):
-    """(topk_ids int32 [T,k], topk_weights float32 [T,k]) for a workload's router."""
+def router_scores(name: str, T: int, E: int, seed: int = 0) -> np.ndarray:
+    """The router scores [T, E] (float64) of a workload: the logits its top-k is taken of."""
     cfg = CONFIGS[name]
     ci = CONFIG_ORDER.index(name)
     if cfg["router"] == "normal":
@@ -184,7 +184,12 @@ def router(name: str, T: int, E: int, k: int, seed: int = 0):
                              E - 8)
     else:
         raise ValueError(cfg["router"])
-    return topk_softmax(scores, k)
+    return scores
+
+
+def router(name: str, T: int, E: int, k: int, seed: int = 0):
+    """(topk_ids int32 [T,k], topk_weights float32 [T,k]) for a workload's router."""
+    return topk_softmax(router_scores(name, T, E, seed), k)
 
 
 def make(name: str, seed: int = 0, T: int | None = None) -> dict:
@@ -200,8 +205,11 @@ def make(name: str, seed: int = 0, T: int | None = None) -> dict:
         n_out = int(round(0.01 * T))
         outliers = choose_rows(seed, _OUTLIER_STREAM + ci, T, n_out)
     x = activations(seed, _X_STREAM + ci, T, H, outliers, 20.0)
-    ids, tw = router(name, T, E, k, seed)
+    scores = router_scores(name, T, E, seed)
+    ids, tw = topk_softmax(scores, k)
+    # the same scores as fp32 router logits (the input of the router's top-k step)
     out = dict(name=name, E=E, H=H, I=I, T=T, k=k, x=x, topk_ids=ids, topk_weights=tw,
+               router_logits=scores.astype(np.float32),
                outlier_rows=outliers if outliers is not None else np.zeros(0, np.int32))
     out.update(weights(cfg["weights"], E, H, I, seed))
     return out
@@ -226,5 +234,6 @@ def make_custom(E: int, H: int, I: int, T: int, k: int, seed: int = 0,
         scores[:, 0] = 1e9
     ids, tw = topk_softmax(scores, k)
     return dict(name=f"custom_E{E}_H{H}_I{I}_T{T}_k{k}", E=E, H=H, I=I, T=T, k=k, x=x,
-                topk_ids=ids, topk_weights=tw, outlier_rows=np.zeros(0, np.int32),
+                topk_ids=ids, topk_weights=tw, router_logits=scores.astype(np.float32),
+                outlier_rows=np.zeros(0, np.int32),
                 Wgu=Wgu, Sgu=Sgu, Bgu=Bgu, Wd=Wd, Sd=Sd, Bd=Bd)

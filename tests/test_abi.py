@@ -130,6 +130,25 @@ def test_deterministic_flag_validation():
     assert "deterministic" in _raw().moe_last_error_string().decode()
 
 
+@pytest.mark.parametrize("T,E,k,tile_m,max_tiles,code", [
+    (4, 128, 8, 128, 32, None),                       # valid: would launch (skipped)
+    (4, 128, 33, 128, 160, mq.MOE_ERR_UNSUPPORTED),    # k above the router's 32
+    (4, 300, 8, 128, 40, mq.MOE_ERR_UNSUPPORTED),      # E > 256
+    (0, 128, 8, 128, 32, mq.MOE_ERR_INVALID_ARG),      # T = 0
+    (4, 8, 9, 128, 32, mq.MOE_ERR_INVALID_ARG),        # k > E
+    (4, 128, 8, 48, 32, mq.MOE_ERR_UNSUPPORTED),       # tile_m 48
+    (4, 128, 8, 128, 31, mq.MOE_ERR_INVALID_ARG),      # max_tiles below the bound
+])
+def test_router_host_validation(T, E, k, tile_m, max_tiles, code):
+    if code is None:
+        pytest.skip("a valid call would launch; covered by the GPU tests")
+    assert _raw().moe_route_logits(16, T, E, k, tile_m, max_tiles, 16, 16, 16, 16, 16, 16, 16,
+                                   16, 16, NULL) == code
+    if tile_m == 128 and max_tiles >= 32:  # the router alone takes no tile arguments
+        assert _raw().moe_router_topk(16, T, E, k, 16, 16, 16, NULL) == code
+    assert _raw().moe_router_topk(NULL, 4, 128, 8, 16, 16, 16, NULL) == mq.MOE_ERR_INVALID_ARG
+
+
 def test_activation_validation():
     """The gate activation is MOE_ACT_GELU_TANH or MOE_ACT_SILU; anything else is refused
     before a launch."""
