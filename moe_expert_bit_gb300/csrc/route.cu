@@ -321,8 +321,16 @@ __global__ void __launch_bounds__(kSortThreads)
 // One warp per token; lane l holds logits l, l + 32, ... (E <= 256: at most 8 per lane).
 constexpr int kRouterMaxK = 32;
 
+// Order-preserving key of a float (not NaN): larger floats give larger unsigned keys; 0 is
+// below every float (-inf maps to 0x007fffff).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Writes the token's ids and weights; returns false (nothing written) if a logit is NaN or
-// +inf, or if the chosen logits are all -inf.
+// +inf, or if the chosen logits are all -inf.  Each of the k rounds takes the warp's
+// largest untaken key with one redux, then the lowest expert id holding it with another.
 __device__ bool router_token(const float *__restrict__ row, int E, int k,
                              int32_t *__restrict__ ids_out, float *__restrict__ w_out, int lane) {
   float v[8];
@@ -342,34 +350,27 @@ __device__ bool router_token(const float *__restrict__ row, int E, int k,
   float my_v = 0.f, top = 0.f;
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    // the lane's best untaken logit (ids ascend with i, so a strict > keeps the lower id)
-    bool have = false;
-    float bv = 0.f;
-    int be = 0;
+    // the lane's best untaken logit; ids ascend with i, so a strict > keeps the lower id
+    uint32_t bk = 0;
+    int bi = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if ((avail >> i) & 1u)
-        if (!have || v[i] > bv) {
-          have = true;
-          bv = v[i];
-          be = lane + 32 * i;
+      if ((avail >> i) & 1u) {
+        const uint32_t key = float_key(v[i]);
+        if (key > bk) {
+          bk = key;
+          bi = i;
         }
-    // warp arg-max: larger logit, then lower expert id
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      const bool oh = __shfl_xor_sync(0xffffffffu, have, off);
-      if (oh && (!have || ov > bv || (ov == bv && oe < be))) {
-        have = true;
-        bv = ov;
-        be = oe;
       }
-    }
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t cand = (bk == mk && avail) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    const int be = (int)__reduce_min_sync(0xffffffffu, cand);
     if (lane == (be & 31)) avail &= ~(1u << (be >> 5));
-    if (j == 0) top = bv;
+    const float val = (mk & 0x80000000u) ? __uint_as_float(mk & 0x7fffffffu)
+                                         : __uint_as_float(~mk);
+    if (j == 0) top = val;
     if (lane == j) {
-      my_v = bv;
+      my_v = val;
       my_e = be;
     }
   }
@@ -645,7 +646,10 @@ moe_status moe_route_logits(const float *logits, int32_t T, int32_t E, int32_t k
     return MOE_ERR_INVALID_ARG;
   }
   if (T <= kRouteOneLaunchTokens) {
-    launch_pdl(route_logits_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, logits, T, E, k,
+    // a warp per token for the router, at least the sort's block
+    int threads = sort_threads(A) > 32 * T ? sort_threads(A) : 32 * T;
+    if (threads > kSortThreads) threads = kSortThreads;
+    launch_pdl(route_logits_kernel, dim3(1), dim3(threads), 0, stream, logits, T, E, k,
                tile_m, topk_ids, topk_weights, sorted_ids, perm, counts, offsets, tiles,
                tile_count, status);
     return check_launch(fn);
