@@ -321,10 +321,11 @@ __global__ void __launch_bounds__(kSortThreads)
 // One warp per token; lane l holds logits l, l + 32, ... (E <= 256: at most 8 per lane).
 constexpr int kRouterMaxK = 32;
 
-// Order-preserving key of a float (not NaN): larger floats give larger unsigned keys; 0 is
-// below every float (-inf maps to 0x007fffff).
+// Order-preserving key of a float (not NaN): larger floats give larger unsigned keys, equal
+// floats equal keys (-0 is read as +0); 0 is below every float (-inf maps to 0x007fffff).
 __device__ __forceinline__ uint32_t float_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -76,6 +76,13 @@ def test_route_logits_shapes_with_ties(T, E, k, tile_m, seed):
     check_route(logits, k, E, tile_m)
 
 
+def test_signed_zeros_are_equal_logits():
+    """-0 and +0 are the same logit: the lower expert id comes first, whichever sign."""
+    row = np.array([[-0.0, 0.0, -0.0, -1.0, 0.0]], np.float32)
+    ids, w, _ = check_route(row, 4, 5)
+    assert list(ids[0]) == [0, 1, 2, 4]
+
+
 def test_minus_infinity_logits_are_chosen_last_with_zero_weight():
     T, E, k = 70, 16, 6
     rng = np.random.default_rng(9)
