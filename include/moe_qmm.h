@@ -289,11 +289,12 @@ moe_status moe_gather_qmm_glu(const moe_bf16_t *x, const uint32_t *Wgu, const mo
  *                           completes leaves the counters (and, when not
  *                           deterministic, the accumulator) zero again, so no
  *                           memset is needed per call; moe_layer_fused also keeps
- *                           a 64-bit count of grid-barrier arrivals after them,
- *                           which every call that completes leaves a multiple of
- *                           the GPU's SM count (zero is such a value; use one
- *                           workspace on one GPU).  After a call that set the
- *                           status word, clear it before reusing it.
+ *                           a 64-bit count of finished CTAs after them, which
+ *                           every call that completes leaves a multiple of the
+ *                           GPU's SM count (zero is such a value; use one
+ *                           workspace on one GPU), and two sets of per-tile
+ *                           counters that it clears itself.  After a call that
+ *                           set the status word, clear it before reusing it.
  *   deterministic    0 or 1 (else MOE_ERR_INVALID_ARG)
  *   y   [T, H]       bf16   out: y[t] = sum_j topk_weights[t, j] * (Wd[e] . h[s]),
  *                           s the slot of a = t*k + j, e = sorted_ids[s]
@@ -367,8 +368,8 @@ moe_status moe_gather_qmm_down_unsort_noalloc(const moe_bf16_t *h, const uint32_
  * Limits: A = T*k <= 256, T <= 64, H and I multiples of 64 whose padded packed rows fit one
  * copy (K/2 + padding <= 2048 bytes); other calls return MOE_ERR_UNSUPPORTED before any
  * launch (use the four calls).  The launch is cooperative (one CTA per SM, all resident at
- * once): it starts when every SM can take its CTA.  Every wait, the grid barrier included,
- * is bounded (MOE_ERR_TIMEOUT).
+ * once): it starts when every SM can take its CTA.  Every wait, the per-tile gate/up
+ * readiness included, is bounded (MOE_ERR_TIMEOUT).
  */
 moe_status moe_layer_fused(const int32_t *topk_ids, const float *topk_weights, int32_t num_tokens,
                            int32_t top_k, int32_t num_experts, const moe_bf16_t *x,

@@ -9,6 +9,10 @@
 
 namespace moeqmm {
 
+// Per-tile gate/up completion counters of the one-launch layer in the down call's
+// workspace: two sets of this many (one per call parity), after the grid's arrival count.
+constexpr int kFusedTileFlags = 512;
+
 // ---- host-side error reporting (per host thread) ----
 void set_error(const char *fmt, ...);
 void clear_error();

@@ -10,7 +10,9 @@
 //      descriptors, so the weight stream starts as soon as the ids are read (CTA 0 also
 //      writes the routing state out for the caller);
 //   2. gate/up + GeGLU exactly as the per-call GEMV (split-K teams, h to global memory);
-//   3. a grid barrier (the launch is cooperative, so every CTA is resident): h is complete;
+//   3. per-tile readiness: a CTA publishes the gate/up chunks it did per tile, and the
+//      down phase of a tile waits for that tile's count only (the launch is cooperative,
+//      so every CTA is resident and every count completes);
 //   4. down + un-sort, reading h from L2, with the per-column-block cast (deterministic: one
 //      stored row per assignment, and the per-column-block sum of a token's k rows in order).
 // The producer warp is not held by the barrier: the ring is one stream of gate/up chunks
@@ -87,27 +89,30 @@ struct FArgs {
   uint16_t *h;
   float *y_acc;
   int32_t *cnt;   // H/16 column-block counters, after y_acc
-  unsigned long long *gbar;  // grid barrier: arrivals of every call so far (monotonic)
+  unsigned long long *gbar;  // CTAs finished, over every call so far (a multiple of the grid)
+  uint32_t *tflags;          // [2][kFusedTileFlags] gate/up chunk-passes done per tile
   uint16_t *y;
 };
 
-// The grid barrier (thread 0 of each CTA; the launch is cooperative).  gbar counts the
-// arrivals of every call so far: it is a multiple of the grid size N between calls, so a CTA
-// that reads it at its start (before its own arrival, hence while fewer than N CTAs of this
-// call have arrived) finds base + f with f < N, and every CTA of the call derives the same
-// target, base + N.  A CTA publishes its earlier stores with a fence (they are ordered
-// before it by the block barrier), adds its arrival, and polls with plain volatile loads
-// until the count reaches the target; a fence after the wait makes every CTA's stores
-// visible to it.  No CTA has to act after the others have arrived.
-__device__ __forceinline__ bool grid_barrier(unsigned long long *gbar, unsigned long long target,
-                                             volatile int *abort_flag) {
-  __threadfence();
-  atomicAdd(gbar, 1ull);
-  volatile unsigned long long *vc = gbar;
+// Gate/up -> down readiness, per tile instead of for the whole grid.  The workspace keeps a
+// 64-bit count of finished CTAs over every call (each CTA adds one as it exits), so it is a
+// multiple of the grid size N between calls; a CTA that reads it at its start finds base + f
+// with f < N (it has not finished itself) and every CTA of a call derives the same call
+// number, base / N.  Calls alternate between two sets of per-tile counters by that number's
+// parity; CTA 0 clears the other set for the next call.  A CTA whose compute warps have
+// finished their gate/up chunks publishes its h stores with a fence and adds its chunk-passes
+// to each tile it worked on; the stager waits for a tile's full count (polling with volatile
+// loads, bounded) and fences before it reads that tile's h rows.  The launch is cooperative
+// (every CTA resident), and no gate/up chunk waits on a down chunk, so every count completes.
+__device__ __forceinline__ bool wait_tile_ready(const uint32_t *flag, uint32_t target,
+                                                volatile int *abort_flag) {
+  volatile const uint32_t *v = flag;
   const uint64_t t0 = umma::globaltimer_ns();
-  for (uint32_t i = 1; *vc < target; ++i) {
-    if ((i & 63u) == 0 && (*abort_flag || umma::globaltimer_ns() - t0 > 2000000000ull))
+  for (uint32_t i = 1; *v < target; ++i) {
+    if ((i & 63u) == 0 && (*abort_flag || umma::globaltimer_ns() - t0 > 2000000000ull)) {
+      *abort_flag = 1;
       return false;
+    }
   }
   __threadfence();
   return true;
@@ -140,7 +145,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   int *s_flags = reinterpret_cast<int *>(gsm + L.off_misc + 4);  // [0] range, [1] order
   int *s_ntiles = reinterpret_cast<int *>(gsm + L.off_misc + 12);
   uint32_t *issued = reinterpret_cast<uint32_t *>(gsm + L.off_misc + 16);  // chunks issued
-  unsigned long long *s_gbase =  // the barrier count read at the start
+  unsigned long long *s_gbase =  // the finished-CTA count read at the start
       reinterpret_cast<unsigned long long *>(gsm + L.off_misc + 32);
   int *s_order_bad = reinterpret_cast<int *>(gsm + L.off_misc + 24);
   int32_t *sc_ids = reinterpret_cast<int32_t *>(gsm + (size_t)(nbuf - 1) * L.slot);
@@ -189,9 +194,15 @@ __global__ void __launch_bounds__(kFThreads, 1)
   if (warp == nwc + 1) {
     for (int r = lane; r < p.T; r += 32)
       bulk_load(xall + (size_t)r * L.xrbh, p.x + (int64_t)r * p.H, xbytes_g, &xfull[0]);
-    // the grid barrier's count, read before this CTA arrives there (the start barrier of the
-    // compute warps and the stager orders it before the arrival)
+    // the finished-CTA count (the start barrier of the compute warps and the stager orders
+    // this before any use); CTA 0 clears the tile counters of the next call
     if (lane == 0) *s_gbase = *reinterpret_cast<volatile unsigned long long *>(p.gbar);
+    if (blockIdx.x == 0) {
+      const unsigned long long base = __shfl_sync(
+          0xffffffffu, *reinterpret_cast<volatile unsigned long long *>(s_gbase), 0);
+      uint32_t *next = p.tflags + ((base / gridDim.x + 1) & 1) * kFusedTileFlags;
+      for (int i = lane; i < kFusedTileFlags; i += 32) next[i] = 0;
+    }
   }
   if (warp == nwc && lane == 0) {
     prefetch_tensormap(&tmap_gu);
@@ -500,16 +511,18 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
   }
 
-  // ------------------------------------------------ grid barrier: h is complete
-  named_sync(kFBarGrid, nt);
-  if (tid == 0) {
-    const unsigned long long n = gridDim.x;
-    s_flags[1] = grid_barrier(p.gbar, (*s_gbase / n + 1) * n, abort_flag) ? 0 : 1;
-  }
-  named_sync(kFBarGrid, nt);
-  if (s_flags[1]) {
-    ok = false;
-    if (tid == 0) raise_status(p.status, MOE_ERR_TIMEOUT);
+  // ------------------------------------------------ h of this CTA's gate/up chunks is done
+  uint32_t *tflags = p.tflags + ((*s_gbase / gridDim.x) & 1) * kFusedTileFlags;
+  if (warp < nwc) {
+    named_sync(kFBarGrid, nwc * 32);
+    if (tid == 0 && ok) {
+      __threadfence();
+      for (int tile = g0 / cpt_g; tile * cpt_g < g1; ++tile) {
+        const int j0 = max(g0 - tile * cpt_g, 0), j1 = min(g1 - tile * cpt_g, cpt_g);
+        const int passes = (s_tiles[3 * tile + 2] + kFPassG - 1) / kFPassG;
+        atomicAdd(tflags + tile, (uint32_t)((j1 - j0) * passes));
+      }
+    }
   }
 
   if (warp == nwc + 1) {
@@ -517,14 +530,19 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint32_t xit = 0;
     for (int tile = d0 / cpt_d; ok && tile * cpt_d < d1; ++tile) {
       const int row0 = s_tiles[3 * tile + 1], R = s_tiles[3 * tile + 2];
+      // every gate/up chunk-pass of this tile has published its h rows
+      if (lane == 0)
+        ok = wait_tile_ready(tflags + tile, (uint32_t)(cpt_g * ((R + kFPassG - 1) / kFPassG)),
+                             abort_flag);
+      if (!(ok = __shfl_sync(0xffffffffu, ok, 0))) break;
       for (int r0 = 0; ok && r0 < R; r0 += kFPassD, ++xit) {
         const int Rp = min(kFPassD, R - r0), xb = xit & 1;
         ok = mbar_wait(&xempty[xb], ((xit >> 1) & 1) ^ 1, abort_flag);
         if (!(ok = __all_sync(0xffffffffu, ok))) break;
         uint8_t *xbuf = xall + (size_t)xb * kFPassD * L.xrbi;
         float *xs = xsall + (size_t)xb * kFPassD * Gi;
-        // plain loads from L2 (h was written by other CTAs before the barrier), permuted
-        // in registers; the 8 blocks of a group are 8 consecutive lanes
+        // plain loads from L2 (h was written by other CTAs before their tile counts),
+        // permuted in registers; the 8 blocks of a group are 8 consecutive lanes
         const int nblk = Rp * Gi * 8;
         for (int base = 0; base < nblk; base += 32) {
           const int i = base + lane;
@@ -662,6 +680,9 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     if (ok && qn) count_blocks();
     if (!ok) raise_status(p.status, MOE_ERR_TIMEOUT);
+    // this CTA is done: one more finished CTA in the count that numbers the calls
+    named_sync(kFBarGrid, nwc * 32);
+    if (tid == 0) atomicAdd(p.gbar, 1ull);
   }
 }
 
@@ -690,9 +711,10 @@ moe_status fused_layer_check(int32_t T, int32_t k, int32_t E, int32_t H, int32_t
                              int32_t tile_m, int32_t max_tiles) {
   const int64_t A = (int64_t)T * k;
   if (A > kFMaxA || T > kFMaxT) return MOE_ERR_UNSUPPORTED;
+  // the per-tile counters in the workspace cover every tile a call can have
+  if (moe_max_tiles((int32_t)A, E, tile_m) > (size_t)kFusedTileFlags) return MOE_ERR_UNSUPPORTED;
   if (!gemv_supported(H, I) || H % kFDownRows || I % 8) return MOE_ERR_UNSUPPORTED;
   if (fused_nbuf(H, I, T, (int)A, E, max_tiles) < 4) return MOE_ERR_UNSUPPORTED;
-  (void)tile_m;
   return MOE_OK;
 }
 
@@ -750,8 +772,10 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   a.y_acc = y_acc;
   // counters after the accumulator: T x H, or A x H per-assignment rows when deterministic
   a.cnt = reinterpret_cast<int32_t *>(y_acc + (int64_t)(det ? A : T) * H);
-  // after the counters, 16-byte aligned (the counters take H / 16 * 4 bytes, H % 64 == 0)
+  // after the counters, 16-byte aligned (the counters take H / 16 * 4 bytes, H % 64 == 0),
+  // then two spare ints and the per-tile counters
   a.gbar = reinterpret_cast<unsigned long long *>(a.cnt + H / 16);
+  a.tflags = reinterpret_cast<uint32_t *>(a.cnt + H / 16 + 4);
   a.y = y;
   // cooperative: every CTA resident at once (the grid barrier waits for all of them)
   cudaLaunchConfig_t cfg = {};

@@ -467,9 +467,11 @@ size_t moe_max_tiles(int32_t A, int32_t E, int32_t BM) {
 
 size_t moe_workspace_bytes(int32_t T, int32_t H) {
   if (T < 1 || H < 1) return 0;
-  // the fp32 accumulator, then one int counter per 16 output columns and the fused
-  // layer's grid barrier (a 64-bit arrival count, two spare ints), 16-byte padded
-  const size_t counters = ((static_cast<size_t>(H) / 16 + 4) * sizeof(int32_t) + 15) / 16 * 16;
+  // the fp32 accumulator, then one int counter per 16 output columns, the fused layer's
+  // 64-bit arrival count (+ two spare ints) and its two sets of per-tile counters, 16-byte
+  // padded
+  const size_t counters =
+      ((static_cast<size_t>(H) / 16 + 4 + 2 * kFusedTileFlags) * sizeof(int32_t) + 15) / 16 * 16;
   return static_cast<size_t>(T) * static_cast<size_t>(H) * sizeof(float) + counters;
 }
 

@@ -42,15 +42,16 @@ def test_size_helpers():
     assert mq.moe_max_tiles(32, 128, 64) == 32
     assert mq.moe_max_tiles(64, 8, 32) == 2 + 8
     assert mq.moe_max_tiles(10, 0, 32) == 0
-    # accumulator + one int per 16 columns + 4 ints (grid barrier), padded to 16 bytes
-    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 720
-    assert mq.moe_workspace_bytes(4, 64) == 4 * 64 * 4 + 32
-    assert mq.moe_workspace_bytes(1, 192) == 192 * 4 + 64
+    # accumulator + one int per 16 columns + 4 ints (the arrival count) + 2 x 512 per-tile
+    # counters of the one-launch layer, padded to 16 bytes
+    assert mq.moe_workspace_bytes(2048, 2816) == 2048 * 2816 * 4 + 720 + 4096
+    assert mq.moe_workspace_bytes(4, 64) == 4 * 64 * 4 + 32 + 4096
+    assert mq.moe_workspace_bytes(1, 192) == 192 * 4 + 64 + 4096
     assert mq.moe_workspace_bytes(0, 2816) == 0
     # the un-sort's workspace: per token, or one row per assignment when deterministic
     assert mq.moe_unsort_workspace_bytes(4, 8, 2816) == mq.moe_workspace_bytes(4, 2816)
-    assert mq.moe_unsort_workspace_bytes(4, 8, 2816, True) == 32 * 2816 * 4 + 720
-    assert mq.moe_unsort_workspace_bytes(2048, 8, 2816, True) == 16384 * 2816 * 4 + 720
+    assert mq.moe_unsort_workspace_bytes(4, 8, 2816, True) == 32 * 2816 * 4 + 720 + 4096
+    assert mq.moe_unsort_workspace_bytes(2048, 8, 2816, True) == 16384 * 2816 * 4 + 720 + 4096
     assert mq.moe_unsort_workspace_bytes(4, 0, 2816, True) == 0
     assert mq.moe_unsort_workspace_bytes(1 << 20, 1 << 12, 64, True) == 0  # A beyond int32
 
