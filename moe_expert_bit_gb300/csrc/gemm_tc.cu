@@ -37,8 +37,8 @@
 //               several k-blocks into one stage.
 //   warps 4-7   epilogue: TMEM -> registers -> GeGLU product -> h, or
 //               router-weighted fp32 vector reductions into y_acc
-//   warps 8-15  dequant, two warpgroups taking alternate k-blocks: nibbles +
-//               scale/bias -> bf16 weights -> TMEM
+//   warps 8-15  dequant, two warpgroups taking the k-blocks in turn: nibbles
+//               + scale/bias -> bf16 weights -> TMEM
 // Rings of mbarriers connect the roles; every wait is bounded (a timeout
 // sets the status word to MOE_ERR_TIMEOUT and the CTA drains and exits).
 #include <cuda.h>
@@ -56,8 +56,9 @@ namespace tc {
 
 using namespace umma;
 
-constexpr int kThreads = 512;
+constexpr int kDeqGroups = 2;  // dequant warpgroups, taking k-blocks in turn
 constexpr int kDeqWarp0 = 8;
+constexpr int kThreads = (kDeqWarp0 + 4 * kDeqGroups) * 32;
 constexpr int kEpiWarp0 = 4;
 constexpr int kBM = 128;      // weight rows per n-block (MMA M)
 constexpr int kMaxN = 128;    // token rows per tile (MMA N upper bound)
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNibStages; ++i) {
       mbar_init(&S.nib_full[i], 1);
-      mbar_init(&S.nib_empty[i], 8);  // both dequant warpgroups
+      mbar_init(&S.nib_empty[i], 4 * kDeqGroups);  // every dequant warp
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&S.a_full[i], 4);
@@ -223,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.sc_full[i], 1);
-      mbar_init(&S.sc_empty[i], 8);  // both dequant warpgroups
+      mbar_init(&S.sc_empty[i], 4 * kDeqGroups);  // every dequant warp
     }
     for (int i = 0; i < kAccSets; ++i) {
       mbar_init(&S.acc_full[i], 1);
@@ -464,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&S.acc_empty[set]);
     }
   } else if (warp >= kDeqWarp0) {
-    // ------------------------------------------------ dequant (two warpgroups)
-    const int grp = (warp - kDeqWarp0) >> 2;  // takes the k-blocks of its parity
+    // ------------------------------------------------ dequant (kDeqGroups warpgroups)
+    const int grp = (warp - kDeqWarp0) >> 2;  // takes every kDeqGroups-th k-block
     const int wq = warp & 3;                  // TMEM lane quarter
     const int r = 32 * wq + lane;             // A row == TMEM lane
     int nibrow;
@@ -489,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // both warpgroups wait for every stage, so that their arrivals on the
         // empty barrier always belong to the stage's current phase
         if (kk == 0 && !(ok = mbar_wait(&S.nib_full[sn], (ist / kNibStages) & 1, abort))) break;
-        if ((int)(in & 1) == grp) {
+        if ((int)(in % kDeqGroups) == grp) {
           const uint8_t *row = ringN + sn * kNibBytes + nibrow * 128;
           const uint4 q0 = *reinterpret_cast<const uint4 *>(row + (((2 * kk) ^ sw) << 4));
           const uint4 q1 = *reinterpret_cast<const uint4 *>(row + (((2 * kk + 1) ^ sw) << 4));

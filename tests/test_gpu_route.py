@@ -151,3 +151,29 @@ def test_fused_route_flags_out_of_range_ids():
     ids[7, 0] = 8
     g = fused_route(ids, 8, 32)
     assert g["status"] == mq.MOE_ERR_RANGE and g["tile_count"] == 0
+
+
+@pytest.mark.parametrize("T,k,E,offset", [
+    (4000, 8, 128, 0),   # 32000 assignments: beyond the on-chip staging of the ids
+    (2048, 8, 128, 1),   # 16384 staged, from an id buffer that is not 16-byte aligned
+    (37, 3, 5, 3),       # ragged, unaligned
+])
+def test_fused_route_large_and_unaligned_inputs(T, k, E, offset):
+    rng = np.random.default_rng(T + offset)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    a = gpu_route(ids, E, 64)
+    buf = torch.zeros(T * k + offset, dtype=torch.int32, device="cuda")
+    buf[offset:] = torch.from_numpy(ids.ravel()).cuda()
+    view = buf[offset:].view(T, k)  # data pointer offset by `offset` ints
+    r = mq.Routing(T, k, E, 64)
+    mq.moe_sort_and_build_tiles(view, E, 64, r.sorted_ids, r.perm, r.counts, r.offsets, r.tiles,
+                                r.tile_count, r.status)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) == 0
+    tc = int(r.tile_count.item())
+    assert tc == a["tile_count"]
+    assert np.array_equal(r.sorted_ids.cpu().numpy(), a["sorted_ids"])
+    assert np.array_equal(r.perm.cpu().numpy(), a["perm"])
+    assert np.array_equal(r.tiles.cpu().numpy()[:3 * tc].reshape(-1, 3), a["tiles"])
+    st, sid, perm, counts = oracle.sort_assignments(ids, E)
+    assert np.array_equal(r.perm.cpu().numpy(), perm)
