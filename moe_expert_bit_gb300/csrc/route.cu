@@ -69,12 +69,10 @@ struct SortSmem {
 };
 
 // Returns false (status raised) if an id is out of range.  Block of 64 .. kSortThreads
-// threads, a multiple of 32.  ids may be global or shared memory; sorted_copy (shared
-// memory of A ints, or null) receives a copy of the sorted ids for the tile builder.
+// threads, a multiple of 32.
 __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t A, int32_t E,
                           int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
-                          int32_t *__restrict__ counts, int32_t *__restrict__ status,
-                          int32_t *sorted_copy) {
+                          int32_t *__restrict__ counts, int32_t *__restrict__ status) {
   int32_t(*cnt)[MOE_MAX_EXPERTS] = sm.warp;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthr = blockDim.x, nw = nthr >> 5;
@@ -157,7 +155,7 @@ __device__ bool sort_body(SortSmem &sm, const int32_t *__restrict__ ids, int32_t
       const int32_t slot = cnt[warp][e] + rank;
       sorted_ids[slot] = e;
       perm[slot] = a;
-      if (sorted_copy) sorted_copy[slot] = e;
+      if (A <= kSmemSorted) sm.sorted[slot] = e;
     }
     __syncwarp();
     if (valid && rank == 0) cnt[warp][e] += __popc(same);
@@ -174,7 +172,7 @@ __global__ void __launch_bounds__(kSortThreads)
   griddep_wait();
   griddep_launch();
   if (load_status(status) != 0) return;
-  sort_body(sm, ids, A, E, sorted_ids, perm, counts, status, nullptr);
+  sort_body(sm, ids, A, E, sorted_ids, perm, counts, status);
 }
 
 constexpr int kTileThreads = 512;
@@ -291,15 +289,7 @@ __global__ void __launch_bounds__(kTileThreads)
 }
 
 // Steps a1 and a2 in one launch: the sort, then (after a block barrier, which also
-// makes this block's global writes of sorted_ids visible to it) the tile builder.  Calls of
-// up to kStageIds assignments first copy the ids into dynamic shared memory (one coalesced
-// pass; both passes of the sort then read them on-chip) and keep the sorted ids there for
-// the builder; larger calls read and check them in global memory.
-constexpr int kStageIds = 16384;
-__host__ __device__ constexpr int route_dyn_smem(int64_t A) {
-  return A <= kStageIds ? (int)(8 * A) : 0;
-}
-
+// makes this block's global writes of sorted_ids visible to it) the tile builder.
 __global__ void __launch_bounds__(kSortThreads)
     route_kernel(const int32_t *__restrict__ ids, int32_t A, int32_t E, int32_t BM,
                  int32_t *__restrict__ sorted_ids, int32_t *__restrict__ perm,
@@ -308,50 +298,20 @@ __global__ void __launch_bounds__(kSortThreads)
                  int32_t *__restrict__ status) {
   __shared__ SortSmem ssm;
   __shared__ TileSmem tsm;
-  extern __shared__ int32_t dyn[];
   griddep_wait();
   griddep_launch();
   if (load_status(status) != 0) {
     if (threadIdx.x == 0) *tile_count = 0;
     return;
   }
-  const bool staged = A <= kStageIds;
-  int32_t *ids_s = dyn, *sorted_s = dyn + A;
-  if (staged) {
-    const bool vec = (reinterpret_cast<uintptr_t>(ids) & 15) == 0;
-    const int n4 = vec ? A / 4 : 0;
-    for (int i = threadIdx.x; i < n4; i += blockDim.x)
-      reinterpret_cast<int4 *>(ids_s)[i] = __ldg(reinterpret_cast<const int4 *>(ids) + i);
-    for (int i = 4 * n4 + threadIdx.x; i < A; i += blockDim.x) ids_s[i] = __ldg(ids + i);
-    __syncthreads();
-  }
-  if (!sort_body(ssm, staged ? ids_s : ids, A, E, sorted_ids, perm, counts, status,
-                 staged ? sorted_s : nullptr)) {
+  if (!sort_body(ssm, ids, A, E, sorted_ids, perm, counts, status)) {
     if (threadIdx.x == 0) *tile_count = 0;
     return;
   }
   __syncthreads();
   // the builder checks the sort's output: its on-chip copy when there is one
-  build_body(tsm, staged ? sorted_s : sorted_ids, A, E, BM, offsets, tiles, tile_count, status,
-             ssm.off);
-}
-
-// launch of route_kernel with its dynamic shared memory (the attribute is set once per
-// device for the largest size)
-static void launch_route(const int32_t *ids, int32_t A, int32_t E, int32_t BM,
-                         int32_t *sorted_ids, int32_t *perm, int32_t *counts, int32_t *offsets,
-                         int32_t *tiles, int32_t *tile_count, int32_t *status,
-                         cudaStream_t stream) {
-  static bool configured[64];
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaFuncSetAttribute((const void *)route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         route_dyn_smem(kStageIds));
-    configured[dev] = true;
-  }
-  launch_pdl(route_kernel, dim3(1), dim3(sort_threads(A)), route_dyn_smem(A), stream, ids, A, E,
-             BM, sorted_ids, perm, counts, offsets, tiles, tile_count, status);
+  build_body(tsm, A <= kSmemSorted ? ssm.sorted : sorted_ids, A, E, BM, offsets, tiles,
+             tile_count, status, ssm.off);
 }
 
 // ---------------------------------------------------------------- router top-k + softmax
@@ -481,8 +441,7 @@ __global__ void __launch_bounds__(kSortThreads)
     return;
   }
   const int32_t A = T * k;
-  if (!sort_body(ssm, topk_ids, A, E, sorted_ids, perm, counts, status,
-                 A <= kSmemSorted ? ssm.sorted : nullptr)) {
+  if (!sort_body(ssm, topk_ids, A, E, sorted_ids, perm, counts, status)) {
     if (threadIdx.x == 0) *tile_count = 0;
     return;
   }
@@ -614,8 +573,9 @@ moe_status moe_sort_and_build_tiles(const int32_t *topk_ids, int32_t T, int32_t 
     set_error("moe_sort_and_build_tiles: max_tiles %d < required %zu", max_tiles, need);
     return MOE_ERR_INVALID_ARG;
   }
-  launch_route(topk_ids, static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets,
-               tiles, tile_count, status, stream);
+  launch_pdl(route_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, topk_ids,
+             static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets, tiles,
+             tile_count, status);
   return check_launch("moe_sort_and_build_tiles");
 }
 
@@ -699,8 +659,9 @@ moe_status moe_route_logits(const float *logits, int32_t T, int32_t E, int32_t k
   }
   launch_router(logits, T, E, k, topk_ids, topk_weights, status, stream);
   if ((st = check_launch(fn)) != MOE_OK) return st;
-  launch_route(topk_ids, static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets,
-               tiles, tile_count, status, stream);
+  launch_pdl(route_kernel, dim3(1), dim3(sort_threads(A)), 0, stream, topk_ids,
+             static_cast<int32_t>(A), E, tile_m, sorted_ids, perm, counts, offsets, tiles,
+             tile_count, status);
   return check_launch(fn);
 }
 
