@@ -154,6 +154,20 @@ def dist_init():
     return world, rank, local
 
 
+def slowest_rank_times(times_ms, dist, device):
+    """This rank's timed totals -> their maximum over all ranks: the job is as slow as its
+    slowest replica."""
+    import torch
+    t = torch.tensor(list(times_ms), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_throughput(units_per_replica, world, ms_per_step):
+    """Whole-job rate: every replica's units over the slowest replica's step time."""
+    return world * units_per_replica / (ms_per_step * 1e-3)
+
+
 def run_reference(args, world, rank):
     """The fp64 CPU oracle on the host cores, on a bounded sample of the workload."""
     if rank != 0:
@@ -400,9 +414,7 @@ def main():
     status = int(r.status.item())
 
     if world > 1:
-        t = torch.tensor([total_ms, e2e_total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_total_ms = float(t[0]), float(t[1])
+        total_ms, e2e_total_ms = slowest_rank_times([total_ms, e2e_total_ms], dist, dev)
 
     counts = np.bincount(d["topk_ids"].ravel(), minlength=E)
     touched = int((counts > 0).sum())
@@ -427,7 +439,7 @@ def main():
     if args.router_logits and T > 64:
         launches_per_step += 1  # the router over every SM, then the sort
     line = {
-        "metric": "MoE layer assignments/s", "value": world * A / (ms * 1e-3),
+        "metric": "MoE layer assignments/s", "value": job_throughput(A, world, ms),
         "unit": "assignments/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
@@ -461,7 +473,8 @@ def main():
                      "traffic": kernel_traffic(("layer_fused_" if use_fused else
                                                 "gather_qmm_geglu_") + args.config),
                      "algorithmic_bytes": geglu_bytes},
-        "e2e": {"value": world * A / (e2e_total_ms / args.steps * 1e-3), "unit": "assignments/s",
+        "e2e": {"value": job_throughput(A, world, e2e_total_ms / args.steps),
+                "unit": "assignments/s",
                 "h2d_bytes_per_step": int(x_h.numel() * 2 + (logits_h.numel() * 4 if args.router_logits
                                           else ids_h.numel() * 4 + tw_h.numel() * 4)),
                 "d2h_bytes_per_step": int(y_h.numel() * 2)},

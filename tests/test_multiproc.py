@@ -1,0 +1,78 @@
+"""The multi-process path of bench.py on CPU (gloo, world size 2).
+
+The layer does not exchange data between GPUs (one independent replica per rank, no
+collective on the data path); what the benchmark does across ranks is host logic: the
+slowest rank's time is the job's time, the job's rate counts every rank's units, and only
+rank 0 prints.  Both are exercised here with two real processes.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, times, out_q):
+    import torch.distributed as dist
+
+    import bench
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        got = bench.slowest_rank_times(times[rank], dist, "cpu")
+        dist.barrier()
+        out_q.put((rank, got))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_slowest_rank_time_over_two_gloo_ranks():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    times = [[10.0, 31.5], [12.5, 30.0]]  # rank 1 is slower on the first total
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, times, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = dict(q.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got[0] == got[1] == [12.5, 31.5]
+
+
+def test_job_throughput_counts_every_replica():
+    import bench
+    # 32 assignments per replica, 40 us per (slowest) step
+    assert bench.job_throughput(32, 1, 0.040) == pytest.approx(800_000.0)
+    assert bench.job_throughput(32, 2, 0.040) == pytest.approx(1_600_000.0)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    """`bench.py --impl reference` launched as two ranks: rank 0 times the oracle and prints
+    one JSON line, rank 1 exits 0 without work."""
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py",
+           "--impl", "reference", "--gpus", "2", "--steps", "1", "--warmup", "3",
+           "--config", "tiny", "--ref-slots", "8"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    rec = json.loads(lines[0])
+    assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
+    assert rec["e2e"]["h2d_bytes_per_step"] == 0
