@@ -290,14 +290,18 @@ def main():
     E, H, I, T, k = d["E"], d["H"], d["I"], d["T"], d["k"]
     A = T * k
     W = device_weights(d, dev, torch)
-    x_h = pinned_bf16(d["x"], torch)
-    ids_h = torch.from_numpy(d["topk_ids"]).pin_memory()
-    tw_h = torch.from_numpy(d["topk_weights"]).pin_memory()
-    x = x_h.to(dev)
-    ids = ids_h.to(dev)
-    tw = tw_h.to(dev)
-    logits_h = torch.from_numpy(d["router_logits"]).pin_memory()
-    logits = logits_h.to(dev)
+    # a step's inputs sit back to back in one pinned host buffer and one device buffer, so
+    # that the end-to-end step moves them in one copy: x and the top-k ids and weights, or x
+    # and the router logits
+    if args.router_logits:
+        in_h, in_d, (x, logits) = packed_inputs([d["x"].view(np.int16), d["router_logits"]],
+                                                [torch.bfloat16, torch.float32], torch, dev)
+        ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+        tw = torch.empty(T, k, dtype=torch.float32, device=dev)
+    else:
+        in_h, in_d, (x, ids, tw) = packed_inputs(
+            [d["x"].view(np.int16), d["topk_ids"], d["topk_weights"]],
+            [torch.bfloat16, torch.int32, torch.float32], torch, dev)
     buf = mq.MoeLayerBuffers(T, k, E, H, I, args.tile_m, device=dev,
                              deterministic=args.deterministic)
     y_h = torch.empty(T, H, dtype=torch.bfloat16).pin_memory()
@@ -349,12 +353,7 @@ def main():
             ev[2].record(stream)
 
     def e2e_step():
-        x.copy_(x_h, non_blocking=True)
-        if args.router_logits:
-            logits.copy_(logits_h, non_blocking=True)
-        else:
-            ids.copy_(ids_h, non_blocking=True)
-            tw.copy_(tw_h, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
         step()
         y_h.copy_(buf.y, non_blocking=True)
 
@@ -475,8 +474,7 @@ def main():
                      "algorithmic_bytes": geglu_bytes},
         "e2e": {"value": job_throughput(A, world, e2e_total_ms / args.steps),
                 "unit": "assignments/s",
-                "h2d_bytes_per_step": int(x_h.numel() * 2 + (logits_h.numel() * 4 if args.router_logits
-                                          else ids_h.numel() * 4 + tw_h.numel() * 4)),
+                "h2d_bytes_per_step": int(in_h.numel()),
                 "d2h_bytes_per_step": int(y_h.numel() * 2)},
         "clocks": clk,
         "gpu_launches": launches_per_step * args.steps,
@@ -503,8 +501,20 @@ def device_weights(d, dev, torch):
     return out
 
 
-def pinned_bf16(a, torch):
-    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+def packed_inputs(arrays, dtypes, torch, dev):
+    """numpy arrays -> (pinned host bytes, device bytes, device views of each array in its
+    torch dtype), each array at a 16-byte aligned offset of the two buffers."""
+    offs, total = [], 0
+    for a in arrays:
+        offs.append(total)
+        total += (a.nbytes + 15) // 16 * 16
+    host = torch.zeros(total, dtype=torch.uint8).pin_memory()
+    hv = host.numpy()
+    for a, o in zip(arrays, offs):
+        hv[o:o + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).ravel()
+    devbuf = host.to(dev)
+    views = [devbuf[o:o + a.nbytes].view(dt).view(a.shape) for a, o, dt in zip(arrays, offs, dtypes)]
+    return host, devbuf, views
 
 
 if __name__ == "__main__":
