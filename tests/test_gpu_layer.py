@@ -197,3 +197,31 @@ def test_geglu_workspace_entry_equals_gathering_entry(case):
     assert torch.equal(h0, h1)
     perm = r.perm.cpu().numpy()
     assert torch.equal(xs.cpu(), dev["x"].cpu()[torch.from_numpy(perm // d["k"]).long()])
+
+
+@pytest.mark.parametrize("E,H,I,T,k,variant", [
+    (256, 128, 64, 64, 4, mq.VARIANT_GEMV),   # the most experts the layer takes
+    (256, 128, 64, 64, 4, mq.VARIANT_TC),
+    (3, 3904, 128, 9, 2, mq.VARIANT_GEMV),    # the widest hidden size of the GEMV (a padded
+                                              # row of 1952 B fills one TMA box)
+    (3, 4096, 128, 9, 2, mq.VARIANT_TC),      # the widest reduction of the tensor-core GEMM
+    (3, 192, 3904, 9, 2, mq.VARIANT_GEMV),    # the widest intermediate size of the GEMV
+])
+def test_largest_shapes_each_variant_takes(E, H, I, T, k, variant):
+    _variant_or_skip(variant)
+    d = synth.make_custom(E, H, I, T, k, seed=8)
+    full_compare(d, 128, variant)
+
+
+def test_widths_beyond_the_variants_are_refused():
+    """H = 4096 is beyond the GEMV's one-box rows and H = 4160 beyond the tensor-core
+    reduction: the library says so before any launch; AUTO picks the variant that takes it."""
+    d = synth.make_custom(2, 4096, 64, 4, 1, seed=9)
+    with pytest.raises(mq.MoeError) as ei:
+        run_layer(d, 128, mq.VARIANT_GEMV)
+    assert ei.value.status == mq.MOE_ERR_UNSUPPORTED
+    full_compare(d, 128, mq.VARIANT_AUTO)  # the tensor-core GEMM takes it
+    d = synth.make_custom(2, 4160, 64, 4, 1, seed=9)
+    with pytest.raises(mq.MoeError) as ei:
+        run_layer(d, 128, mq.VARIANT_AUTO)
+    assert ei.value.status == mq.MOE_ERR_UNSUPPORTED
