@@ -36,7 +36,7 @@ constexpr int kFPassD = 4;                       // down rows staged per pass (t
 constexpr int kFMaxA = 256;                      // assignments the fused kernel takes
 constexpr int kFMaxT = 64;                       // token rows it stages
 constexpr int kFCountQ = 4;                      // down blocks counted per fence
-// named barriers: 1 compute + stager (grid barrier), 2 + 2p / 3 + 2p team p's combine,
+// named barriers: 1 the compute warps (gate/up done; CTA done), 2 + 2p / 3 + 2p team p's combine,
 // 10 the tile list is ready (the producer arrives, every other warp waits), 11 the
 // routing among the non-producer warps, 15 the start (compute + stager)
 constexpr int kFBarGrid = 1, kFBarTiles = 10, kFBarRoute = 11, kFBarStart = 15;
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint64_t *xempty = xready + 2;   // [2] every compute warp done with them
   uint64_t *scratch_free = xempty + 2;  // the routing scratch in the last slot is released
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gsm + L.off_misc);
-  int *s_flags = reinterpret_cast<int *>(gsm + L.off_misc + 4);  // [0] range, [1] order
+  int *s_flags = reinterpret_cast<int *>(gsm + L.off_misc + 4);  // [0] range or status
   int *s_ntiles = reinterpret_cast<int *>(gsm + L.off_misc + 12);
   uint32_t *issued = reinterpret_cast<uint32_t *>(gsm + L.off_misc + 16);  // chunks issued
   unsigned long long *s_gbase =  // the finished-CTA count read at the start
@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     *abort_flag = 0;
     *s_order_bad = 0;
     *issued = 0;
-    s_flags[0] = s_flags[1] = 0;
+    s_flags[0] = 0;
     fence_mbar_init();
     // the token rows go out first: they depend on nothing
     mbar_arrive_expect_tx(&xfull[0], (uint32_t)p.T * xbytes_g);
@@ -777,7 +777,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   a.gbar = reinterpret_cast<unsigned long long *>(a.cnt + H / 16);
   a.tflags = reinterpret_cast<uint32_t *>(a.cnt + H / 16 + 4);
   a.y = y;
-  // cooperative: every CTA resident at once (the grid barrier waits for all of them)
+  // cooperative: every CTA resident at once (a tile's down phase waits for other CTAs' gate/up)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(fused_sm_count());
   cfg.blockDim = dim3(kFThreads);

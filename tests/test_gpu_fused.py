@@ -91,7 +91,7 @@ def test_fused_equals_four_calls_and_leaves_workspace_zero():
     assert torch.equal(b2.h, ref.h)
     assert np.abs(bf16_to_f64(b2.y) - y1).max() <= 2e-2 * max(1.0, np.abs(y1).max())
     assert int(torch.count_nonzero(b2.y_acc[:n_zero]).item()) == 0
-    # the grid barrier's arrival count (after the counters): one per CTA per call
+    # the count of finished CTAs (after the counters): one per CTA per call
     n_sm = torch.cuda.get_device_properties(0).multi_processor_count
     assert int(b2.y_acc[n_zero:n_zero + 2].view(torch.int64).item()) == 2 * n_sm
 
