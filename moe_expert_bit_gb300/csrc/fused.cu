@@ -83,6 +83,7 @@ struct FArgs {
   const int32_t *topk_ids;
   const float *topk_weights;
   const uint16_t *x, *Sgu, *Bgu, *Sd, *Bd;
+  const uint32_t *Wd;  // the packed down rows (for the L2 prefetch of the last down chunks)
   int32_t T, k, A, E, H, I, BM, max_tiles, nbuf;
   int32_t act;  // the gate activation of the gated product (MOE_ACT_*)
   int32_t *sorted_ids, *perm, *counts, *offsets, *tiles, *tile_count, *status;
@@ -366,6 +367,23 @@ __global__ void __launch_bounds__(kFThreads, 1)
     const uint32_t tx_g = 16u * L.Sh + 64u * Gh;
     const uint32_t tx_d = (uint32_t)kFDownRows * L.Si + 4u * kFDownRows * Gi;
     for (int phase = 0; phase < 2 && ok; ++phase) {
+      if (phase == 1 && lane < 3) {
+        // the down chunks beyond the ring's first fill would be fetched only once down
+        // compute frees their buffers: fetch them into L2 now, while the grid finishes its
+        // gate/up and hands off (HBM is otherwise idle then).  Per tile their packed rows,
+        // scales and biases are each one contiguous range.
+        const int pf0 = d0 + nbuf;
+        for (int tl = pf0 / cpt_d; pf0 < d1 && tl * cpt_d < d1; ++tl) {
+          const int ja = max(pf0 - tl * cpt_d, 0), jb = min(d1 - tl * cpt_d, cpt_d);
+          const int64_t r = (int64_t)s_tiles[3 * tl] * p.H + (int64_t)kFDownRows * ja;
+          const uint32_t rows = (uint32_t)(kFDownRows * (jb - ja));
+          if (lane == 0)
+            bulk_prefetch_l2(reinterpret_cast<const uint8_t *>(p.Wd) + r * (p.I / 2),
+                             rows * (uint32_t)(p.I / 2));
+          else
+            bulk_prefetch_l2((lane == 1 ? p.Sd : p.Bd) + r * Gi, 2u * rows * Gi);
+        }
+      }
       const int c0 = phase ? d0 : g0, c1 = phase ? d1 : g1, cpt = phase ? cpt_d : cpt_g;
       const int pass = phase ? kFPassD : kFPassG;
       for (int tile = c0 / cpt; ok && tile * cpt < c1; ++tile) {
@@ -751,6 +769,7 @@ moe_status launch_fused_layer(const int32_t *topk_ids, const float *topk_weights
   a.Bgu = Bgu;
   a.Sd = Sd;
   a.Bd = Bd;
+  a.Wd = Wd;
   a.T = T;
   a.k = k;
   a.A = A;
