@@ -109,6 +109,12 @@ struct Params {
   int32_t act;              // GEGLU: the gate activation (MOE_ACT_*)
 };
 
+// The B operand's tensor maps: the same rows with boxes of 16, 32, 64 and 128 rows (a tile of
+// na rows loads each k-block with one na-row box; gathering launches pass one-row boxes)
+struct XMaps {
+  CUtensorMap m[4];
+};
+
 struct Smem {
   uint64_t nib_full[kNibStages], nib_empty[kNibStages];
   uint64_t a_full[kAStages], a_empty[kAStages];
@@ -190,7 +196,8 @@ __device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                   const __grid_constant__ CUtensorMap tmap_x, const Params p) {
+                   const __grid_constant__ XMaps xmaps, const Params p) {
+  const CUtensorMap &tmap_x = xmaps.m[0];
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
@@ -240,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmap_w);
-    prefetch_tensormap(&tmap_x);
+    for (int i = 0; i < 4; ++i) prefetch_tensormap(&xmaps.m[i]);
   }
   tc_fence_before();
   __syncthreads();
@@ -332,15 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         S.tok[min(j + 3, U.R - 1)], &S.b_full[sb]);
           }
         } else {
-          // contiguous sorted rows (h, or x gathered into slot order beforehand), 16 per box
-          const int nbox = na / 16;
+          // contiguous sorted rows (h, or x gathered into slot order beforehand): each
+          // k-block's na rows in one box (one copy instruction), from the map of that height
+          const CUtensorMap *mx = &xmaps.m[na == 16 ? 0 : na == 32 ? 1 : na == 64 ? 2 : 3];
           if (lane == 0) mbar_arrive_expect_tx(&S.b_full[sb], (uint32_t)(nk * na * 128));
           __syncwarp();
-          for (int i = lane; i < nk * nbox; i += 32) {
-            const int kk = i / nbox, bx = i - kk * nbox;
-            tma_load_2d(stage + kk * na * 128 + bx * 2048, &tmap_x, (kb0 + kk) * 64,
-                        U.row0 + bx * 16, &S.b_full[sb]);
-          }
+          if (lane < nk)
+            tma_load_2d(stage + lane * na * 128, mx, (kb0 + lane) * 64, U.row0, &S.b_full[sb]);
         }
       }
     }
@@ -550,8 +555,17 @@ static int num_sms() {
   return n;
 }
 
+// bf16 rows [rows, cols] with boxes of 64 columns x {16, 32, 64, 128} rows (128-byte swizzle)
+static bool make_row_maps(XMaps *xm, const void *base, int cols, int rows) {
+  for (int i = 0; i < 4; ++i)
+    if (!make_map_2d(&xm->m[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, (uint64_t)cols,
+                     (uint64_t)rows, 64, 16u << i, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  return true;
+}
+
 template <int MODE>
-static moe_status launch(const CUtensorMap &mw, const CUtensorMap &mx, const Params &p,
+static moe_status launch(const CUtensorMap &mw, const XMaps &xm, const Params &p,
                          const moe_tiles_t &t, cudaStream_t stream, const char *what) {
   const int smem = smem_bytes<MODE>(p.K);
   int dev = 0;
@@ -567,7 +581,7 @@ static moe_status launch(const CUtensorMap &mw, const CUtensorMap &mx, const Par
   int grid = num_sms();
   if (max_units < grid) grid = max_units;
   if (grid < 1) grid = 1;
-  gemm_tc_kernel<MODE><<<grid, kThreads, smem, stream>>>(mw, mx, p);
+  gemm_tc_kernel<MODE><<<grid, kThreads, smem, stream>>>(mw, xm, p);
   return check_launch(what);
 }
 
@@ -626,7 +640,9 @@ moe_status launch_geglu_tc(const uint16_t *x, const uint32_t *Wgu, const uint16_
   p.rows_per_expert = 2 * I;
   p.num_blocks = I / 64;
   p.act = act;
-  return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
+  tc::XMaps xm;  // rows are gathered with one-row boxes: every entry the same map
+  for (int i = 0; i < 4; ++i) xm.m[i] = mx;
+  return tc::launch<tc::GEGLU>(mw, xm, p, t, stream, what);
 }
 
 moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const uint16_t *Sgu,
@@ -643,11 +659,11 @@ moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const 
              reinterpret_cast<uint4 *>(x_sorted), (const int32_t *)t.status);
   moe_status st = check_launch(what);
   if (st != MOE_OK) return st;
-  CUtensorMap mw, mx;
+  CUtensorMap mw;
+  tc::XMaps xm;
   if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wgu, H / 8,
                    (uint64_t)t.num_experts * 2 * I, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x_sorted, H, t.num_assignments, 64,
-                   16, CU_TENSOR_MAP_SWIZZLE_128B)) {
+      !tc::make_row_maps(&xm, x_sorted, H, t.num_assignments)) {
     set_error("%s: tensor map encoding failed", what);
     return MOE_ERR_CUDA;
   }
@@ -668,7 +684,7 @@ moe_status launch_geglu_tc_sorted(const uint16_t *x, const uint32_t *Wgu, const 
   p.num_blocks = I / 64;
   p.act = act;
   p.x_sorted = 1;
-  return tc::launch<tc::GEGLU>(mw, mx, p, t, stream, what);
+  return tc::launch<tc::GEGLU>(mw, xm, p, t, stream, what);
 }
 
 moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_t *Sd,
@@ -676,11 +692,11 @@ moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_
                           int32_t H, int32_t I, float *y_acc, bool per_slot,
                           cudaStream_t stream) {
   const char *what = "moe_gather_qmm_down_unsort (tensor cores)";
-  CUtensorMap mw, mx;
+  CUtensorMap mw;
+  tc::XMaps xm;
   if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Wd, I / 8,
                        (uint64_t)t.num_experts * H, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, hin, I, t.num_assignments, 64,
-                       16, CU_TENSOR_MAP_SWIZZLE_128B)) {
+      !tc::make_row_maps(&xm, hin, I, t.num_assignments)) {
     set_error("%s: tensor map encoding failed", what);
     return MOE_ERR_CUDA;
   }
@@ -700,7 +716,7 @@ moe_status launch_down_tc(const uint16_t *hin, const uint32_t *Wd, const uint16_
   p.N_out = H;
   p.rows_per_expert = H;
   p.num_blocks = (H + tc::kBM - 1) / tc::kBM;
-  return tc::launch<tc::DOWN>(mw, mx, p, t, stream, what);
+  return tc::launch<tc::DOWN>(mw, xm, p, t, stream, what);
 }
 
 }  // namespace moeqmm
