@@ -22,8 +22,11 @@
 // The dequantised weight tile is the MMA's A operand and lives in TMEM: the
 // dequant warps write it with tcgen05.st (a 128 x 64 bf16 k-block is 32
 // columns) and tcgen05.mma reads it from there, so weights never make a
-// round trip through shared memory.  TMEM: columns [0, 128) hold four A
-// stages, [128, 512) three fp32 accumulators of 128 columns.
+// round trip through shared memory.  TMEM: columns [0, 128) hold two A
+// stages of two k-blocks each, [128, 512) three fp32 accumulators of 128
+// columns.  The single MMA-issuing thread pays an mbarrier wait, a fence and
+// a commit per A stage and per B stage, each worth roughly one MMA issue, so
+// both kinds of stage carry two k-blocks of a full tile.
 //
 // One persistent CTA per SM, 16 warps with fixed roles:
 //   warp 0      W producer: TMA of the packed nibbles (128-byte row segments,
@@ -63,11 +66,13 @@ constexpr int kEpiWarp0 = 4;
 constexpr int kBM = 128;      // weight rows per n-block (MMA M)
 constexpr int kMaxN = 128;    // token rows per tile (MMA N upper bound)
 constexpr int kNibKB = 4;       // k-blocks per nibble stage: 128-byte rows
-constexpr int kNibStages = 5;
-constexpr int kAStages = 4;   // TMEM A stages of 32 columns
+constexpr int kNibStages = 4;
+constexpr int kAStages = 2;   // TMEM A stages of two k-blocks (64 columns)
+constexpr int kAStageKB = 2;  // k-blocks per A stage: one wait, one fence, one commit per pair
 constexpr int kAccSets = 3;   // TMEM accumulators of 128 columns
 constexpr int kNibBytes = kBM * 32 * kNibKB;  // 128 rows x 128 bytes (4 k-blocks)
-constexpr int kBBytes = kMaxN * 128;  // one stage: kMaxN rows x 1 k-block, or fewer rows x more k-blocks
+constexpr int kBKB = 2;  // k-blocks of a full (kMaxN-row) tile per B stage
+constexpr int kBBytes = kMaxN * 128 * kBKB;  // one stage: kMaxN rows x 2 k-blocks, or fewer rows x more
 constexpr int kAccCols = 128;
 constexpr int kTmemCols = 512;
 constexpr int kMaxK = 4096;
@@ -78,7 +83,7 @@ enum Mode { GEGLU = 0, DOWN = 1 };
 
 template <int MODE>
 struct Cfg {
-  static constexpr int kBStages = 5;
+  static constexpr int kBStages = 3;
   static constexpr int kOffB = 0;
   static constexpr int kOffNib = kOffB + kBStages * kBBytes;
   static constexpr int kOffEpi = kOffNib + kNibStages * kNibBytes;
@@ -253,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = S.tmem_base;
-  const uint32_t tmem_acc = tmem_base + kAStages * 32;
+  const uint32_t tmem_acc = tmem_base + kAStages * kAStageKB * 32;
 
   if (warp == 0) {
     // ------------------------------------------------ W producer: scales + packed nibbles
@@ -311,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; ok && u < total_units; u += gridDim.x) {
       const Unit U = get_unit(p, u);
       const int na = n_alloc_of(U.R);
-      const int kbps = kMaxN / na;  // k-blocks per stage
+      const int kbps = kMaxN * kBKB / na;  // k-blocks per stage
       const int nst = (G + kbps - 1) / kbps;
       const bool gather = MODE == GEGLU && !p.x_sorted;
       if (gather) {
@@ -365,32 +370,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t N = (uint32_t)max(16, (U.R + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32(kBM, N);
         const int na = n_alloc_of(U.R);
-        const int kbps = kMaxN / na;
+        const int kbps = kMaxN * kBKB / na;
         const int set = iacc % kAccSets;
         if (!(ok = mbar_wait(&S.acc_empty[set], ((iacc / kAccSets) & 1) ^ 1, abort))) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_acc + (uint32_t)(set * kAccCols);
         int sb = 0;
-        for (int kb = 0; kb < G; ++kb, ++ia) {
-          const int kk = kb % kbps;
-          if (kk == 0) {
-            sb = ib % kBStages;
-            if (!(ok = mbar_wait(&S.b_full[sb], (ib / kBStages) & 1, abort))) break;
-          }
+        for (int kb0 = 0; kb0 < G; kb0 += kAStageKB, ++ia) {
           const int sa = ia % kAStages;
           if (!(ok = mbar_wait(&S.a_full[sa], (ia / kAStages) & 1, abort))) break;
           tc_fence_after();
-          const uint32_t a_tmem = tmem_base + (uint32_t)(sa * 32);
-          const uint32_t b0 = smem_addr(ringB + sb * kBBytes) + (uint32_t)(kk * na * 128);
+          const int nkb = min(kAStageKB, G - kb0);
+          for (int j = 0; j < nkb; ++j) {
+            const int kb = kb0 + j;
+            const int kk = kb % kbps;
+            if (kk == 0) {
+              sb = ib % kBStages;
+              if (!(ok = mbar_wait(&S.b_full[sb], (ib / kBStages) & 1, abort))) break;
+            }
+            const uint32_t a_tmem = tmem_base + (uint32_t)((sa * kAStageKB + j) * 32);
+            const uint32_t b0 = smem_addr(ringB + sb * kBBytes) + (uint32_t)(kk * na * 128);
 #pragma unroll
-          for (int k16 = 0; k16 < 4; ++k16)
-            umma_f16_ta(d_tmem, a_tmem + 8 * k16, smem_desc_k128(b0 + 32 * k16), idesc,
-                        (kb | k16) != 0);
-          umma_commit(&S.a_empty[sa]);
-          if (kk == kbps - 1 || kb == G - 1) {
-            umma_commit(&S.b_empty[sb]);
-            ++ib;
+            for (int k16 = 0; k16 < 4; ++k16)
+              umma_f16_ta(d_tmem, a_tmem + 8 * k16, smem_desc_k128(b0 + 32 * k16), idesc,
+                          (kb | k16) != 0);
+            if (kk == kbps - 1 || kb == G - 1) {
+              umma_commit(&S.b_empty[sb]);
+              ++ib;
+            }
           }
+          if (!ok) break;
+          umma_commit(&S.a_empty[sa]);
         }
         if (!ok) break;
         umma_commit(&S.acc_full[set]);
@@ -489,40 +499,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int set = isc & 1;
       if (!(ok = mbar_wait(&S.sc_full[set], (isc >> 1) & 1, abort))) break;
       const uint16_t *sc = reinterpret_cast<const uint16_t *>(ringS + set * scb) + nibrow * G;
-      for (int kb = 0; kb < G; ++kb, ++in) {
-        const int kk = kb % kNibKB;
+      for (int kb0 = 0; kb0 < G; kb0 += kAStageKB, ++in) {
+        // one A stage: k-blocks kb0 and kb0 + 1 (one only at an odd end), both inside the
+        // same nibble stage (kNibKB is a multiple of kAStageKB)
+        const int nkb = min(kAStageKB, G - kb0);
+        const int kk0 = kb0 % kNibKB;
         const int sn = ist % kNibStages;
-        // both warpgroups wait for every stage, so that their arrivals on the
-        // empty barrier always belong to the stage's current phase
-        if (kk == 0 && !(ok = mbar_wait(&S.nib_full[sn], (ist / kNibStages) & 1, abort))) break;
+        // every dequant warpgroup waits for every nibble stage, so that their arrivals on
+        // the empty barrier always belong to the stage's current phase
+        if (kk0 == 0 && !(ok = mbar_wait(&S.nib_full[sn], (ist / kNibStages) & 1, abort))) break;
         if ((int)(in % kDeqGroups) == grp) {
-          const uint8_t *row = ringN + sn * kNibBytes + nibrow * 128;
-          const uint4 q0 = *reinterpret_cast<const uint4 *>(row + (((2 * kk) ^ sw) << 4));
-          const uint4 q1 = *reinterpret_cast<const uint4 *>(row + (((2 * kk + 1) ^ sw) << 4));
-          const uint16_t s16 = sc[kb], b16 = sc[kBM * G + kb];
-          const uint32_t s2u = (uint32_t)s16 | ((uint32_t)s16 << 16);
-          const uint32_t b2u = (uint32_t)b16 | ((uint32_t)b16 << 16);
-          const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&b2u);
-          uint32_t w[32];
-          dequant8(q0.x, s2, b2, w + 0);
-          dequant8(q0.y, s2, b2, w + 4);
-          dequant8(q0.z, s2, b2, w + 8);
-          dequant8(q0.w, s2, b2, w + 12);
-          dequant8(q1.x, s2, b2, w + 16);
-          dequant8(q1.y, s2, b2, w + 20);
-          dequant8(q1.z, s2, b2, w + 24);
-          dequant8(q1.w, s2, b2, w + 28);
           const int sa = in % kAStages;
-          if (!(ok = mbar_wait(&S.a_empty[sa], ((in / kAStages) & 1) ^ 1, abort))) break;
-          tc_fence_after();
-          tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)(sa * 32), w);
-          tmem_st_wait();
+          for (int j = 0; j < nkb && ok; ++j) {
+            const int kb = kb0 + j, kk = kk0 + j;
+            const uint8_t *row = ringN + sn * kNibBytes + nibrow * 128;
+            const uint4 q0 = *reinterpret_cast<const uint4 *>(row + (((2 * kk) ^ sw) << 4));
+            const uint4 q1 = *reinterpret_cast<const uint4 *>(row + (((2 * kk + 1) ^ sw) << 4));
+            const uint16_t s16 = sc[kb], b16 = sc[kBM * G + kb];
+            const uint32_t s2u = (uint32_t)s16 | ((uint32_t)s16 << 16);
+            const uint32_t b2u = (uint32_t)b16 | ((uint32_t)b16 << 16);
+            const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162 *>(&s2u);
+            const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162 *>(&b2u);
+            uint32_t w[32];
+            dequant8(q0.x, s2, b2, w + 0);
+            dequant8(q0.y, s2, b2, w + 4);
+            dequant8(q0.z, s2, b2, w + 8);
+            dequant8(q0.w, s2, b2, w + 12);
+            dequant8(q1.x, s2, b2, w + 16);
+            dequant8(q1.y, s2, b2, w + 20);
+            dequant8(q1.z, s2, b2, w + 24);
+            dequant8(q1.w, s2, b2, w + 28);
+            if (j == 0) {  // the stage's previous MMAs have read it
+              if (!(ok = mbar_wait(&S.a_empty[sa], ((in / kAStages) & 1) ^ 1, abort))) break;
+              tc_fence_after();
+            }
+            tmem_st_32x32b_x32(tmem_base + a_lane + (uint32_t)((sa * kAStageKB + j) * 32), w);
+            tmem_st_wait();
+          }
+          if (!ok) break;
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.a_full[sa]);
         }
-        if (kk == kNibKB - 1 || kb == G - 1) {
+        if ((kb0 + nkb) % kNibKB == 0 || kb0 + nkb == G) {
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.nib_empty[sn]);
           ++ist;
