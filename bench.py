@@ -432,6 +432,11 @@ def main():
         torch.cuda.synchronize(dev)
         return t0.elapsed_time(t1)
 
+    # the clock sampler starts first, so that no idle pause separates the warm-up steps from
+    # the timed ones
+    clocks = ClockSampler(dev.index if world == 1 else local)
+    clocks.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         flush_l2()
         step()
@@ -440,9 +445,6 @@ def main():
         raise SystemExit(f"device status {int(r.status.item())} after warm-up")
 
     # ---- timed region: K steps, L2 flushed between them outside the events ----
-    clocks = ClockSampler(dev.index if world == 1 else local)
-    clocks.start()
-    time.sleep(0.3)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
@@ -545,6 +547,8 @@ def main():
                    "l2": "flushed between steps outside the timed events: 512 MB write, "
                          "then 256 MB read (the flush's dirty lines written back)",
                    "parallelism": f"{world} independent replica(s), no collective"},
+        "step_us_spread": {"min": 1e3 * min(step_ms), "median": 1e3 * statistics.median(step_ms),
+                           "max": 1e3 * max(step_ms)},
         "weight_GBps": w_bytes / (ms * 1e-3) / 1e9,
         "TFLOPs": flops / (ms * 1e-3) / 1e12,
         "layer_roofline": {"t_roof_us": t_roof_ms * 1e3, "frac": t_roof_ms / ms,
