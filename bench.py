@@ -13,6 +13,8 @@ kernel may start while the previous one finishes), with the 129 MB L2
 flushed between steps outside the events: a 512 MB write, then a 256 MB read
 so that the flush's dirty lines are written back before the step starts;
 barrier + synchronize on both sides of the timed region; the max over ranks.
+One untimed flush is queued ahead of the first step, and Python's collector is off
+during the timed passes, so that no host time falls between a step's events.
 A second pass of K steps with events between the calls gives the per-kernel
 breakdown and the roofline figure of the gate/up kernel.  Under torchrun each rank runs its own copy of
 the workload on its own GPU (independent layers, no collective): weak
@@ -24,6 +26,7 @@ method has here) on the host cores, on a bounded sample of the workload.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -445,11 +448,20 @@ def main():
         raise SystemExit(f"device status {int(r.status.item())} after warm-up")
 
     # ---- timed region: K steps, L2 flushed between them outside the events ----
+    # Python's collector stays off through the timed passes (as timeit does): a collection
+    # that lands while the GPU has nothing queued (the first step after the synchronize)
+    # would add host time to that step's events
+    gc.collect()
+    gc.disable()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     wall0 = time.perf_counter()
+    # one more flush ahead of the first step: the GPU queue is empty after the synchronize,
+    # and this gives the host time to enqueue step 0 before its first event is reached
+    # (every later step already has the previous flush ahead of it)
+    flush_l2()
     for i in range(args.steps):
         flush_l2()
         ev[i][0].record(stream)
@@ -464,6 +476,7 @@ def main():
 
     # ---- breakdown pass: events between the calls (which also serialises them) ----
     bev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    flush_l2()  # the host ahead of step 0, as above
     for i in range(args.steps):
         flush_l2()
         bev[i][0].record(stream)
@@ -480,6 +493,7 @@ def main():
         e2e_step()
     torch.cuda.synchronize(dev)
     e2e_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    flush_l2()  # the host ahead of step 0, as above
     for i in range(args.steps):
         flush_l2()
         e2e_ev[i][0].record(stream)
@@ -503,6 +517,7 @@ def main():
     e2e_check = all(
         bool(((st["y_h"].float() - y_ref).abs() <= 2e-2 * y_ref.abs().clamp(min=1.0)).all())
         for st in sets)
+    gc.enable()
     clk = clocks.stop()
     status = max(int(st["buf"].routing.status.item()) for st in sets)
 
