@@ -124,26 +124,76 @@ def _check(status: int):
         raise MoeError(status, msg)
 
 
-def _ptr(t, dtype, name, numel=None):
-    if t is None:
-        return None
-    if not isinstance(t, torch.Tensor):
-        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: expected a torch.Tensor")
-    if t.dtype != dtype:
-        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: dtype {t.dtype}, expected {dtype}")
-    if not t.is_cuda:
-        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: must be a CUDA tensor")
-    if not t.is_contiguous():
-        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: must be contiguous")
-    if numel is not None and t.numel() < numel:
-        raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: {t.numel()} elements, need {numel}")
-    return ctypes.c_void_p(t.data_ptr())
+class _Call:
+    """The tensors of one library call.
+
+    Each tensor is checked as it is marshalled: its dtype, at least the elements the call's
+    shapes imply (the C ABI takes plain pointers and cannot check a size, so a short tensor
+    would be read or written past its end), and contiguity.  Their device is checked when
+    the stream, the last argument of every entry point, is marshalled: every tensor on the
+    GPU the call runs on, and the stream on it too.
+    """
+
+    __slots__ = ("tensors",)
+
+    def __init__(self):
+        self.tensors = []
+
+    def __call__(self, t, dtype, name, numel=None):
+        if t is None:
+            return None
+        if not isinstance(t, torch.Tensor):
+            raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: expected a torch.Tensor")
+        if t.dtype != dtype:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: dtype {t.dtype}, expected {dtype}")
+        if numel is not None and t.numel() < numel:
+            raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: {t.numel()} elements, need {numel}")
+        if not t.is_contiguous():
+            raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: must be contiguous")
+        self.tensors.append((t, name))
+        return ctypes.c_void_p(t.data_ptr())
+
+    def bf16(self, t, name, numel=None):
+        return self(t, torch.bfloat16, name, numel)
+
+    def gate_up(self, Wgu, Sgu, Bgu, E, H, I):
+        """Wgu [E, 2I, H/8] (uint32 as int32), Sgu and Bgu [E, 2I, H/64] bf16."""
+        return (self(Wgu, torch.int32, "Wgu", E * 2 * I * (H // 8)),
+                self.bf16(Sgu, "Sgu", E * 2 * I * (H // 64)),
+                self.bf16(Bgu, "Bgu", E * 2 * I * (H // 64)))
+
+    def down(self, Wd, Sd, Bd, E, H, I):
+        """Wd [E, H, I/8] (uint32 as int32), Sd and Bd [E, H, I/64] bf16."""
+        return (self(Wd, torch.int32, "Wd", E * H * (I // 8)),
+                self.bf16(Sd, "Sd", E * H * (I // 64)),
+                self.bf16(Bd, "Bd", E * H * (I // 64)))
+
+    def stream(self, stream):
+        cur = None
+        for t, name in self.tensors:
+            if not t.is_cuda:
+                raise MoeError(MOE_ERR_INVALID_ARG, f"{name}: must be a CUDA tensor")
+            if cur is None:
+                cur = torch.cuda.current_device()
+            if t.device.index != cur:
+                raise MoeError(MOE_ERR_INVALID_ARG,
+                               f"{name}: on {t.device}, but the call runs on cuda:{cur}")
+        if stream is None:
+            stream = torch.cuda.current_stream()
+        dev = getattr(stream, "device_index", None)
+        if dev is not None and cur is not None and dev != cur:
+            raise MoeError(MOE_ERR_INVALID_ARG,
+                           f"stream of cuda:{dev}, but the tensors are on cuda:{cur}")
+        return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream")
+                               else int(stream))
 
 
-def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+def _routing_dims(routing):
+    """(T, k, A, E) of a Routing or a MoeTiles."""
+    if isinstance(routing, MoeTiles):
+        return (routing.num_tokens, routing.top_k, routing.num_assignments,
+                routing.num_experts)
+    return routing.T, routing.k, routing.A, routing.E
 
 
 def moe_max_tiles(num_assignments: int, num_experts: int, tile_m: int) -> int:
@@ -165,22 +215,24 @@ def moe_unsort_workspace_bytes(num_tokens: int, top_k: int, hidden: int,
 def moe_sort_assignments(topk_ids, num_experts, sorted_ids, perm, counts, status, stream=None):
     T, k = topk_ids.shape
     A = T * k
+    a = _Call()
     _check(load().moe_sort_assignments(
-        _ptr(topk_ids, torch.int32, "topk_ids"), T, k, num_experts,
-        _ptr(sorted_ids, torch.int32, "sorted_ids", A), _ptr(perm, torch.int32, "perm", A),
-        _ptr(counts, torch.int32, "counts", num_experts), _ptr(status, torch.int32, "status", 1),
-        _stream(stream)))
+        a(topk_ids, torch.int32, "topk_ids"), T, k, num_experts,
+        a(sorted_ids, torch.int32, "sorted_ids", A), a(perm, torch.int32, "perm", A),
+        a(counts, torch.int32, "counts", num_experts), a(status, torch.int32, "status", 1),
+        a.stream(stream)))
 
 
 def moe_build_expert_tiles(sorted_ids, num_experts, tile_m, offsets, tiles, tile_count, status,
                            stream=None):
     A = sorted_ids.numel()
     max_tiles = tiles.numel() // 3
+    a = _Call()
     _check(load().moe_build_expert_tiles(
-        _ptr(sorted_ids, torch.int32, "sorted_ids"), A, num_experts, tile_m, max_tiles,
-        _ptr(offsets, torch.int32, "offsets", num_experts + 1), _ptr(tiles, torch.int32, "tiles"),
-        _ptr(tile_count, torch.int32, "tile_count", 1), _ptr(status, torch.int32, "status", 1),
-        _stream(stream)))
+        a(sorted_ids, torch.int32, "sorted_ids"), A, num_experts, tile_m, max_tiles,
+        a(offsets, torch.int32, "offsets", num_experts + 1), a(tiles, torch.int32, "tiles"),
+        a(tile_count, torch.int32, "tile_count", 1), a(status, torch.int32, "status", 1),
+        a.stream(stream)))
 
 
 def moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, sorted_ids, perm, counts, offsets,
@@ -188,39 +240,42 @@ def moe_sort_and_build_tiles(topk_ids, num_experts, tile_m, sorted_ids, perm, co
     """moe_sort_assignments + moe_build_expert_tiles in one launch (same outputs)."""
     T, k = topk_ids.shape
     A = T * k
+    a = _Call()
     _check(load().moe_sort_and_build_tiles(
-        _ptr(topk_ids, torch.int32, "topk_ids"), T, k, num_experts, tile_m, tiles.numel() // 3,
-        _ptr(sorted_ids, torch.int32, "sorted_ids", A), _ptr(perm, torch.int32, "perm", A),
-        _ptr(counts, torch.int32, "counts", num_experts),
-        _ptr(offsets, torch.int32, "offsets", num_experts + 1), _ptr(tiles, torch.int32, "tiles"),
-        _ptr(tile_count, torch.int32, "tile_count", 1), _ptr(status, torch.int32, "status", 1),
-        _stream(stream)))
+        a(topk_ids, torch.int32, "topk_ids"), T, k, num_experts, tile_m, tiles.numel() // 3,
+        a(sorted_ids, torch.int32, "sorted_ids", A), a(perm, torch.int32, "perm", A),
+        a(counts, torch.int32, "counts", num_experts),
+        a(offsets, torch.int32, "offsets", num_experts + 1), a(tiles, torch.int32, "tiles"),
+        a(tile_count, torch.int32, "tile_count", 1), a(status, torch.int32, "status", 1),
+        a.stream(stream)))
 
 
 def moe_router_topk(logits, top_k, topk_ids, topk_weights, status, stream=None):
     """Router logits [T, E] fp32 -> top-k ids (descending logit, ties to the lower id) and
     the softmax over the chosen logits."""
     T, E = logits.shape
+    a = _Call()
     _check(load().moe_router_topk(
-        _ptr(logits, torch.float32, "logits"), T, E, top_k,
-        _ptr(topk_ids, torch.int32, "topk_ids", T * top_k),
-        _ptr(topk_weights, torch.float32, "topk_weights", T * top_k),
-        _ptr(status, torch.int32, "status", 1), _stream(stream)))
+        a(logits, torch.float32, "logits"), T, E, top_k,
+        a(topk_ids, torch.int32, "topk_ids", T * top_k),
+        a(topk_weights, torch.float32, "topk_weights", T * top_k),
+        a(status, torch.int32, "status", 1), a.stream(stream)))
 
 
 def moe_route_logits(logits, top_k, tile_m, topk_ids, topk_weights, routing, stream=None):
     """moe_router_topk, then the sort and the tile builder into ``routing`` (a Routing)."""
     T, E = logits.shape
     r = routing
+    a = _Call()
     _check(load().moe_route_logits(
-        _ptr(logits, torch.float32, "logits"), T, E, top_k, tile_m, r.tiles.numel() // 3,
-        _ptr(topk_ids, torch.int32, "topk_ids", T * top_k),
-        _ptr(topk_weights, torch.float32, "topk_weights", T * top_k),
-        _ptr(r.sorted_ids, torch.int32, "sorted_ids", T * top_k),
-        _ptr(r.perm, torch.int32, "perm", T * top_k), _ptr(r.counts, torch.int32, "counts", E),
-        _ptr(r.offsets, torch.int32, "offsets", E + 1), _ptr(r.tiles, torch.int32, "tiles"),
-        _ptr(r.tile_count, torch.int32, "tile_count", 1),
-        _ptr(r.status, torch.int32, "status", 1), _stream(stream)))
+        a(logits, torch.float32, "logits"), T, E, top_k, tile_m, r.tiles.numel() // 3,
+        a(topk_ids, torch.int32, "topk_ids", T * top_k),
+        a(topk_weights, torch.float32, "topk_weights", T * top_k),
+        a(r.sorted_ids, torch.int32, "sorted_ids", T * top_k),
+        a(r.perm, torch.int32, "perm", T * top_k), a(r.counts, torch.int32, "counts", E),
+        a(r.offsets, torch.int32, "offsets", E + 1), a(r.tiles, torch.int32, "tiles"),
+        a(r.tile_count, torch.int32, "tile_count", 1),
+        a(r.status, torch.int32, "status", 1), a.stream(stream)))
 
 
 class Routing:
@@ -251,25 +306,26 @@ def _tiles_arg(routing):
     return ctypes.byref(routing.struct())
 
 
-def _bf16(t, name, numel=None):
-    return _ptr(t, torch.bfloat16, name, numel)
-
-
 def moe_gather_qmm_geglu(x, Wgu, Sgu, Bgu, routing, hidden, inter, h, variant=VARIANT_AUTO,
                          stream=None):
+    T, _, A, E = _routing_dims(routing)
+    a = _Call()
     _check(load().moe_gather_qmm_geglu(
-        _bf16(x, "x"), _ptr(Wgu, torch.int32, "Wgu"), _bf16(Sgu, "Sgu"), _bf16(Bgu, "Bgu"),
-        _tiles_arg(routing), hidden, inter, variant, _bf16(h, "h"), _stream(stream)))
+        a.bf16(x, "x", T * hidden), *a.gate_up(Wgu, Sgu, Bgu, E, hidden, inter),
+        _tiles_arg(routing), hidden, inter, variant, a.bf16(h, "h", A * inter), a.stream(stream)))
 
 
 def moe_gather_qmm_geglu_ws(x, Wgu, Sgu, Bgu, routing, hidden, inter, x_sorted_ws, h,
                             variant=VARIANT_AUTO, stream=None):
     """moe_gather_qmm_geglu with the [A, hidden] bf16 workspace of the sorted activation
     rows (used by the tensor-core variant)."""
+    T, _, A, E = _routing_dims(routing)
+    a = _Call()
     _check(load().moe_gather_qmm_geglu_ws(
-        _bf16(x, "x"), _ptr(Wgu, torch.int32, "Wgu"), _bf16(Sgu, "Sgu"), _bf16(Bgu, "Bgu"),
+        a.bf16(x, "x", T * hidden), *a.gate_up(Wgu, Sgu, Bgu, E, hidden, inter),
         _tiles_arg(routing), hidden, inter, variant,
-        _bf16(x_sorted_ws, "x_sorted_ws", routing.A * hidden), _bf16(h, "h"), _stream(stream)))
+        a.bf16(x_sorted_ws, "x_sorted_ws", A * hidden), a.bf16(h, "h", A * inter),
+        a.stream(stream)))
 
 
 def _activation(activation) -> int:
@@ -284,22 +340,27 @@ def moe_gather_qmm_glu(x, Wgu, Sgu, Bgu, routing, hidden, inter, h, activation="
                        x_sorted_ws=None, variant=VARIANT_AUTO, stream=None):
     """The gated product with either gate activation ("gelu_tanh": GeGLU, "silu": SwiGLU);
     x_sorted_ws ([A, hidden] bf16) is optional (the tensor-core variant's sorted rows)."""
+    T, _, A, E = _routing_dims(routing)
+    a = _Call()
     _check(load().moe_gather_qmm_glu(
-        _bf16(x, "x"), _ptr(Wgu, torch.int32, "Wgu"), _bf16(Sgu, "Sgu"), _bf16(Bgu, "Bgu"),
+        a.bf16(x, "x", T * hidden), *a.gate_up(Wgu, Sgu, Bgu, E, hidden, inter),
         _tiles_arg(routing), hidden, inter, variant, _activation(activation),
-        _bf16(x_sorted_ws, "x_sorted_ws", routing.A * hidden) if x_sorted_ws is not None
-        else None, _bf16(h, "h"), _stream(stream)))
+        a.bf16(x_sorted_ws, "x_sorted_ws", A * hidden) if x_sorted_ws is not None
+        else None, a.bf16(h, "h", A * inter), a.stream(stream)))
 
 
 def moe_gather_qmm_down_unsort(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y_acc_ws, y,
                                variant=VARIANT_AUTO, stream=None, deterministic=False):
     """deterministic: y_acc_ws holds one fp32 row per assignment and y is the fixed-order sum
     of each token's k rows (bit-identical from run to run)."""
+    T, k, A, E = _routing_dims(routing)
+    ws = (moe_unsort_workspace_bytes(T, k, hidden, deterministic) + 3) // 4
+    a = _Call()
     _check(load().moe_gather_qmm_down_unsort(
-        _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
-        _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
-        variant, _ptr(y_acc_ws, torch.float32, "y_acc_ws"), 1 if deterministic else 0,
-        _bf16(y, "y"), _stream(stream)))
+        a.bf16(h, "h", A * inter), *a.down(Wd, Sd, Bd, E, hidden, inter),
+        _tiles_arg(routing), a(topk_weights, torch.float32, "topk_weights", A), hidden,
+        inter, variant, a(y_acc_ws, torch.float32, "y_acc_ws", ws),
+        1 if deterministic else 0, a.bf16(y, "y", T * hidden), a.stream(stream)))
 
 
 def moe_gather_qmm_down_unsort_noalloc(h, Wd, Sd, Bd, routing, topk_weights, hidden, inter, y,
@@ -307,10 +368,12 @@ def moe_gather_qmm_down_unsort_noalloc(h, Wd, Sd, Bd, routing, topk_weights, hid
     """moe_gather_qmm_down_unsort without a workspace argument: for callers that cannot
     allocate device memory.  The accumulator is the library's built-in fixed array
     (T * hidden <= NOALLOC_MAX_Y_ELEMENTS); calls that overlap on the GPU race on it."""
+    T, _, A, E = _routing_dims(routing)
+    a = _Call()
     _check(load().moe_gather_qmm_down_unsort_noalloc(
-        _bf16(h, "h"), _ptr(Wd, torch.int32, "Wd"), _bf16(Sd, "Sd"), _bf16(Bd, "Bd"),
-        _tiles_arg(routing), _ptr(topk_weights, torch.float32, "topk_weights"), hidden, inter,
-        variant, 1 if deterministic else 0, _bf16(y, "y"), _stream(stream)))
+        a.bf16(h, "h", A * inter), *a.down(Wd, Sd, Bd, E, hidden, inter),
+        _tiles_arg(routing), a(topk_weights, torch.float32, "topk_weights", A), hidden,
+        inter, variant, 1 if deterministic else 0, a.bf16(y, "y", T * hidden), a.stream(stream)))
 
 
 class MoeLayerBuffers:
@@ -338,6 +401,18 @@ class MoeLayerBuffers:
         return self._x_sorted
 
 
+def _check_buffers(b, T, k, E, H, I, tile_m=None):
+    """Buffers reused for a call must have been made for its shapes: the routing state of
+    another T, k or E would be read with the wrong sizes."""
+    r = b.routing
+    got = (r.T, r.k, r.E, b.H, b.I) + ((r.tile_m,) if tile_m is not None else ())
+    want = (T, k, E, H, I) + ((tile_m,) if tile_m is not None else ())
+    if got != want:
+        raise MoeError(MOE_ERR_INVALID_ARG,
+                       f"buffers made for (T, k, E, H, I{', tile_m' if tile_m else ''}) = "
+                       f"{got}, the call has {want}")
+
+
 def fused_layer_fits(num_tokens, top_k, num_experts, hidden, inter, tile_m=128) -> bool:
     """Whether moe_layer_fused takes a call of this shape (the library's own host check)."""
     return load().moe_layer_fused_supported(num_tokens, top_k, num_experts, hidden, inter,
@@ -353,20 +428,25 @@ def moe_layer_fused(x, topk_ids, topk_weights, weights, num_experts, buffers, st
     I = weights["Wd"].shape[2] * 8
     A = T * k
     r, E = buffers.routing, num_experts
+    _check_buffers(buffers, T, k, E, H, I)
+    det = buffers.deterministic
+    ws = ((moe_unsort_workspace_bytes(T, k, H, True) if det else moe_workspace_bytes(T, H))
+          + 3) // 4
+    a = _Call()
     _check(load().moe_layer_fused(
-        _ptr(topk_ids, torch.int32, "topk_ids", A), _ptr(topk_weights, torch.float32,
+        a(topk_ids, torch.int32, "topk_ids", A), a(topk_weights, torch.float32,
                                                          "topk_weights", A),
-        T, k, E, _bf16(x, "x"), _ptr(weights["Wgu"], torch.int32, "Wgu"),
-        _bf16(weights["Sgu"], "Sgu"), _bf16(weights["Bgu"], "Bgu"),
-        _ptr(weights["Wd"], torch.int32, "Wd"), _bf16(weights["Sd"], "Sd"),
-        _bf16(weights["Bd"], "Bd"), H, I, r.tile_m, r.max_tiles,
-        _ptr(r.sorted_ids, torch.int32, "sorted_ids", A), _ptr(r.perm, torch.int32, "perm", A),
-        _ptr(r.counts, torch.int32, "counts", E), _ptr(r.offsets, torch.int32, "offsets", E + 1),
-        _ptr(r.tiles, torch.int32, "tiles", 3 * r.max_tiles),
-        _ptr(r.tile_count, torch.int32, "tile_count", 1), _ptr(r.status, torch.int32, "status", 1),
-        _bf16(buffers.h, "h"), _ptr(buffers.y_acc, torch.float32, "y_acc_ws"),
-        _activation(activation), 1 if buffers.deterministic else 0, _bf16(buffers.y, "y"),
-        _stream(stream)))
+        T, k, E, a.bf16(x, "x", T * H),
+        *a.gate_up(weights["Wgu"], weights["Sgu"], weights["Bgu"], E, H, I),
+        *a.down(weights["Wd"], weights["Sd"], weights["Bd"], E, H, I), H, I, r.tile_m,
+        r.max_tiles,
+        a(r.sorted_ids, torch.int32, "sorted_ids", A), a(r.perm, torch.int32, "perm", A),
+        a(r.counts, torch.int32, "counts", E), a(r.offsets, torch.int32, "offsets", E + 1),
+        a(r.tiles, torch.int32, "tiles", 3 * r.max_tiles),
+        a(r.tile_count, torch.int32, "tile_count", 1), a(r.status, torch.int32, "status", 1),
+        a.bf16(buffers.h, "h", A * I), a(buffers.y_acc, torch.float32, "y_acc_ws", ws),
+        _activation(activation), 1 if det else 0, a.bf16(buffers.y, "y", T * H),
+        a.stream(stream)))
 
 
 def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, variant=VARIANT_AUTO,
@@ -383,6 +463,8 @@ def moe_layer(x, topk_ids, topk_weights, weights, num_experts, tile_m=128, varia
     if buffers is not None and deterministic is not None and \
             bool(deterministic) != buffers.deterministic:
         raise MoeError(MOE_ERR_INVALID_ARG, "buffers were allocated for the other un-sort mode")
+    if buffers is not None:
+        _check_buffers(buffers, T, k, num_experts, H, I, tile_m)
     b = buffers or MoeLayerBuffers(T, k, num_experts, H, I, tile_m, device=x.device,
                                    deterministic=bool(deterministic))
     r = b.routing

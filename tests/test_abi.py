@@ -205,3 +205,89 @@ def test_fused_layer_host_validation(kw, code):
 def test_fused_layer_supported(shape, ok):
     assert mq.fused_layer_fits(*shape) is ok
     assert (_raw().moe_layer_fused_supported(*shape) == mq.MOE_OK) is ok
+
+
+# --- the binding's own checks (before any library call; CPU tensors suffice) ---
+
+def _cpu_weights(E, H, I, shrink=None):
+    """Tensors of the layer's weight shapes on the CPU; ``shrink`` names one to cut short."""
+    shapes = {"Wgu": (E, 2 * I, H // 8, "i"), "Sgu": (E, 2 * I, H // 64, "b"),
+              "Bgu": (E, 2 * I, H // 64, "b"), "Wd": (E, H, I // 8, "i"),
+              "Sd": (E, H, I // 64, "b"), "Bd": (E, H, I // 64, "b")}
+    out = {}
+    for name, (a, b, c, kind) in shapes.items():
+        n = a * b * c - (1 if name == shrink else 0)
+        out[name] = torch.zeros(n, dtype=torch.int32 if kind == "i" else torch.bfloat16)
+    return out
+
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.mark.parametrize("shrink", ["x", "h", "Wgu", "Sgu", "Bgu"])
+def test_binding_refuses_short_tensors_gate_up(shrink):
+    """Every tensor must hold the elements the call's shapes imply: the library takes plain
+    pointers, and a short tensor would be read or written past its end."""
+    T, k, E, H, I = 4, 2, 8, 128, 64
+    r = mq.Routing(T, k, E, 32, device="cpu")
+    w = _cpu_weights(E, H, I, shrink)
+    x = torch.zeros(T * H - (shrink == "x"), dtype=torch.bfloat16)
+    h = torch.zeros(T * k * I - (shrink == "h"), dtype=torch.bfloat16)
+    with pytest.raises(mq.MoeError) as ei:
+        mq.moe_gather_qmm_glu(x, w["Wgu"], w["Sgu"], w["Bgu"], r, H, I, h)
+    assert ei.value.status == mq.MOE_ERR_INVALID_ARG
+    assert str(ei.value).split("]")[1].strip().startswith(shrink + ":")
+    assert "elements, need" in str(ei.value)
+
+
+@pytest.mark.parametrize("shrink", ["h", "Wd", "Sd", "Bd", "topk_weights", "y_acc_ws", "y"])
+@pytest.mark.parametrize("det", [False, True])
+def test_binding_refuses_short_tensors_down(shrink, det):
+    T, k, E, H, I = 4, 2, 8, 128, 64
+    r = mq.Routing(T, k, E, 32, device="cpu")
+    w = _cpu_weights(E, H, I, shrink)
+    ws = (mq.moe_unsort_workspace_bytes(T, k, H, det) + 3) // 4
+    h = torch.zeros(T * k * I - (shrink == "h"), dtype=torch.bfloat16)
+    tw = torch.zeros(T * k - (shrink == "topk_weights"), dtype=torch.float32)
+    y_acc = torch.zeros(ws - (shrink == "y_acc_ws"), dtype=torch.float32)
+    y = torch.zeros(T * H - (shrink == "y"), dtype=torch.bfloat16)
+    with pytest.raises(mq.MoeError) as ei:
+        mq.moe_gather_qmm_down_unsort(h, w["Wd"], w["Sd"], w["Bd"], r, tw, H, I, y_acc, y,
+                                      deterministic=det)
+    assert ei.value.status == mq.MOE_ERR_INVALID_ARG
+    assert str(ei.value).split("]")[1].strip().startswith(shrink + ":")
+
+
+def test_binding_full_size_cpu_tensors_reach_the_device_check():
+    """With every size right, the first refusal is the device: nothing runs on the CPU."""
+    T, k, E, H, I = 4, 2, 8, 128, 64
+    r = mq.Routing(T, k, E, 32, device="cpu")
+    w = _cpu_weights(E, H, I)
+    x = torch.zeros(T * H, dtype=torch.bfloat16)
+    h = torch.zeros(T * k * I, dtype=torch.bfloat16)
+    with pytest.raises(mq.MoeError) as ei:
+        mq.moe_gather_qmm_glu(x, w["Wgu"], w["Sgu"], w["Bgu"], r, H, I, h)
+    assert "must be a CUDA tensor" in str(ei.value)
+
+
+@pytest.mark.parametrize("field,value", [("T", 5), ("k", 1), ("E", 16), ("H", 192), ("I", 128),
+                                         ("tile_m", 64)])
+def test_layer_refuses_buffers_of_other_shapes(field, value):
+    """Reused buffers carry the routing state of the shapes they were made for; a call of
+    other shapes would read it with the wrong sizes."""
+    dims = dict(T=4, k=2, E=8, H=128, I=64, tile_m=32)
+    b = mq.MoeLayerBuffers(dims["T"], dims["k"], dims["E"], dims["H"], dims["I"],
+                           dims["tile_m"], device="cpu")
+    dims[field] = value
+    T, k, E, H, I = (dims[n] for n in ("T", "k", "E", "H", "I"))
+    w = _cpu_weights(E, H, I)
+    w = {n: t.view(E, -1, t.numel() // (E * (2 * I if n.endswith("gu") else H)))
+         for n, t in w.items()}
+    x = torch.zeros(T, H, dtype=torch.bfloat16)
+    ids = torch.zeros(T, k, dtype=torch.int32)
+    tw = torch.zeros(T, k, dtype=torch.float32)
+    for fused in (False, True):
+        with pytest.raises(mq.MoeError) as ei:
+            mq.moe_layer(x, ids, tw, w, E, tile_m=dims["tile_m"], buffers=b, fused=fused)
+        assert ei.value.status == mq.MOE_ERR_INVALID_ARG
+        assert "buffers made for" in str(ei.value)
