@@ -75,8 +75,10 @@ typedef enum {
 /* Kernel choice for the two projection calls. */
 typedef enum {
   MOE_VARIANT_AUTO = 0, /* weight-streaming GEMV for decode-sized calls, tensor-core GEMM otherwise */
-  MOE_VARIANT_GEMV = 1, /* CUDA-core weight-streaming kernel (any size) */
-  MOE_VARIANT_TC = 2    /* tcgen05 tensor-core grouped GEMM */
+  MOE_VARIANT_GEMV = 1, /* CUDA-core weight-streaming kernel: any number of assignments,
+                           H <= 3904 and I <= 2880 */
+  MOE_VARIANT_TC = 2    /* tcgen05 tensor-core grouped GEMM: tile_m <= 128, H <= 4096 and
+                           I <= 3136 */
 } moe_variant;
 
 /* The gate activation of the gated product h = act(gate) * up. */
@@ -234,8 +236,10 @@ moe_status moe_route_logits(const float *logits, int32_t num_tokens, int32_t num
  *        u = sum_k Wu[e][n][k] x[...][k],  e = sorted_ids[s],
  *        gelu_tanh(z) = 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3)))
  *      fp32 accumulation; the GELU product in fp32; h rounded to bf16.
- * Requires H % 64 == 0 and I % 64 == 0 (MOE_ERR_UNSUPPORTED otherwise) and
- * the routing state of this layer in `tiles`.  Does nothing if *status != 0.
+ * Requires H % 64 == 0 and I % 64 == 0, and the shape within the chosen
+ * variant's limits (see moe_variant; AUTO picks a variant that takes the shape),
+ * else MOE_ERR_UNSUPPORTED before any launch; and the routing state of this
+ * layer in `tiles`.  Does nothing if *status != 0.
  */
 moe_status moe_gather_qmm_geglu(const moe_bf16_t *x, const uint32_t *Wgu, const moe_bf16_t *Sgu,
                                 const moe_bf16_t *Bgu, const moe_tiles_t *tiles, int32_t hidden,
@@ -309,8 +313,10 @@ moe_status moe_gather_qmm_glu(const moe_bf16_t *x, const uint32_t *Wgu, const mo
  * variant and sizes then give bit-identical y (Layr-Labs/mlx PR #4, the final
  * merge-readiness pass: an exact output-invariance gate).  The two variants
  * may still differ from each other in the last bits.
- * Tokens whose weights are all zero get y = 0 exactly.  Requires H % 64 == 0
- * and I % 64 == 0.  Does nothing if *status != 0.
+ * Tokens whose weights are all zero get y = 0 exactly.  Requires H % 64 == 0,
+ * I % 64 == 0 and the shape within the chosen variant's limits (see
+ * moe_variant), else MOE_ERR_UNSUPPORTED before any launch.  Does nothing if
+ * *status != 0.
  */
 moe_status moe_gather_qmm_down_unsort(const moe_bf16_t *h, const uint32_t *Wd,
                                       const moe_bf16_t *Sd, const moe_bf16_t *Bd,

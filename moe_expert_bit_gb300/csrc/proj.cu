@@ -74,14 +74,14 @@ static moe_status resolve_variant(const char *fn, const moe_tiles_t *t, int32_t 
                                   int32_t *variant) {
   const bool tc_ok = tc_supported(H, I, t->tile_m) == MOE_OK;
   if (*variant == MOE_VARIANT_TC && !tc_ok) {
-    set_error("%s: tensor-core variant supports tile_m <= 128 and H, I <= 4096 "
+    set_error("%s: tensor-core variant supports tile_m <= 128, H <= 4096 and I <= 3136 "
               "(got tile_m=%d H=%d I=%d)", fn, t->tile_m, H, I);
     return MOE_ERR_UNSUPPORTED;
   }
   const bool gemv_ok = gemv_supported(H, I);
   if (*variant == MOE_VARIANT_GEMV && !gemv_ok) {
-    set_error("%s: weight-streaming variant needs its shared-memory tile to fit (H=%d I=%d)", fn,
-              H, I);
+    set_error("%s: weight-streaming variant supports H <= 3904 and I <= 2880 (got H=%d I=%d)",
+              fn, H, I);
     return MOE_ERR_UNSUPPORTED;
   }
   if (*variant == MOE_VARIANT_AUTO) {

@@ -291,3 +291,33 @@ def test_layer_refuses_buffers_of_other_shapes(field, value):
             mq.moe_layer(x, ids, tw, w, E, tile_m=dims["tile_m"], buffers=b, fused=fused)
         assert ei.value.status == mq.MOE_ERR_INVALID_ARG
         assert "buffers made for" in str(ei.value)
+
+
+@pytest.mark.parametrize("H,I,variant,limit", [
+    (3968, 64, mq.VARIANT_GEMV, "H <= 3904"),     # a padded weight row beyond one TMA box
+    (64, 2944, mq.VARIANT_GEMV, "I <= 2880"),     # fewer than two down ring buffers fit
+    (4160, 64, mq.VARIANT_TC, "H <= 4096"),       # beyond the GEMM's reduction length
+    (64, 3200, mq.VARIANT_TC, "I <= 3136"),       # the down kernel's shared memory
+    (4160, 64, mq.VARIANT_AUTO, "no kernel variant"),
+    (64, 3200, mq.VARIANT_AUTO, "no kernel variant"),
+])
+def test_variant_size_limits_are_refused_before_a_launch(H, I, variant, limit):
+    """Each variant's largest sizes (the GPU tests run the largest accepted ones); one step of
+    64 beyond is refused on the host with MOE_ERR_UNSUPPORTED and a message naming it."""
+    t = _tiles()
+    lib = _raw()
+    assert lib.moe_gather_qmm_geglu(16, 16, 16, 16, ctypes.byref(t), H, I, variant, 16,
+                                    NULL) == mq.MOE_ERR_UNSUPPORTED
+    assert limit in lib.moe_last_error_string().decode()
+    for det in (0, 1):
+        assert lib.moe_gather_qmm_down_unsort(16, 16, 16, 16, ctypes.byref(t), 16, H, I,
+                                              variant, 16, det, 16, NULL) == \
+            mq.MOE_ERR_UNSUPPORTED
+        assert limit in lib.moe_last_error_string().decode()
+
+
+def test_tensor_core_variant_refuses_tiles_above_128_rows():
+    t = _tiles(tile_m=256, max_tiles=8)
+    assert _raw().moe_gather_qmm_geglu(16, 16, 16, 16, ctypes.byref(t), 128, 64,
+                                       mq.VARIANT_TC, 16, NULL) == mq.MOE_ERR_UNSUPPORTED
+    assert "tile_m <= 128" in _raw().moe_last_error_string().decode()
