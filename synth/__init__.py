@@ -237,3 +237,33 @@ def make_custom(E: int, H: int, I: int, T: int, k: int, seed: int = 0,
                 topk_ids=ids, topk_weights=tw, router_logits=scores.astype(np.float32),
                 outlier_rows=np.zeros(0, np.int32),
                 Wgu=Wgu, Sgu=Sgu, Bgu=Bgu, Wd=Wd, Sd=Sd, Bd=Bd)
+
+
+def activation_grid(z_bits: np.ndarray, H: int = 64) -> dict:
+    """A one-token, one-expert layer whose gate pre-activations are the given bf16 values.
+
+    x = e_0 (1.0 in column 0 of an H-wide row, H a multiple of 64).  Every gate row n holds the 4-bit code 1 at
+    column 0 and 0 elsewhere, with scale z_n and bias 0; every up row the code 1 at column 0
+    with scale 1.0 and bias 0.  So the gate pre-activation of row n is z_n and its up
+    pre-activation 1.0, exactly in any precision, and h[n] is the gate activation at z_n
+    alone.  The down weights are all zero.  ``z_bits``: bf16 bit patterns (uint16), a
+    multiple of 64 of them (the intermediate size).
+    """
+    z_bits = np.ascontiguousarray(z_bits, np.uint16)
+    I = int(z_bits.size)
+    if I % 64 or I == 0 or H % 64 or H == 0:
+        raise ValueError("the grid needs a positive multiple of 64 values and of 64 columns")
+    one = np.uint16(0x3F80)  # bf16 1.0
+    Wgu = np.zeros((1, 2 * I, H // 8), np.uint32)
+    Wgu[0, :, 0] = 1  # code 1 in the low nibble: column 0
+    Sgu = np.zeros((1, 2 * I, H // 64), np.uint16)
+    Sgu[0, :I, 0] = z_bits
+    Sgu[0, I:, 0] = one
+    x = np.zeros((1, H), np.uint16)
+    x[0, 0] = one
+    return dict(name=f"activation_grid_I{I}", E=1, H=H, I=I, T=1, k=1, x=x,
+                topk_ids=np.zeros((1, 1), np.int32), topk_weights=np.ones((1, 1), np.float32),
+                router_logits=np.zeros((1, 1), np.float32), outlier_rows=np.zeros(0, np.int32),
+                Wgu=Wgu, Sgu=Sgu, Bgu=np.zeros_like(Sgu),
+                Wd=np.zeros((1, H, I // 8), np.uint32), Sd=np.zeros((1, H, I // 64), np.uint16),
+                Bd=np.zeros((1, H, I // 64), np.uint16))

@@ -39,3 +39,9 @@ def excess(gpu: np.ndarray, ref: np.ndarray, rowwise: np.ndarray | None = None) 
         rowmax = np.maximum(1.0, np.abs(ref).max(axis=1, keepdims=True))
         scale = np.where(np.asarray(rowwise)[:, None], rowmax, scale)
     return float(np.max(np.abs(gpu - ref) / (REL * scale))) if gpu.size else 0.0
+
+
+def bf16_bits(v) -> np.ndarray:
+    """float -> bf16 bit patterns (uint16), round to nearest even (finite inputs)."""
+    u = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)

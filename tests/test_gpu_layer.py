@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from _util import REL, bf16_to_f64, excess, to_device
+from _util import bf16_bits, bf16_to_f64, excess, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -164,14 +164,35 @@ def test_bad_routing_leaves_outputs_untouched(variant):
     assert bool((b.h.float() == 7.0).all()) and bool((b.y.float() == -3.0).all())
 
 
-def test_gelu_hardware_tanh_against_libm():
-    """The GeGLU epilogue's tanh (tanh.approx.f32) stays within its error bound of std::tanh:
-    checked through the layer on a workload whose gate values span [-8, 8]."""
-    d = synth.make("tiny")
-    b = run_layer(d, 32, mq.VARIANT_GEMV)
-    ref = oracle.layer(d)
-    assert excess(bf16_to_f64(b.h), ref["h"]) <= 0.5  # well inside the 2e-2 bound
-    assert REL == 2e-2
+# The kernels compute both gate activations as 0.5 z (1 + tanh(u)) in fp32 on the hardware
+# tanh (tanh.approx.f32, relative error about 2^-11): 1 + tanh(u) is then off by ~2^-11 and
+# the activation by ~2^-12 |z|, before h is rounded to bf16 (half an ulp: 2^-9 relative).
+# Bounds with a margin of 4 and 2: ACT_ABS x |z| + ACT_REL x |act(z)|.
+ACT_ABS = 2.0 ** -10
+ACT_REL = 2.0 ** -8
+
+
+@pytest.mark.parametrize("activation", ["gelu_tanh", "silu"])
+@pytest.mark.parametrize("path", ["gemv", "tc", "fused"])
+def test_gate_activation_pointwise_on_a_grid(activation, path):
+    """Each kernel's gate activation at 512 bf16 values in [-12, 12], through the whole layer
+    on the grid workload (the gate pre-activation of h[n] is exactly z_n, its up
+    pre-activation exactly 1), against the fp64 activation."""
+    if path == "tc":
+        _variant_or_skip(mq.VARIANT_TC)
+    bits = bf16_bits(np.linspace(-12.0, 12.0, 512))
+    d = synth.activation_grid(bits, H=128)
+    dev = to_device(d)
+    variant = {"gemv": mq.VARIANT_GEMV, "tc": mq.VARIANT_TC, "fused": mq.VARIANT_AUTO}[path]
+    b = mq.moe_layer(dev["x"], dev["topk_ids"], dev["topk_weights"], dev, 1, tile_m=128,
+                     variant=variant, fused=path == "fused", activation=activation)
+    torch.cuda.synchronize()
+    assert int(b.routing.status.item()) == 0
+    z = synth.bf16_bits_to_f64(bits)
+    ref = (oracle.gelu_tanh if activation == "gelu_tanh" else oracle.silu)(z)
+    h = bf16_to_f64(b.h)[0]
+    assert np.all(np.abs(h - ref) <= ACT_REL * np.abs(ref) + ACT_ABS * np.abs(z))
+    assert not bool(torch.any(b.y != 0))
 
 
 @pytest.mark.parametrize("case", ["custom", "prefill_skewed"])

@@ -1,8 +1,10 @@
 """The seeded input generator: determinism and the workload properties it promises."""
 import numpy as np
+import pytest
 
 import oracle
 import synth
+from _util import bf16_bits
 
 
 def test_counter_generator_is_deterministic_and_streams_differ():
@@ -43,3 +45,18 @@ def test_zipf_router_leaves_at_least_eight_experts_empty():
     assert counts.sum() == 16384
     assert counts.max() > 8 * counts[counts > 0].min()  # heavy head
     assert all(len(set(r.tolist())) == 8 for r in ids)
+
+
+@pytest.mark.parametrize("activation", ["gelu_tanh", "silu"])
+def test_activation_grid_isolates_the_gate_activation(activation):
+    """The grid layer's gate pre-activations are the given values and its up ones 1.0, so the
+    oracle's h is the activation at those values alone (exactly), and y is zero."""
+    bits = bf16_bits(np.linspace(-12.0, 12.0, 128))
+    d = synth.activation_grid(bits)
+    ref = oracle.layer(d, activation=activation)
+    z = synth.bf16_bits_to_f64(bits)
+    f = oracle.gelu_tanh if activation == "gelu_tanh" else oracle.silu
+    assert np.array_equal(ref["h"][0], f(z))
+    assert not np.any(ref["y"])
+    with pytest.raises(ValueError):
+        synth.activation_grid(bits[:100])
