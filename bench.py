@@ -22,6 +22,15 @@ scaling, value = all ranks' assignments / the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this
 method has here) on the host cores, on a bounded sample of the workload.
+
+Keys of the line beyond the common ones: ``step_us_spread`` (min, median and
+max of the K step times), ``weight_GBps`` and ``TFLOPs`` (touched weight bytes
+and layer FLOPs per step time), ``layer_roofline`` (the step against
+max(weight bytes / HBM peak, FLOPs / bf16 peak)), ``kernels_us`` (the
+breakdown pass), ``roofline`` (the dominant kernel: algorithmic bytes per
+launch / its duration, with the committed ncu DRAM bytes as ``traffic``),
+``e2e`` (through the public calls with host buffers), ``clocks`` (nvidia-smi
+samples during the timed passes), ``gpu_launches`` and ``cpu_baseline``.
 """
 from __future__ import annotations
 
