@@ -44,6 +44,11 @@
  *     Every kernel reads the status word first and does nothing if it is not
  *     0, so a later call on the same stream is a no-op; the caller reads the
  *     word whenever it synchronises.  No kernel traps or asserts.
+ *   - A workspace and a routing state belong to one call at a time.  Calls
+ *     that share them must be ordered on the GPU (one stream, or events
+ *     between streams); calls that may run concurrently need their own.
+ *     The down call leaves its workspace zeroed for the next call, and the
+ *     one-launch layer keeps a count of its calls there.
  *   - Index type is int32 (values stay below 2^31).
  *   - Flat assignment index: a = t * top_k + j for token t and choice j.
  *   - No exception crosses the ABI.
